@@ -1,0 +1,263 @@
+"""Python access to the SPIN decode-step oracle (``spin_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``. The product path never loads it.
+
+The oracle shares no code with the CUDA library; both take their inputs from
+the ``workload`` generator. See ``spin_oracle.c`` for the page citations and
+the readings taken where the pages leave a rule open.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+D = 128
+PART = 64
+PAGE_ELEMS = 2 * PART * D
+
+
+def build(force: bool = False, out: Optional[str] = None, defines=()) -> str:
+    """Compile spin_oracle.c into a shared library (gcc, OpenMP when available)."""
+    src = os.path.join(_HERE, "spin_oracle.c")
+    dst = out or _LIB_PATH
+    if not force and out is None and os.path.exists(dst) and os.path.getmtime(dst) >= os.path.getmtime(src):
+        return dst
+    extra = [f"-D{d}" for d in defines]
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-ffp-contract=off", "-std=c11"] + extra + [src, "-o", dst + ".tmp",
+                                                                                             "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True)
+    os.replace(dst + ".tmp", dst)
+    return dst
+
+
+class ManageOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("hits", "misses", "resident_before", "free_before", "demand", "cutoff", "evicted", "error")]
+
+
+class StepIO(ctypes.Structure):
+    _fields_ = [
+        ("summ", ctypes.c_void_p),
+        ("host_pages", ctypes.c_void_p),
+        ("q", ctypes.c_void_p),
+        ("G", ctypes.c_int32),
+        ("k", ctypes.c_int32),
+        ("t", ctypes.c_int32),
+        ("scores", ctypes.c_void_p),
+        ("sel", ctypes.c_void_p),
+        ("sel_slot", ctypes.c_void_p),
+        ("sel_hit", ctypes.c_void_p),
+        ("victims", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("mo", ManageOut),
+        ("keff", ctypes.c_int32),
+    ]
+
+
+def _bind(L):
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.oracle_index.argtypes = [vp, i64, vp]
+    L.oracle_offload.argtypes = [vp, vp, i64, vp]
+    L.oracle_scores.argtypes = [vp, i64, vp, i32, vp]
+    L.oracle_topk.argtypes = [vp, i64, i32, vp]
+    L.oracle_topk.restype = i32
+    L.oracle_unit_create.argtypes = [i32, i32]
+    L.oracle_unit_create.restype = vp
+    L.oracle_unit_destroy.argtypes = [vp]
+    L.oracle_resolve.argtypes = [vp, i32]
+    L.oracle_resolve.restype = i32
+    L.oracle_live_segments.argtypes = [vp]
+    L.oracle_live_segments.restype = i32
+    L.oracle_manage.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, ctypes.POINTER(ManageOut)]
+    L.oracle_attend.argtypes = [vp, vp, vp, i32, vp, i32, vp]
+    L.oracle_step_unit.argtypes = [vp, ctypes.POINTER(StepIO)]
+    L.oracle_step_units.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(StepIO), i32, i32]
+    L.oracle_step_units.restype = i32
+    L.oracle_unit_export.argtypes = [vp, vp, vp, vp]
+    L.oracle_unit_slot.argtypes = [vp, i32]
+    L.oracle_unit_slot.restype = vp
+    return L
+
+
+def load(path: Optional[str] = None):
+    """The oracle library (built on first use). `path` loads another build (mutation tests)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(ctypes.CDLL(_LIB_PATH))
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"], "arrays passed to the oracle must be C-contiguous"
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+# ---------------------------------------------------------------------------
+# Stateless pieces
+# ---------------------------------------------------------------------------
+
+def index(k_bits: np.ndarray, lib=None) -> np.ndarray:
+    """Partition mean keys, double [P][128], from bf16 bits K [ntok][128]."""
+    lib = lib or load()
+    k_bits = np.ascontiguousarray(k_bits, np.uint16)
+    n = k_bits.shape[0]
+    P = (n + PART - 1) // PART
+    s = np.empty((P, D), np.float64)
+    lib.oracle_index(_p(k_bits), n, _p(s))
+    return s
+
+
+def offload(k_bits: np.ndarray, v_bits: np.ndarray, lib=None) -> np.ndarray:
+    """Host pages [P][2][64][128] bf16 bits (zero padded)."""
+    lib = lib or load()
+    k_bits = np.ascontiguousarray(k_bits, np.uint16)
+    v_bits = np.ascontiguousarray(v_bits, np.uint16)
+    n = k_bits.shape[0]
+    P = (n + PART - 1) // PART
+    pages = np.empty((P, 2, PART, D), np.uint16)
+    lib.oracle_offload(_p(k_bits), _p(v_bits), n, _p(pages))
+    return pages
+
+
+def scores(summ: np.ndarray, q_bits: np.ndarray, lib=None) -> np.ndarray:
+    lib = lib or load()
+    summ = np.ascontiguousarray(summ, np.float64)
+    q_bits = np.ascontiguousarray(q_bits, np.uint16)
+    sc = np.empty(summ.shape[0], np.float64)
+    lib.oracle_scores(_p(summ), summ.shape[0], _p(q_bits), q_bits.shape[0], _p(sc))
+    return sc
+
+
+def topk(sc: np.ndarray, k: int, lib=None) -> np.ndarray:
+    lib = lib or load()
+    sc = np.ascontiguousarray(sc, np.float64)
+    sel = np.empty(max(k, 1), np.int32)
+    keff = lib.oracle_topk(_p(sc), sc.shape[0], k, _p(sel))
+    return sel[:keff].copy()
+
+
+# ---------------------------------------------------------------------------
+# Stateful unit
+# ---------------------------------------------------------------------------
+
+class Unit:
+    """Oracle page state of one (request, layer, KV head) unit."""
+
+    def __init__(self, ntok: int, cap: int, k_bits: Optional[np.ndarray] = None,
+                 v_bits: Optional[np.ndarray] = None, lib=None):
+        self.lib = lib or load()
+        self.ntok = ntok
+        self.cap = cap
+        self.P = (ntok + PART - 1) // PART
+        self.h = self.lib.oracle_unit_create(ntok, cap)
+        self.summ = None
+        self.host_pages = None
+        if k_bits is not None:
+            self.load_kv(k_bits, v_bits)
+
+    def load_kv(self, k_bits: np.ndarray, v_bits: np.ndarray):
+        """Index + Offload of this unit's keys and values."""
+        assert k_bits.shape[0] == self.ntok
+        self.summ = index(k_bits, self.lib)
+        self.host_pages = offload(k_bits, v_bits, self.lib)
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            self.lib.oracle_unit_destroy(h)
+            self.h = None
+
+    def resolve(self, p: int) -> int:
+        return self.lib.oracle_resolve(self.h, p)
+
+    def live_segments(self) -> int:
+        return self.lib.oracle_live_segments(self.h)
+
+    def export(self):
+        sp = np.empty(self.cap, np.int32)
+        lu = np.empty(self.cap, np.int32)
+        rs = np.empty(max(self.P, 1), np.int32)
+        self.lib.oracle_unit_export(self.h, _p(sp), _p(lu), _p(rs))
+        return sp, lu, rs[:self.P]
+
+    def slot_page(self, s: int) -> np.ndarray:
+        ptr = self.lib.oracle_unit_slot(self.h, s)
+        buf = (ctypes.c_uint16 * PAGE_ELEMS).from_address(ptr)
+        return np.frombuffer(buf, np.uint16).copy().reshape(2, PART, D)
+
+    def manage(self, sel: np.ndarray, t: int):
+        sel = np.ascontiguousarray(sel, np.int32)
+        k = sel.shape[0]
+        sel_slot = np.empty(max(k, 1), np.int32)
+        sel_hit = np.empty(max(k, 1), np.uint8)
+        victims = np.empty(self.cap, np.int32)
+        mo = ManageOut()
+        self.lib.oracle_manage(self.h, _p(sel), k, t, _p(self.host_pages), _p(sel_slot), _p(sel_hit), _p(victims),
+                               ctypes.byref(mo))
+        return sel_slot[:k].copy(), sel_hit[:k].astype(bool), victims[:mo.evicted].copy(), mo
+
+    def attend(self, sel: np.ndarray, sel_slot: np.ndarray, q_bits: np.ndarray) -> np.ndarray:
+        sel = np.ascontiguousarray(sel, np.int32)
+        sel_slot = np.ascontiguousarray(sel_slot, np.int32)
+        q_bits = np.ascontiguousarray(q_bits, np.uint16)
+        G = q_bits.shape[0]
+        out = np.empty((G, D), np.float64)
+        self.lib.oracle_attend(self.h, _p(sel), _p(sel_slot), sel.shape[0], _p(q_bits), G, _p(out))
+        return out
+
+    def step(self, q_bits: np.ndarray, k: int, t: int) -> dict:
+        """Select -> Manage/Retrieve -> Attention for one decode step."""
+        q_bits = np.ascontiguousarray(q_bits, np.uint16)
+        G = q_bits.shape[0]
+        sc = np.empty(max(self.P, 1), np.float64)
+        sel = np.empty(max(k, 1), np.int32)
+        sel_slot = np.empty(max(k, 1), np.int32)
+        sel_hit = np.empty(max(k, 1), np.uint8)
+        victims = np.empty(self.cap, np.int32)
+        out = np.empty((G, D), np.float64)
+        io = StepIO(self.summ.ctypes.data, self.host_pages.ctypes.data, q_bits.ctypes.data, G, k, t,
+                    sc.ctypes.data, sel.ctypes.data, sel_slot.ctypes.data, sel_hit.ctypes.data,
+                    victims.ctypes.data, out.ctypes.data)
+        self.lib.oracle_step_unit(self.h, ctypes.byref(io))
+        keff = io.keff
+        return dict(scores=sc[:self.P].copy(), sel=sel[:keff].copy(), sel_slot=sel_slot[:keff].copy(),
+                    sel_hit=sel_hit[:keff].astype(bool), victims=victims[:io.mo.evicted].copy(), out=out,
+                    mo=io.mo)
+
+
+def step_units_parallel(units, qs, k: int, t: int, threads: int = 0, lib=None):
+    """Run one decode step on many units with the oracle's thread pool; returns threads used."""
+    lib = lib or load()
+    n = len(units)
+    handles = (ctypes.c_void_p * n)(*[u.h for u in units])
+    ios = (StepIO * n)()
+    keep = []
+    for i, (u, q) in enumerate(zip(units, qs)):
+        q = np.ascontiguousarray(q, np.uint16)
+        sel = np.empty(max(k, 1), np.int32)
+        ss = np.empty(max(k, 1), np.int32)
+        sh = np.empty(max(k, 1), np.uint8)
+        out = np.empty((q.shape[0], D), np.float64)
+        keep.append((q, sel, ss, sh, out))
+        ios[i] = StepIO(u.summ.ctypes.data, u.host_pages.ctypes.data, q.ctypes.data, q.shape[0], k, t, None,
+                        sel.ctypes.data, ss.ctypes.data, sh.ctypes.data, None, out.ctypes.data)
+    used = lib.oracle_step_units(handles, ios, n, threads)
+    return used, keep
