@@ -1,0 +1,195 @@
+/*
+ * spin.h — C ABI of the GB300 (sm_103a) SPIN sparse-decode data path.
+ *
+ * The library implements, per decode step and per layer, the data path of SPIN
+ * ("Unifying Sparse Attention with Hierarchical Memory for Scalable Long-Context
+ * LLM Serving", arXiv 2604.26837) over a page-based, per-KV-head KV store split
+ * between HBM and pinned host memory:
+ *   Select   score every partition summary against the query, per-KV-head top-k;
+ *   Resolve  look the selected partitions up in a two-level page table;
+ *   Evict    bucketed LRU when the free pages do not cover the misses;
+ *   Retrieve copy the missing pages host -> HBM;
+ *   Attend   exact softmax attention over the selected tokens only.
+ * Page citations: m.x-techcon.com "吞吐量提升5.66倍！微软、港中大等Spin框架如何统一稀疏注意力
+ * 与分级内存…" (below [XT]), section "Spin的核心设计" 1-3, Figures 3, 5, 6; and
+ * gist.science/pt "Unifying Sparse Attention with Hierarchical Memory…" (below [GS]),
+ * section 2 A-C.
+ *
+ * Fixed geometry: head_dim 128, partition = page = 64 tokens of one KV head,
+ * second-level segment = 64 directory-adjacent partitions, 64 LRU buckets.
+ * A page is stored as K[64][128] then V[64][128], bf16 (uint16 bits),
+ * token-major, zero padded past the last valid token: 32768 bytes.
+ *
+ * Units. A unit is one (request b, layer l, KV head h). Query head hq belongs to
+ * KV head hq / G with G = q_heads / kv_heads (grouped-query attention).
+ *
+ * Ownership. The caller owns every pointer it passes (queries, outputs, KV
+ * sources, streams, host buffers of the debug calls). The library owns, from
+ * spin_create to spin_destroy: the HBM page pool, the two-level tables, the
+ * partition summaries, the pinned host page store, per-layer scratch, its
+ * internal streams and events. KV sources passed to spin_index_offload are
+ * copied and may be freed when that call's stream work has completed.
+ *
+ * Errors. Every int-returning call returns a spin_status. No call throws, traps
+ * or aborts. Kernels report device-side conditions (pool exhausted, a bounded
+ * wait that ran out) through a device error word that the next synchronising
+ * call (spin_stats, spin_debug_*) turns into a status; after a device error the
+ * context keeps returning that status. spin_last_error(ctx) gives a message
+ * (spin_last_error(NULL) the message of the last failed spin_create).
+ *
+ * Threading. A context may be used from one host thread at a time. Decode
+ * steps of different layers may be enqueued on different streams; the steps of
+ * one layer must be ordered on one stream.
+ */
+#ifndef SPIN_H_
+#define SPIN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPIN_HEAD_DIM 128
+#define SPIN_PART_TOKENS 64
+#define SPIN_SEG_ENTRIES 64
+#define SPIN_LRU_BUCKETS 64
+#define SPIN_PAGE_BYTES 32768
+#define SPIN_MAX_GROUP 16
+
+typedef struct spin_ctx spin_ctx;
+typedef void* spin_stream_t; /* a cudaStream_t; NULL = the legacy default stream */
+
+typedef enum spin_status {
+  SPIN_OK = 0,
+  SPIN_ERR_INVALID = 1,  /* bad argument or configuration; nothing was enqueued */
+  SPIN_ERR_CUDA = 2,     /* a CUDA runtime call failed (no device, launch failure …) */
+  SPIN_ERR_OOM = 3,      /* a device or pinned host allocation failed */
+  SPIN_ERR_CAPACITY = 4, /* the shared segment pool ran out during a step */
+  SPIN_ERR_TIMEOUT = 5,  /* a bounded device-side wait ran out */
+  SPIN_ERR_STATE = 6     /* call out of order (e.g. decode before every request was offloaded) */
+} spin_status;
+
+typedef enum spin_flags {
+  SPIN_FLAG_STAGE_TIMING = 1u << 0, /* record CUDA events around every stage; read via spin_stats */
+  SPIN_FLAG_NO_GRAPH = 1u << 1,     /* launch the step's kernels directly instead of replaying a CUDA graph */
+  SPIN_FLAG_TEST_FAIL_PINNED = 1u << 16 /* test hook: the pinned host allocation reports failure */
+} spin_flags;
+
+/* Configuration of one context. All counts are per context. */
+typedef struct spin_config {
+  int32_t batch;             /* B >= 1 requests */
+  int32_t layers;            /* L >= 1 */
+  int32_t q_heads;           /* Hq; Hq % Hkv == 0 and Hq / Hkv <= SPIN_MAX_GROUP */
+  int32_t kv_heads;          /* Hkv >= 1 */
+  int32_t head_dim;          /* must be 128 */
+  int32_t part_tokens;       /* must be 64 */
+  int32_t topk;              /* k >= 1 partitions selected per unit per step, <= 512 */
+  int32_t buf_mult;          /* resident capacity per unit = buf_mult * topk pages (mandatory + buffer), >= 1 */
+  const int64_t* ctx_len;    /* [batch] tokens per request, >= 0 (host pointer, copied) */
+  int32_t seg_entries;       /* 0 or 64 */
+  int64_t seg_pool_segments; /* segments in the shared second-level pool; 0 = enough for any page state */
+  int32_t device;            /* CUDA device ordinal */
+  uint32_t flags;            /* spin_flags */
+} spin_config;
+
+/* Counters since spin_create. */
+typedef struct spin_stats_t {
+  int64_t steps;             /* completed decode-step calls (one per layer) */
+  int64_t hits;              /* selected pages found resident */
+  int64_t misses;            /* selected pages retrieved from host */
+  int64_t evictions;         /* pages reclaimed by the bucketed LRU */
+  int64_t lru_rounds;        /* unit-steps that ran the LRU */
+  int64_t retrieved_bytes;   /* misses * SPIN_PAGE_BYTES */
+  int64_t selected_bytes;    /* selected pages * SPIN_PAGE_BYTES (bytes attention read) */
+  int64_t live_segments;     /* second-level segments currently allocated */
+  int64_t pool_segments;     /* segments in the shared pool */
+  int64_t metadata_bytes;    /* HBM bytes of the page metadata: directory + segment pool + per-page state */
+  int64_t flat_table_bytes;  /* HBM bytes of a flat [unit][max partitions] table plus the same per-page state */
+  int64_t hbm_pool_bytes;    /* HBM page pool */
+  int64_t host_store_bytes;  /* pinned host page store */
+  int64_t summary_bytes;     /* HBM partition summaries (fp32) */
+  int64_t timed_calls;       /* decode calls with stage timing */
+  double ms_select;          /* summed stage times (SPIN_FLAG_STAGE_TIMING), milliseconds */
+  double ms_manage;
+  double ms_retrieve;
+  double ms_attention;
+  double ms_combine;
+  uint32_t device_error;     /* raw device error word (0 = none) */
+} spin_stats_t;
+
+/* Host-side view filled by spin_debug_export; any pointer may be NULL. Shapes use
+ * U = batch * kv_heads units of the layer (unit ul = b * kv_heads + h), k = topk,
+ * cap = buf_mult * topk, Pmax = the largest partition count of any request. */
+typedef struct spin_state_view {
+  int32_t* keff;       /* [U] partitions selected in the last step = min(k, P_b) */
+  int32_t* sel;        /* [U][k] selected partitions of the last step, ascending, -1 padded */
+  int32_t* sel_slot;   /* [U][k] slot (0..cap-1) holding each selected partition */
+  uint8_t* sel_hit;    /* [U][k] 1 when the partition was resident before the step */
+  int32_t* slot_part;  /* [U][cap] partition held by each slot, -1 = free */
+  int32_t* last_use;   /* [U][cap] step of each slot's last use */
+  int32_t* resolve;    /* [U][Pmax] slot found by the two-level walk, -1 = not resident */
+  int32_t* live_segs;  /* [U] second-level segments the unit holds */
+  int32_t* unit_info;  /* [U][8] last step: hits, misses, resident before, demand, cutoff (-1 none), evicted, step, 0 */
+  float* scores;       /* [U][Pmax] fp32 scores of the last step (entries >= P_b undefined) */
+} spin_state_view;
+
+/* Create a context: validates cfg, allocates the pinned host page store
+ * (sum_b ceil(ctx_len[b]/64) * L * Hkv pages), the HBM page pool (B*L*Hkv*cap
+ * pages), the summaries, the two-level tables (directory [units][ceil(Pmax/64)],
+ * shared segment pool) and per-layer scratch, on cfg->device. Every page starts
+ * on the host and the GPU holds nothing. *out is set only on SPIN_OK. */
+int spin_create(const spin_config* cfg, spin_ctx** out);
+
+/* Index + Offload ([XT] §1, Fig 3; [GS] §2A) of request b in `layer`:
+ * k, v: bf16 [kv_heads][n_tokens][128], row-major; n_tokens must equal
+ * cfg->ctx_len[b]. src_is_host != 0: k and v are host pointers (pinned or
+ * pageable); 0: device pointers on the context's device. Computes the fp32 mean
+ * key of every partition (the partition summary) and writes every page into the
+ * pinned host store. Asynchronous on `stream`. */
+int spin_index_offload(spin_ctx* ctx, int32_t b, int32_t layer, const uint16_t* k, const uint16_t* v,
+                       int64_t n_tokens, int32_t src_is_host, spin_stream_t stream);
+
+/* One decode step of one layer for the whole batch ([XT] §2 and Fig 5 steps 1-4,
+ * §3; [GS] §2B-C). q: device bf16 [batch][q_heads][128]; out: device fp32
+ * [batch][q_heads][128] = softmax(q K_sel^T / sqrt(128)) V_sel over the tokens of
+ * the k selected partitions of the query head's KV head (zeros for an empty
+ * request). Asynchronous on `stream`; the layer's step counter t advances by one
+ * per call. Requires every request of `layer` to have been offloaded. */
+int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream);
+
+/* The same step with host buffers: q_host [batch][q_heads][128] bf16 and
+ * out_host [batch][q_heads][128] fp32 (pinned for asynchronous copies). The
+ * host->device copy of q, the step and the device->host copy of out are all
+ * enqueued on `stream`; out_host is valid once the stream has reached that point. */
+int spin_decode_step_host(spin_ctx* ctx, int32_t layer, const uint16_t* q_host, float* out_host,
+                          spin_stream_t stream);
+
+/* Synchronises the context's device work and fills *out. Returns the device
+ * error status if a kernel reported one. */
+int spin_stats(spin_ctx* ctx, spin_stats_t* out);
+
+/* Synchronises, then copies the page state and last-step selection of `layer`
+ * into the caller's host buffers (parity testing and inspection). */
+int spin_debug_export(spin_ctx* ctx, int32_t layer, spin_state_view* view);
+
+/* Synchronises, then copies the 32768-byte HBM page in slot `slot` of unit
+ * (layer, b, h) to dst (host). */
+int spin_debug_read_page(spin_ctx* ctx, int32_t layer, int32_t b, int32_t h, int32_t slot, uint16_t* dst);
+
+/* Synchronises, then copies the fp32 summaries [P_b][128] of unit (layer, b, h) to dst (host). */
+int spin_debug_summaries(spin_ctx* ctx, int32_t layer, int32_t b, int32_t h, float* dst);
+
+/* Releases everything the context owns (synchronises first). NULL is a no-op. */
+void spin_destroy(spin_ctx* ctx);
+
+/* Message of the last failure on ctx (or of the last failed spin_create when
+ * ctx is NULL). The string lives until the next call on the same context. */
+const char* spin_last_error(const spin_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPIN_H_ */

@@ -1,0 +1,114 @@
+"""A Python handle around one spin_ctx (marshalling only; every step runs in libspin.so).
+
+PyTorch supplies device memory and streams; numpy supplies host buffers.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import numpy as np
+
+from . import _binding as B
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+class SpinContext:
+    """Owns one library context: configuration, offload, decode steps, stats, state export."""
+
+    def __init__(self, batch: int, layers: int, q_heads: int, kv_heads: int, ctx_len: Sequence[int], topk: int,
+                 buf_mult: int, device: int = 0, seg_pool_segments: int = 0, flags: int = 0):
+        self.B, self.L, self.Hq, self.Hkv = batch, layers, q_heads, kv_heads
+        self.G = q_heads // kv_heads
+        self.ctx_len = [int(x) for x in ctx_len]
+        self.k, self.buf_mult = topk, buf_mult
+        self.cap = topk * buf_mult
+        self.P = [(n + B.PART_TOKENS - 1) // B.PART_TOKENS for n in self.ctx_len]
+        self.P_max = max(self.P) if self.P else 0
+        self.device = device
+        self._ctx_arr = (ctypes.c_int64 * batch)(*self.ctx_len)
+        cfg = B.spin_config(batch, layers, q_heads, kv_heads, B.HEAD_DIM, B.PART_TOKENS, topk, buf_mult,
+                            self._ctx_arr, 0, seg_pool_segments, device, flags)
+        self.h = B.spin_create(cfg)
+
+    @classmethod
+    def for_workload(cls, w, device: int = 0, **kw) -> "SpinContext":
+        return cls(w.B, w.L, w.Hq, w.Hkv, w.ctx_len, w.topk, w.buf_mult, device=device, **kw)
+
+    def close(self):
+        if getattr(self, "h", None):
+            B.spin_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # ---- Index + Offload ----
+    def index_offload_host(self, b: int, layer: int, k_bits: np.ndarray, v_bits: np.ndarray, stream: int = 0):
+        """k_bits, v_bits: uint16 [Hkv][ctx_len[b]][128] host arrays (kept alive until the stream syncs)."""
+        n = self.ctx_len[b]
+        assert k_bits.shape == (self.Hkv, n, B.HEAD_DIM) and v_bits.shape == k_bits.shape
+        B.spin_index_offload(self.h, b, layer, _ptr(k_bits), _ptr(v_bits), n, True, stream)
+
+    def index_offload_device(self, b: int, layer: int, k_dev, v_dev, stream: int = 0):
+        """k_dev, v_dev: contiguous CUDA tensors [Hkv][ctx_len[b]][128] of bf16 or int16 bits."""
+        n = self.ctx_len[b]
+        B.spin_index_offload(self.h, b, layer, k_dev.data_ptr(), v_dev.data_ptr(), n, False, stream)
+
+    # ---- decode ----
+    def decode_step(self, layer: int, q_dev, out_dev, stream: int = 0):
+        """q_dev: CUDA bf16/int16 [B][Hq][128]; out_dev: CUDA fp32 [B][Hq][128]."""
+        B.spin_decode_step(self.h, layer, q_dev.data_ptr(), out_dev.data_ptr(), stream)
+
+    def decode_step_host(self, layer: int, q_host_ptr: int, out_host_ptr: int, stream: int = 0):
+        B.spin_decode_step_host(self.h, layer, q_host_ptr, out_host_ptr, stream)
+
+    # ---- inspection ----
+    def stats(self, check: bool = True) -> dict:
+        st = B.spin_stats(self.h, check=check)
+        d = st.as_dict()
+        d["rc"] = st.rc
+        return d
+
+    def export(self, layer: int, resolve: bool = True, scores: bool = False) -> dict:
+        Ul = self.B * self.Hkv
+        out = dict(
+            keff=np.empty(Ul, np.int32),
+            sel=np.empty((Ul, self.k), np.int32),
+            sel_slot=np.empty((Ul, self.k), np.int32),
+            sel_hit=np.empty((Ul, self.k), np.uint8),
+            slot_part=np.empty((Ul, self.cap), np.int32),
+            last_use=np.empty((Ul, self.cap), np.int32),
+            unit_info=np.empty((Ul, 8), np.int32),
+        )
+        if resolve:
+            out["resolve"] = np.empty((Ul, max(self.P_max, 1)), np.int32)
+            out["live_segs"] = np.empty(Ul, np.int32)
+        if scores:
+            out["scores"] = np.empty((Ul, max(self.P_max, 1)), np.float32)
+        v = B.spin_state_view(*[(_ptr(out[n]) if n in out else None) for n, _ in B.spin_state_view._fields_])
+        B.spin_debug_export(self.h, layer, v)
+        return out
+
+    def read_page(self, layer: int, b: int, h: int, slot: int) -> np.ndarray:
+        dst = np.empty((2, B.PART_TOKENS, B.HEAD_DIM), np.uint16)
+        B.spin_debug_read_page(self.h, layer, b, h, slot, _ptr(dst))
+        return dst
+
+    def summaries(self, layer: int, b: int, h: int) -> np.ndarray:
+        dst = np.empty((max(self.P[b], 1), B.HEAD_DIM), np.float32)
+        B.spin_debug_summaries(self.h, layer, b, h, _ptr(dst))
+        return dst[:self.P[b]]

@@ -1,0 +1,713 @@
+// Host runtime and C ABI of the SPIN sparse-decode library (see include/spin.h).
+//
+// Owns the memory tiers and metadata of the method (m.x-techcon.com SPIN article,
+// section "Spin的核心设计" 2 and 3, Figures 5 and 6; gist.science/pt section 2B-C):
+//   * pinned, device-mapped host page store: every page of every unit (Offload);
+//   * HBM page pool: cap = buf_mult * k pages per unit (mandatory + buffer pages);
+//   * two-level page table: a static directory [units][ceil(Pmax/64)] whose
+//     entries point to 64-entry segments drawn on demand from one shared pool;
+//   * per-page state: slot -> partition, last-use step (bucketed-LRU timestamps);
+//   * fp32 partition summaries in HBM.
+// A decode step of one layer enqueues five kernels on the caller's stream:
+// score -> select+manage -> retrieve -> attention -> combine.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/spin.h"
+#include "spin_internal.cuh"
+
+using namespace spin;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct LayerBuf {
+  float* scores = nullptr;
+  int32_t* sel = nullptr;
+  int32_t* sel_slot = nullptr;
+  uint8_t* sel_hit = nullptr;
+  int32_t* keff = nullptr;
+  int32_t* unit_info = nullptr;
+  int64_t* miss_src = nullptr;
+  int64_t* miss_dst = nullptr;
+  int32_t* counters = nullptr;
+  float* partials = nullptr;
+  uint16_t* q_stage = nullptr;  // for the host-buffer entry point
+  float* out_stage = nullptr;
+  LayerArgs args{};
+};
+
+constexpr int kNumStages = 5;  // select, manage, retrieve, attention, combine
+
+struct TimedCall {
+  cudaEvent_t ev[kNumStages + 1];
+};
+
+}  // namespace
+
+struct spin_ctx {
+  // configuration
+  int device = 0;
+  uint32_t flags = 0;
+  int B = 0, L = 0, Hq = 0, Hkv = 0, G = 0, k = 0, cap = 0, D = 0, P_max = 0, ppt = 1, n_chunks = 1;
+  int sm_count = 0;
+  std::vector<int64_t> ctx_len;
+  std::vector<int32_t> P_b, ntok_b;
+  std::vector<int64_t> poff_b;
+  int64_t pages_per_layer = 0, units = 0, S = 0;
+  // memory
+  std::vector<void*> dev_allocs;
+  uint16_t* h_store = nullptr;  // pinned host page store
+  uint16_t* d_store = nullptr;  // its device-usable address
+  uint16_t* d_pool = nullptr;
+  float* d_summ = nullptr;
+  int32_t *d_P_b = nullptr, *d_ntok_b = nullptr;
+  int64_t* d_poff_b = nullptr;
+  int32_t *d_dir = nullptr, *d_seg = nullptr, *d_seg_live = nullptr;
+  uint32_t* d_bitmap = nullptr;
+  int32_t *d_slot_part = nullptr, *d_last_use = nullptr;
+  unsigned long long* d_stats = nullptr;
+  uint32_t* d_err = nullptr;
+  uint16_t *d_stage_k = nullptr, *d_stage_v = nullptr;
+  int64_t stage_tokens = 0;
+  std::vector<LayerBuf> layers;
+  CUtensorMap tmap{};
+  std::vector<uint8_t> offloaded;  // [L][B]
+  int64_t steps_host = 0;
+  uint32_t sticky = 0;
+  std::string msg;
+  // stage timing
+  std::vector<TimedCall> pending;
+  std::vector<cudaEvent_t> spare_events;
+  double ms[kNumStages] = {0, 0, 0, 0, 0};
+  int64_t timed_calls = 0;
+  int64_t bytes_meta = 0, bytes_flat = 0, bytes_pool = 0, bytes_store = 0, bytes_summ = 0;
+};
+
+namespace {
+
+int fail(spin_ctx* c, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  if (c) c->msg = buf;
+  else g_create_error = buf;
+  return code;
+}
+
+int cuda_fail(spin_ctx* c, cudaError_t e, const char* what) {
+  cudaGetLastError();
+  return fail(c, e == cudaErrorMemoryAllocation ? SPIN_ERR_OOM : SPIN_ERR_CUDA, "%s: %s", what,
+              cudaGetErrorString(e));
+}
+
+#define SPIN_CUDA(c, call, what)                  \
+  do {                                            \
+    cudaError_t e_ = (call);                      \
+    if (e_ != cudaSuccess) return cuda_fail(c, e_, what); \
+  } while (0)
+
+template <typename T>
+cudaError_t dalloc(spin_ctx* c, T** p, size_t count) {
+  void* v = nullptr;
+  cudaError_t e = cudaMalloc(&v, std::max<size_t>(count, 1) * sizeof(T));
+  if (e != cudaSuccess) return e;
+  c->dev_allocs.push_back(v);
+  *p = static_cast<T*>(v);
+  return cudaSuccess;
+}
+
+void free_all(spin_ctx* c) {
+  for (void* p : c->dev_allocs) cudaFree(p);
+  c->dev_allocs.clear();
+  if (c->h_store) cudaFreeHost(c->h_store);
+  c->h_store = nullptr;
+  for (auto& t : c->pending)
+    for (auto e : t.ev) cudaEventDestroy(e);
+  c->pending.clear();
+  for (auto e : c->spare_events) cudaEventDestroy(e);
+  c->spare_events.clear();
+}
+
+int check_device_error(spin_ctx* c) {
+  if (!c->sticky) {
+    uint32_t e = 0;
+    if (cudaMemcpy(&e, c->d_err, sizeof(e), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return cuda_fail(c, cudaGetLastError(), "reading the device error word");
+    c->sticky = e;
+  }
+  if (c->sticky & kErrCapacity)
+    return fail(c, SPIN_ERR_CAPACITY, "the shared second-level segment pool ran out (device error 0x%x)", c->sticky);
+  if (c->sticky & kErrTimeout)
+    return fail(c, SPIN_ERR_TIMEOUT, "a bounded device wait ran out (device error 0x%x)", c->sticky);
+  if (c->sticky) return fail(c, SPIN_ERR_CUDA, "device invariant error 0x%x", c->sticky);
+  return SPIN_OK;
+}
+
+int sync_ctx(spin_ctx* c) {
+  SPIN_CUDA(c, cudaDeviceSynchronize(), "synchronising the device");
+  // fold finished stage timings
+  for (auto& t : c->pending) {
+    for (int s = 0; s < kNumStages; ++s) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, t.ev[s], t.ev[s + 1]) == cudaSuccess) c->ms[s] += ms;
+    }
+    for (auto e : t.ev) c->spare_events.push_back(e);
+  }
+  c->pending.clear();
+  return check_device_error(c);
+}
+
+int encode_tensor_map(spin_ctx* c) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+    return fail(c, SPIN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const uint64_t slots = (uint64_t)c->units * (uint64_t)c->cap;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)(slots * 128)};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = reinterpret_cast<EncodeTiledFn>(fn)(&c->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->d_pool, dims,
+                                                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(c, SPIN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SPIN_OK;
+}
+
+int get_event(spin_ctx* c, cudaEvent_t* e) {
+  if (!c->spare_events.empty()) {
+    *e = c->spare_events.back();
+    c->spare_events.pop_back();
+    return SPIN_OK;
+  }
+  SPIN_CUDA(c, cudaEventCreate(e), "creating a timing event");
+  return SPIN_OK;
+}
+
+int validate(const spin_config* cfg) {
+  if (!cfg) return fail(nullptr, SPIN_ERR_INVALID, "cfg is NULL");
+  if (cfg->batch < 1 || cfg->layers < 1 || cfg->kv_heads < 1 || cfg->q_heads < 1)
+    return fail(nullptr, SPIN_ERR_INVALID, "batch, layers, q_heads and kv_heads must be >= 1");
+  if (cfg->q_heads % cfg->kv_heads != 0 || cfg->q_heads / cfg->kv_heads > kMaxGroup)
+    return fail(nullptr, SPIN_ERR_INVALID, "q_heads must be a multiple of kv_heads with a group of at most %d",
+                kMaxGroup);
+  if (cfg->head_dim != kD) return fail(nullptr, SPIN_ERR_INVALID, "head_dim must be %d", kD);
+  if (cfg->part_tokens != kPart) return fail(nullptr, SPIN_ERR_INVALID, "part_tokens must be %d", kPart);
+  if (cfg->seg_entries != 0 && cfg->seg_entries != kSeg)
+    return fail(nullptr, SPIN_ERR_INVALID, "seg_entries must be 0 or %d", kSeg);
+  if (cfg->topk < 1 || cfg->topk > kMaxTopk) return fail(nullptr, SPIN_ERR_INVALID, "topk must be in [1, %d]", kMaxTopk);
+  if (cfg->buf_mult < 1 || (int64_t)cfg->buf_mult * cfg->topk > 8192)
+    return fail(nullptr, SPIN_ERR_INVALID, "buf_mult must be >= 1 with buf_mult * topk <= 8192");
+  if (!cfg->ctx_len) return fail(nullptr, SPIN_ERR_INVALID, "ctx_len is NULL");
+  for (int b = 0; b < cfg->batch; ++b) {
+    if (cfg->ctx_len[b] < 0 || cfg->ctx_len[b] > (int64_t)32768 * kPart)
+      return fail(nullptr, SPIN_ERR_INVALID, "ctx_len[%d] = %lld outside [0, %d]", b, (long long)cfg->ctx_len[b],
+                  32768 * kPart);
+  }
+  if (cfg->seg_pool_segments < 0) return fail(nullptr, SPIN_ERR_INVALID, "seg_pool_segments must be >= 0");
+  const int64_t units = (int64_t)cfg->batch * cfg->layers * cfg->kv_heads;
+  if (units * cfg->buf_mult * cfg->topk >= (int64_t)1 << 24)
+    return fail(nullptr, SPIN_ERR_INVALID, "units * capacity must stay below 2^24 pages");
+  return SPIN_OK;
+}
+
+LayerArgs make_args(spin_ctx* c, int l) {
+  LayerArgs a{};
+  LayerBuf& lb = c->layers[l];
+  a.layer = l;
+  a.B = c->B;
+  a.Hq = c->Hq;
+  a.Hkv = c->Hkv;
+  a.G = c->G;
+  a.k = c->k;
+  a.cap = c->cap;
+  a.D = c->D;
+  a.P_max = c->P_max;
+  a.n_chunks = c->n_chunks;
+  a.ppt = c->ppt;
+  a.S = (int32_t)c->S;
+  a.P_b = c->d_P_b;
+  a.ntok_b = c->d_ntok_b;
+  a.poff_b = c->d_poff_b;
+  a.layer_page_base = (int64_t)l * c->pages_per_layer;
+  a.unit_base = (int64_t)l * c->B * c->Hkv;
+  a.summ = c->d_summ;
+  a.host_store = c->d_store;
+  a.pool = c->d_pool;
+  a.dir = c->d_dir;
+  a.seg = c->d_seg;
+  a.seg_live = c->d_seg_live;
+  a.seg_bitmap = c->d_bitmap;
+  a.slot_part = c->d_slot_part;
+  a.last_use = c->d_last_use;
+  a.scores = lb.scores;
+  a.sel = lb.sel;
+  a.sel_slot = lb.sel_slot;
+  a.sel_hit = lb.sel_hit;
+  a.keff = lb.keff;
+  a.unit_info = lb.unit_info;
+  a.miss_src = lb.miss_src;
+  a.miss_dst = lb.miss_dst;
+  a.counters = lb.counters;
+  a.partials = lb.partials;
+  a.stats = c->d_stats;
+  a.err = c->d_err;
+  return a;
+}
+
+int create_impl(const spin_config* cfg, spin_ctx* c) {
+  c->device = cfg->device;
+  c->flags = cfg->flags;
+  c->B = cfg->batch;
+  c->L = cfg->layers;
+  c->Hq = cfg->q_heads;
+  c->Hkv = cfg->kv_heads;
+  c->G = c->Hq / c->Hkv;
+  c->k = cfg->topk;
+  c->cap = cfg->buf_mult * cfg->topk;
+  c->ctx_len.assign(cfg->ctx_len, cfg->ctx_len + c->B);
+  c->P_b.resize(c->B);
+  c->ntok_b.resize(c->B);
+  c->poff_b.resize(c->B);
+  int64_t poff = 0;
+  c->P_max = 0;
+  int64_t auto_S = 0;
+  for (int b = 0; b < c->B; ++b) {
+    c->ntok_b[b] = (int32_t)c->ctx_len[b];
+    c->P_b[b] = (int32_t)((c->ctx_len[b] + kPart - 1) / kPart);
+    c->poff_b[b] = poff;
+    poff += c->P_b[b];
+    c->P_max = std::max(c->P_max, c->P_b[b]);
+    const int64_t Du = (c->P_b[b] + kSeg - 1) / kSeg;
+    auto_S += std::min<int64_t>(Du, c->cap) * c->Hkv * c->L;
+  }
+  c->D = std::max(1, (c->P_max + kSeg - 1) / kSeg);
+  c->pages_per_layer = poff * c->Hkv;
+  c->units = (int64_t)c->B * c->L * c->Hkv;
+  c->S = cfg->seg_pool_segments > 0 ? cfg->seg_pool_segments : std::max<int64_t>(auto_S, 1);
+  if (c->S >= (int64_t)1 << 30) return fail(nullptr, SPIN_ERR_INVALID, "seg_pool_segments too large");
+
+  // Test hook: report a failed pinned allocation before touching the device.
+  if (c->flags & SPIN_FLAG_TEST_FAIL_PINNED)
+    return fail(nullptr, SPIN_ERR_OOM, "pinned host allocation failed (injected by SPIN_FLAG_TEST_FAIL_PINNED)");
+
+  cudaError_t e = cudaSetDevice(c->device);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "selecting the CUDA device");
+  int major = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, c->device);
+  cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
+  if (major < 10) return fail(nullptr, SPIN_ERR_CUDA, "device %d is not a Blackwell GPU (sm_%d)", c->device, major);
+
+  // pinned host page store (mapped: kernels read it directly)
+  const int64_t total_pages = c->pages_per_layer * c->L;
+  c->bytes_store = total_pages * kPageBytes;
+  if (total_pages > 0) {
+    void* h = nullptr;
+    e = cudaHostAlloc(&h, (size_t)c->bytes_store, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(nullptr, SPIN_ERR_OOM, "pinned host allocation of %lld bytes failed: %s",
+                  (long long)c->bytes_store, cudaGetErrorString(e));
+    }
+    c->h_store = static_cast<uint16_t*>(h);
+    void* d = nullptr;
+    e = cudaHostGetDevicePointer(&d, h, 0);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "mapping the host page store");
+    c->d_store = static_cast<uint16_t*>(d);
+  }
+
+  // HBM
+  const int64_t slots = c->units * c->cap;
+  c->bytes_pool = slots * kPageBytes;
+  c->bytes_summ = total_pages * kD * 4;
+#define ALLOC(ptr, n, what) \
+  if ((e = dalloc(c, &(ptr), (size_t)(n))) != cudaSuccess) return cuda_fail(nullptr, e, what)
+  ALLOC(c->d_pool, slots * kPageElems, "allocating the HBM page pool");
+  ALLOC(c->d_summ, total_pages * kD, "allocating the summaries");
+  ALLOC(c->d_P_b, c->B, "allocating request tables");
+  ALLOC(c->d_ntok_b, c->B, "allocating request tables");
+  ALLOC(c->d_poff_b, c->B, "allocating request tables");
+  ALLOC(c->d_dir, c->units * c->D, "allocating the directory");
+  ALLOC(c->d_seg, c->S * kSeg, "allocating the segment pool");
+  ALLOC(c->d_seg_live, c->S, "allocating the segment pool");
+  const int64_t nwords = (c->S + 31) / 32;
+  ALLOC(c->d_bitmap, nwords, "allocating the segment bitmap");
+  ALLOC(c->d_slot_part, slots, "allocating the page state");
+  ALLOC(c->d_last_use, slots, "allocating the page state");
+  ALLOC(c->d_stats, 8, "allocating counters");
+  ALLOC(c->d_err, 1, "allocating counters");
+  c->bytes_meta = (c->units * c->D + c->S * kSeg + c->S + nwords + 2 * slots) * 4;
+  c->bytes_flat = (c->units * (int64_t)c->P_max + 2 * slots) * 4;
+
+  SPIN_CUDA(nullptr, cudaMemcpy(c->d_P_b, c->P_b.data(), 4 * c->B, cudaMemcpyHostToDevice), "uploading tables");
+  SPIN_CUDA(nullptr, cudaMemcpy(c->d_ntok_b, c->ntok_b.data(), 4 * c->B, cudaMemcpyHostToDevice), "uploading tables");
+  SPIN_CUDA(nullptr, cudaMemcpy(c->d_poff_b, c->poff_b.data(), 8 * c->B, cudaMemcpyHostToDevice), "uploading tables");
+  SPIN_CUDA(nullptr, cudaMemset(c->d_dir, 0xff, (size_t)c->units * c->D * 4), "initialising the directory");
+  SPIN_CUDA(nullptr, cudaMemset(c->d_seg, 0xff, (size_t)c->S * kSeg * 4), "initialising the segment pool");
+  SPIN_CUDA(nullptr, cudaMemset(c->d_seg_live, 0, (size_t)c->S * 4), "initialising the segment pool");
+  {
+    std::vector<uint32_t> bm(nwords, 0u);
+    if (c->S % 32) bm[nwords - 1] = ~((1u << (c->S % 32)) - 1u);  // bits past S are never free
+    SPIN_CUDA(nullptr, cudaMemcpy(c->d_bitmap, bm.data(), nwords * 4, cudaMemcpyHostToDevice), "initialising the bitmap");
+  }
+  SPIN_CUDA(nullptr, cudaMemset(c->d_slot_part, 0xff, (size_t)slots * 4), "initialising the page state");
+  SPIN_CUDA(nullptr, cudaMemset(c->d_last_use, 0, (size_t)slots * 4), "initialising the page state");
+  SPIN_CUDA(nullptr, cudaMemset(c->d_stats, 0, 8 * 8), "initialising counters");
+  SPIN_CUDA(nullptr, cudaMemset(c->d_err, 0, 4), "initialising counters");
+
+  // attention work split: pages per task
+  const int64_t pages_layer = (int64_t)c->B * c->Hkv * c->k;
+  c->ppt = (int)std::max<int64_t>(1, std::min<int64_t>(8, pages_layer / (4 * std::max(1, c->sm_count))));
+  c->n_chunks = (c->k + c->ppt - 1) / c->ppt;
+
+  const int64_t Ul = (int64_t)c->B * c->Hkv;
+  c->layers.resize(c->L);
+  for (int l = 0; l < c->L; ++l) {
+    LayerBuf& lb = c->layers[l];
+    ALLOC(lb.scores, Ul * std::max(1, c->P_max), "allocating layer scratch");
+    ALLOC(lb.sel, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.sel_slot, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.sel_hit, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.keff, Ul, "allocating layer scratch");
+    ALLOC(lb.unit_info, Ul * 8, "allocating layer scratch");
+    ALLOC(lb.miss_src, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.miss_dst, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.counters, 4, "allocating layer scratch");
+    ALLOC(lb.partials, Ul * c->n_chunks * c->G * kPartialStride, "allocating layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.counters, 0, 16), "initialising layer counters");
+    SPIN_CUDA(nullptr, cudaMemset(lb.keff, 0, Ul * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.sel, 0xff, Ul * c->k * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.sel_slot, 0xff, Ul * c->k * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.sel_hit, 0, Ul * c->k), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.unit_info, 0, Ul * 8 * 4), "initialising layer scratch");
+    lb.args = make_args(c, l);
+  }
+#undef ALLOC
+  c->offloaded.assign((size_t)c->L * c->B, 0);
+
+  int rc = encode_tensor_map(c);
+  if (rc != SPIN_OK) {
+    g_create_error = c->msg;
+    return rc;
+  }
+  SPIN_CUDA(nullptr, attention_configure(), "configuring the attention kernel");
+  SPIN_CUDA(nullptr, select_manage_configure(select_manage_smem_bytes(c->layers[0].args)),
+            "configuring the select kernel");
+  SPIN_CUDA(nullptr, cudaDeviceSynchronize(), "finishing context set-up");
+  return SPIN_OK;
+}
+
+// Enqueue one layer's step. q/out are device pointers.
+int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStream_t st) {
+  LayerBuf& lb = c->layers[layer];
+  LayerArgs a = lb.args;
+  a.q = q;
+  a.out = out;
+  const bool timed = (c->flags & SPIN_FLAG_STAGE_TIMING) != 0;
+  TimedCall tc{};
+  if (timed) {
+    for (auto& e : tc.ev) {
+      int rc = get_event(c, &e);
+      if (rc) return rc;
+    }
+  }
+  auto mark = [&](int i) {
+    if (timed) cudaEventRecord(tc.ev[i], st);
+  };
+  const int retrieve_grid = 2 * c->sm_count;
+  mark(0);
+  SPIN_CUDA(c, launch_score(a, st), "launching score");
+  mark(1);
+  SPIN_CUDA(c, launch_select_manage(a, st), "launching select/manage");
+  mark(2);
+  SPIN_CUDA(c, launch_retrieve(a, retrieve_grid, st), "launching retrieve");
+  mark(3);
+  SPIN_CUDA(c, launch_attention(a, &c->tmap, c->sm_count, st), "launching attention");
+  mark(4);
+  SPIN_CUDA(c, launch_combine(a, st), "launching combine");
+  mark(5);
+  if (timed) {
+    c->pending.push_back(tc);
+    c->timed_calls += 1;
+  }
+  c->steps_host += 1;
+  return SPIN_OK;
+}
+
+int check_layer(spin_ctx* c, int layer) {
+  if (layer < 0 || layer >= c->L) return fail(c, SPIN_ERR_INVALID, "layer %d outside [0, %d)", layer, c->L);
+  for (int b = 0; b < c->B; ++b)
+    if (!c->offloaded[(size_t)layer * c->B + b])
+      return fail(c, SPIN_ERR_STATE, "request %d of layer %d has not been offloaded", b, layer);
+  if (c->sticky) return check_device_error(c);
+  return SPIN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spin_create(const spin_config* cfg, spin_ctx** out) {
+  if (!out) return fail(nullptr, SPIN_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  int rc = validate(cfg);
+  if (rc) return rc;
+  spin_ctx* c = new (std::nothrow) spin_ctx();
+  if (!c) return fail(nullptr, SPIN_ERR_OOM, "host allocation of the context failed");
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) {
+    cudaGetLastError();
+    prev = -1;
+  }
+  rc = create_impl(cfg, c);
+  if (prev >= 0) cudaSetDevice(prev);
+  if (rc != SPIN_OK) {
+    free_all(c);
+    delete c;
+    return rc;
+  }
+  *out = c;
+  return SPIN_OK;
+}
+
+int spin_index_offload(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k, const uint16_t* v,
+                       int64_t n_tokens, int32_t src_is_host, spin_stream_t stream) {
+  if (!c) return fail(nullptr, SPIN_ERR_INVALID, "ctx is NULL");
+  if (b < 0 || b >= c->B || layer < 0 || layer >= c->L)
+    return fail(c, SPIN_ERR_INVALID, "request %d / layer %d out of range", b, layer);
+  if (n_tokens != c->ctx_len[b])
+    return fail(c, SPIN_ERR_INVALID, "n_tokens %lld differs from ctx_len[%d] = %lld", (long long)n_tokens, b,
+                (long long)c->ctx_len[b]);
+  if (n_tokens > 0 && (!k || !v)) return fail(c, SPIN_ERR_INVALID, "k or v is NULL");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+    return fail(c, SPIN_ERR_INVALID, "k and v must be 16-byte aligned");
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t P = c->P_b[b];
+  const int64_t page0 = (int64_t)layer * c->pages_per_layer + (int64_t)c->Hkv * c->poff_b[b];
+  float* summ0 = c->d_summ + page0 * kD;
+  uint16_t* host0 = c->d_store + page0 * kPageElems;
+  if (n_tokens > 0) {
+    if (!src_is_host) {
+      SPIN_CUDA(c, launch_summarize_offload(k, v, n_tokens, c->Hkv, 0, n_tokens, n_tokens, summ0, host0, P, st),
+                "launching summarize/offload");
+    } else {
+      // stage through HBM in chunks of whole partitions
+      const int64_t chunk_tok = 256 * kPart;
+      if (!c->d_stage_k) {
+        cudaError_t e;
+        if ((e = dalloc(c, &c->d_stage_k, (size_t)c->Hkv * chunk_tok * kD)) != cudaSuccess)
+          return cuda_fail(c, e, "allocating the offload staging buffer");
+        if ((e = dalloc(c, &c->d_stage_v, (size_t)c->Hkv * chunk_tok * kD)) != cudaSuccess)
+          return cuda_fail(c, e, "allocating the offload staging buffer");
+        c->stage_tokens = chunk_tok;
+      }
+      for (int64_t t0 = 0; t0 < n_tokens; t0 += chunk_tok) {
+        const int64_t nt = std::min(chunk_tok, n_tokens - t0);
+        SPIN_CUDA(c,
+                  cudaMemcpy2DAsync(c->d_stage_k, (size_t)nt * kD * 2, k + t0 * kD, (size_t)n_tokens * kD * 2,
+                                    (size_t)nt * kD * 2, (size_t)c->Hkv, cudaMemcpyHostToDevice, st),
+                  "copying K to the staging buffer");
+        SPIN_CUDA(c,
+                  cudaMemcpy2DAsync(c->d_stage_v, (size_t)nt * kD * 2, v + t0 * kD, (size_t)n_tokens * kD * 2,
+                                    (size_t)nt * kD * 2, (size_t)c->Hkv, cudaMemcpyHostToDevice, st),
+                  "copying V to the staging buffer");
+        SPIN_CUDA(c,
+                  launch_summarize_offload(c->d_stage_k, c->d_stage_v, nt, c->Hkv, t0, nt, n_tokens, summ0, host0,
+                                           P, st),
+                  "launching summarize/offload");
+      }
+    }
+  }
+  c->offloaded[(size_t)layer * c->B + b] = 1;
+  return SPIN_OK;
+}
+
+int spin_decode_step(spin_ctx* c, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream) {
+  if (!c) return fail(nullptr, SPIN_ERR_INVALID, "ctx is NULL");
+  if (!q || !out) return fail(c, SPIN_ERR_INVALID, "q or out is NULL");
+  if ((reinterpret_cast<uintptr_t>(q) & 3) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return fail(c, SPIN_ERR_INVALID, "q must be 4-byte and out 16-byte aligned");
+  int rc = check_layer(c, layer);
+  if (rc) return rc;
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  return enqueue_step(c, layer, q, out, static_cast<cudaStream_t>(stream));
+}
+
+int spin_decode_step_host(spin_ctx* c, int32_t layer, const uint16_t* q_host, float* out_host, spin_stream_t stream) {
+  if (!c) return fail(nullptr, SPIN_ERR_INVALID, "ctx is NULL");
+  if (!q_host || !out_host) return fail(c, SPIN_ERR_INVALID, "q_host or out_host is NULL");
+  int rc = check_layer(c, layer);
+  if (rc) return rc;
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  LayerBuf& lb = c->layers[layer];
+  const size_t nq = (size_t)c->B * c->Hq * kD;
+  if (!lb.q_stage) {
+    cudaError_t e;
+    if ((e = dalloc(c, &lb.q_stage, nq)) != cudaSuccess) return cuda_fail(c, e, "allocating the query buffer");
+    if ((e = dalloc(c, &lb.out_stage, nq)) != cudaSuccess) return cuda_fail(c, e, "allocating the output buffer");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SPIN_CUDA(c, cudaMemcpyAsync(lb.q_stage, q_host, nq * 2, cudaMemcpyHostToDevice, st), "copying q to the device");
+  rc = enqueue_step(c, layer, lb.q_stage, lb.out_stage, st);
+  if (rc) return rc;
+  SPIN_CUDA(c, cudaMemcpyAsync(out_host, lb.out_stage, nq * 4, cudaMemcpyDeviceToHost, st), "copying out to the host");
+  return SPIN_OK;
+}
+
+int spin_stats(spin_ctx* c, spin_stats_t* out) {
+  if (!c || !out) return fail(c, SPIN_ERR_INVALID, "ctx or out is NULL");
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  int rc = sync_ctx(c);
+  unsigned long long st[8] = {0};
+  int32_t live = 0;
+  if (cudaMemcpy(st, c->d_stats, sizeof(st), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return cuda_fail(c, cudaGetLastError(), "reading counters");
+  {
+    // live segments = set bits of the bitmap that are real segments
+    const int64_t nwords = (c->S + 31) / 32;
+    std::vector<uint32_t> bm(nwords);
+    if (cudaMemcpy(bm.data(), c->d_bitmap, nwords * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return cuda_fail(c, cudaGetLastError(), "reading the segment bitmap");
+    if (c->S % 32) bm[nwords - 1] &= (1u << (c->S % 32)) - 1u;
+    for (auto w : bm) live += __builtin_popcount(w);
+  }
+  memset(out, 0, sizeof(*out));
+  out->steps = c->steps_host;
+  out->hits = (int64_t)st[kStatHits];
+  out->misses = (int64_t)st[kStatMisses];
+  out->evictions = (int64_t)st[kStatEvictions];
+  out->lru_rounds = (int64_t)st[kStatLruRounds];
+  out->retrieved_bytes = out->misses * kPageBytes;
+  out->selected_bytes = (int64_t)st[kStatSelected] * kPageBytes;
+  out->live_segments = live;
+  out->pool_segments = c->S;
+  out->metadata_bytes = c->bytes_meta;
+  out->flat_table_bytes = c->bytes_flat;
+  out->hbm_pool_bytes = c->bytes_pool;
+  out->host_store_bytes = c->bytes_store;
+  out->summary_bytes = c->bytes_summ;
+  out->timed_calls = c->timed_calls;
+  out->ms_select = c->ms[0];
+  out->ms_manage = c->ms[1];
+  out->ms_retrieve = c->ms[2];
+  out->ms_attention = c->ms[3];
+  out->ms_combine = c->ms[4];
+  out->device_error = c->sticky;
+  return rc;
+}
+
+int spin_debug_export(spin_ctx* c, int32_t layer, spin_state_view* v) {
+  if (!c || !v) return fail(c, SPIN_ERR_INVALID, "ctx or view is NULL");
+  if (layer < 0 || layer >= c->L) return fail(c, SPIN_ERR_INVALID, "layer %d out of range", layer);
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  int rc = sync_ctx(c);
+  LayerBuf& lb = c->layers[layer];
+  const int64_t Ul = (int64_t)c->B * c->Hkv;
+  const int64_t u0 = (int64_t)layer * Ul;
+#define D2H(dst, src, bytes)                                                                \
+  if (dst) {                                                                                \
+    if (cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)                 \
+      return cuda_fail(c, cudaGetLastError(), "copying debug state");                       \
+  }
+  D2H(v->keff, lb.keff, Ul * 4);
+  D2H(v->sel, lb.sel, Ul * c->k * 4);
+  D2H(v->sel_slot, lb.sel_slot, Ul * c->k * 4);
+  D2H(v->sel_hit, lb.sel_hit, Ul * c->k);
+  D2H(v->slot_part, c->d_slot_part + u0 * c->cap, Ul * c->cap * 4);
+  D2H(v->last_use, c->d_last_use + u0 * c->cap, Ul * c->cap * 4);
+  D2H(v->unit_info, lb.unit_info, Ul * 8 * 4);
+  D2H(v->scores, lb.scores, Ul * c->P_max * 4);
+  if (v->resolve || v->live_segs) {
+    int32_t *dres = nullptr, *dlive = nullptr;
+    if (cudaMalloc(&dres, std::max<int64_t>(1, Ul * c->P_max) * 4) != cudaSuccess ||
+        cudaMalloc(&dlive, Ul * 4) != cudaSuccess) {
+      cudaFree(dres);
+      return cuda_fail(c, cudaGetLastError(), "allocating debug buffers");
+    }
+    cudaError_t e = launch_resolve_all(lb.args, dres, dlive, 0);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess && v->resolve) e = cudaMemcpy(v->resolve, dres, Ul * c->P_max * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && v->live_segs) e = cudaMemcpy(v->live_segs, dlive, Ul * 4, cudaMemcpyDeviceToHost);
+    cudaFree(dres);
+    cudaFree(dlive);
+    if (e != cudaSuccess) return cuda_fail(c, e, "resolving the page table");
+  }
+#undef D2H
+  return rc;
+}
+
+int spin_debug_read_page(spin_ctx* c, int32_t layer, int32_t b, int32_t h, int32_t slot, uint16_t* dst) {
+  if (!c || !dst) return fail(c, SPIN_ERR_INVALID, "ctx or dst is NULL");
+  if (layer < 0 || layer >= c->L || b < 0 || b >= c->B || h < 0 || h >= c->Hkv || slot < 0 || slot >= c->cap)
+    return fail(c, SPIN_ERR_INVALID, "page coordinates out of range");
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  int rc = sync_ctx(c);
+  const int64_t unit = ((int64_t)layer * c->B + b) * c->Hkv + h;
+  SPIN_CUDA(c, cudaMemcpy(dst, c->d_pool + (unit * c->cap + slot) * kPageElems, kPageBytes, cudaMemcpyDeviceToHost),
+            "copying a page");
+  return rc;
+}
+
+int spin_debug_summaries(spin_ctx* c, int32_t layer, int32_t b, int32_t h, float* dst) {
+  if (!c || !dst) return fail(c, SPIN_ERR_INVALID, "ctx or dst is NULL");
+  if (layer < 0 || layer >= c->L || b < 0 || b >= c->B || h < 0 || h >= c->Hkv)
+    return fail(c, SPIN_ERR_INVALID, "unit coordinates out of range");
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  int rc = sync_ctx(c);
+  const int64_t page0 = (int64_t)layer * c->pages_per_layer + (int64_t)c->Hkv * c->poff_b[b] + (int64_t)h * c->P_b[b];
+  if (c->P_b[b] > 0)
+    SPIN_CUDA(c, cudaMemcpy(dst, c->d_summ + page0 * kD, (size_t)c->P_b[b] * kD * 4, cudaMemcpyDeviceToHost),
+              "copying summaries");
+  return rc;
+}
+
+void spin_destroy(spin_ctx* c) {
+  if (!c) return;
+  {
+    DeviceGuard g(c->device);
+    cudaDeviceSynchronize();
+    free_all(c);
+  }
+  delete c;
+}
+
+const char* spin_last_error(const spin_ctx* c) { return c ? c->msg.c_str() : g_create_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// Internal definitions shared by the kernels and the host runtime of the
+// SPIN sparse-decode library (sm_103a). Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spin {
+
+constexpr int kD = 128;                       // head dim
+constexpr int kPart = 64;                     // tokens per partition / page
+constexpr int kSeg = 64;                      // entries per second-level segment
+constexpr int kBuckets = 64;                  // LRU timestamp buckets
+constexpr int kPageElems = 2 * kPart * kD;    // bf16 elements per page (K then V)
+constexpr int kPageBytes = kPageElems * 2;    // 32768
+constexpr int kPartialStride = 132;           // floats per (task, head) partial: m, l, pad, pad, acc[128]
+constexpr int kMaxTopk = 512;
+constexpr int kMaxGroup = 16;
+
+// Device error word bits.
+enum : uint32_t {
+  kErrCapacity = 1u,   // shared segment pool exhausted
+  kErrTimeout = 2u,    // a bounded wait ran out
+  kErrInternal = 4u,   // an invariant of the page state was found broken
+};
+
+// Per-layer arguments of the decode-step kernels (passed by value).
+struct LayerArgs {
+  int32_t layer, B, Hq, Hkv, G, k, cap, D, P_max, n_chunks, ppt, S;
+  const int32_t* P_b;        // [B] partitions of request b
+  const int32_t* ntok_b;     // [B] tokens of request b
+  const int64_t* poff_b;     // [B] sum of P over earlier requests
+  int64_t layer_page_base;   // first page of this layer in the host store / summaries
+  int64_t unit_base;         // first global unit of this layer = layer * B * Hkv
+  const float* summ;         // [pages][128] fp32 summaries (all layers)
+  const uint16_t* host_store;// mapped pinned pages [pages][16384] (device-usable address)
+  uint16_t* pool;            // HBM pages [units * cap][16384]
+  int32_t* dir;              // [units][D] segment id or -1
+  int32_t* seg;              // [S][64] slot or -1
+  int32_t* seg_live;         // [S] live entries
+  uint32_t* seg_bitmap;      // [ceil(S/32)] 1 = segment in use
+  int32_t* slot_part;        // [units][cap]
+  int32_t* last_use;         // [units][cap]
+  float* scores;             // [U_l][P_max]
+  int32_t* sel;              // [U_l][k]
+  int32_t* sel_slot;         // [U_l][k] local slot
+  uint8_t* sel_hit;          // [U_l][k]
+  int32_t* keff;             // [U_l]
+  int32_t* unit_info;        // [U_l][8]
+  int64_t* miss_src;         // [U_l * k] host page index
+  int64_t* miss_dst;         // [U_l * k] pool slot index
+  int32_t* counters;         // [4]: miss count, attention task counter, step t, spare
+  float* partials;           // [U_l * n_chunks][G][kPartialStride]
+  unsigned long long* stats; // [8] device counters
+  uint32_t* err;             // device error word
+  const uint16_t* q;         // [B][Hq][128] bf16 (device)
+  float* out;                // [B][Hq][128] fp32 (device)
+};
+
+// Host page index of partition p of (b, h) in the layer described by a.
+__host__ __device__ inline int64_t host_page_index(const LayerArgs& a, int b, int h, int64_t P, int64_t p) {
+  return a.layer_page_base + (int64_t)a.Hkv * a.poff_b[b] + (int64_t)h * P + p;
+}
+
+// Device stats slots.
+enum : int { kStatHits = 0, kStatMisses = 1, kStatEvictions = 2, kStatLruRounds = 3, kStatSelected = 4 };
+
+// ---------------------------------------------------------------------------
+// Launchers (defined in the kernel translation units).
+// ---------------------------------------------------------------------------
+cudaError_t launch_summarize_offload(const uint16_t* k, const uint16_t* v, int64_t head_stride, int32_t kv_heads,
+                                     int64_t tok0, int64_t ntok_chunk, int64_t ntok_total, float* summ_unit0,
+                                     uint16_t* host_unit0, int64_t unit_pages, cudaStream_t st);
+cudaError_t launch_score(const LayerArgs& a, cudaStream_t st);
+cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st);
+cudaError_t launch_retrieve(const LayerArgs& a, int grid, cudaStream_t st);
+cudaError_t launch_attention(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st);
+cudaError_t launch_combine(const LayerArgs& a, cudaStream_t st);
+cudaError_t launch_resolve_all(const LayerArgs& a, int32_t* resolve, int32_t* live_segs, cudaStream_t st);
+size_t select_manage_smem_bytes(const LayerArgs& a);
+size_t attention_smem_bytes();
+cudaError_t attention_configure();
+cudaError_t select_manage_configure(size_t smem);
+
+}  // namespace spin

@@ -1,0 +1,239 @@
+"""Lockstep comparison of the CUDA path (through the C ABI) with the oracle.
+
+Both sides take the same generator inputs; no value produced by the CUDA path
+is ever fed into the oracle. Per decode step and per compared unit:
+
+  selection   Select is stateless, so the GPU set is checked against the
+              oracle's own top-k every step. The sets must be equal outside the
+              tie band: partitions whose oracle score lies within 1e-5 relative
+              of the k-th largest oracle score. Inside the band any choice of
+              the right size is valid.
+  page state  while a unit's selections have matched exactly, the oracle's
+              manager has seen the same history, so slots, hits, timestamps,
+              LRU cutoff and evictions, the resolved table and live segments
+              must agree bit for bit. After a tie-band divergence the unit's
+              state is only checked for validity (invariants below).
+  outputs     max-abs error <= 2e-3 against the oracle's attention over the
+              oracle-enumerated valid set equal to the GPU's set (the oracle's
+              own set when nothing diverged).
+
+Validity invariants checked for every unit of every exported layer: slots hold
+distinct partitions, resolve(p) = s iff slot s holds p, live segments equal the
+occupied 64-partition ranges, the selection is ascending and resident in the
+slots it names, those slots carry the current step.
+"""
+from __future__ import annotations
+
+import itertools
+from dataclasses import dataclass, field
+from typing import Dict, Iterable, List, Optional, Tuple
+
+import numpy as np
+
+import oracle as O
+import workload as W
+
+OUT_TOL = 2e-3
+TIE_REL = 1e-5
+
+
+@dataclass
+class Report:
+    steps: int = 0
+    compared_units: int = 0
+    exact_units: int = 0
+    tie_divergences: int = 0
+    max_out_err: float = 0.0
+    evictions: int = 0
+    misses: int = 0
+    hits: int = 0
+    notes: List[str] = field(default_factory=list)
+
+
+def tie_band(sc: np.ndarray, keff: int) -> Tuple[np.ndarray, float]:
+    order = np.lexsort((np.arange(sc.size), -sc))
+    kth = sc[order[keff - 1]]
+    band = np.abs(sc - kth) <= TIE_REL * abs(kth)
+    return band, kth
+
+
+def check_selection(sc: np.ndarray, sel_o: np.ndarray, sel_g: np.ndarray, where: str) -> bool:
+    """True when identical; False when different only inside the tie band; raises otherwise."""
+    if np.array_equal(sel_o, sel_g):
+        return True
+    keff = sel_o.size
+    assert sel_g.size == keff, f"{where}: GPU selected {sel_g.size} partitions, oracle {keff}"
+    assert np.all(np.diff(sel_g) > 0), f"{where}: GPU selection not strictly ascending"
+    band, kth = tie_band(sc, keff)
+    so, sg = set(sel_o.tolist()), set(sel_g.tolist())
+    outside_o = {p for p in so if not band[p]}
+    outside_g = {p for p in sg if not band[p]}
+    assert outside_o == outside_g, (
+        f"{where}: selections differ outside the tie band: oracle-only {sorted(so - sg)}, gpu-only {sorted(sg - so)}, "
+        f"k-th score {kth!r}, scores {[float(sc[p]) for p in sorted(so ^ sg)]}")
+    return False
+
+
+def valid_sets(sc: np.ndarray, sel_o: np.ndarray) -> Iterable[np.ndarray]:
+    """All selections the tie band allows (oracle arithmetic only)."""
+    keff = sel_o.size
+    band, _ = tie_band(sc, keff)
+    fixed = [p for p in sel_o.tolist() if not band[p]]
+    cands = np.nonzero(band)[0].tolist()
+    need = keff - len(fixed)
+    for comb in itertools.combinations(cands, need):
+        yield np.array(sorted(fixed + list(comb)), np.int32)
+
+
+def check_invariants(ex: dict, ul: int, P: int, t: int, where: str):
+    sp = ex["slot_part"][ul]
+    lu = ex["last_use"][ul]
+    res = [int(p) for p in sp if p >= 0]
+    assert len(set(res)) == len(res), f"{where}: a partition is resident twice"
+    assert all(0 <= p < P for p in res), f"{where}: resident partition out of range"
+    if "resolve" in ex:
+        rs = ex["resolve"][ul][:P]
+        for p in range(P):
+            s = rs[p]
+            if s >= 0:
+                assert sp[s] == p, f"{where}: resolve({p}) = {s} but slot holds {sp[s]}"
+        assert sum(1 for p in range(P) if rs[p] >= 0) == len(res), f"{where}: resolve misses resident pages"
+        assert ex["live_segs"][ul] == len({p // 64 for p in res}), f"{where}: live segments mismatch"
+    keff = int(ex["keff"][ul])
+    sel = ex["sel"][ul][:keff]
+    assert np.all(np.diff(sel) > 0), f"{where}: selection not ascending"
+    for p, s in zip(sel, ex["sel_slot"][ul][:keff]):
+        assert sp[s] == p, f"{where}: selected partition {p} not in its slot {s}"
+        assert lu[s] == t, f"{where}: selected slot {s} has last_use {lu[s]} at step {t}"
+
+
+class Lockstep:
+    """Runs a workload on the GPU and the oracle side by side on chosen units."""
+
+    def __init__(self, w: W.Workload, units: Optional[List[Tuple[int, int, int]]] = None, device: int = 0,
+                 flags: int = 0, seg_pool_segments: int = 0, offload_from_device: bool = False,
+                 gen_threads: int = 0):
+        import torch
+        from sparse_attention_tiered_gb300 import SpinContext
+        self.torch = torch
+        self.w = w
+        self.dev = torch.device(f"cuda:{device}")
+        self.units = units if units is not None else [(l, b, h) for l in range(w.L) for b in range(w.B)
+                                                      for h in range(w.Hkv)]
+        self.ctx = SpinContext.for_workload(w, device=device, flags=flags, seg_pool_segments=seg_pool_segments)
+        self.oracle: Dict[Tuple[int, int, int], O.Unit] = {}
+        self.fresh_cap = max(w.topk, 1)
+        want = {}
+        for (l, b, h) in self.units:
+            want.setdefault((l, b), []).append(h)
+        kbuf = vbuf = None
+        for l in range(w.L):
+            for b in range(w.B):
+                n = w.ctx_len[b]
+                k, v = w.request_kv(l, b, threads=gen_threads)
+                if offload_from_device:
+                    kd = torch.from_numpy(k.view(np.int16)).to(self.dev)
+                    vd = torch.from_numpy(v.view(np.int16)).to(self.dev)
+                    self.ctx.index_offload_device(b, l, kd, vd)
+                    torch.cuda.synchronize()
+                    del kd, vd
+                else:
+                    self.ctx.index_offload_host(b, l, k, v)
+                    torch.cuda.synchronize()  # the host arrays are reused/freed next
+                for h in want.get((l, b), []):
+                    self.oracle[(l, b, h)] = O.Unit(n, w.cap, np.ascontiguousarray(k[h]), np.ascontiguousarray(v[h]))
+        self.diverged = set()
+        self.qs = w.queries()
+        self.t = 0
+        self.out = torch.empty((w.L, w.B, w.Hq, 128), dtype=torch.float32, device=self.dev)
+        self.report = Report()
+
+    def close(self):
+        self.ctx.close()
+
+    def step(self, check: bool = True):
+        torch = self.torch
+        w = self.w
+        qb = self.qs.bf16()
+        qd = torch.from_numpy(qb.view(np.int16)).to(self.dev)
+        for l in range(w.L):
+            self.ctx.decode_step(l, qd[l], self.out[l])
+        torch.cuda.synchronize()
+        if check:
+            self._check(qb)
+        self.qs.advance()
+        self.t += 1
+        self.report.steps += 1
+
+    def _check(self, qb: np.ndarray):
+        w, t = self.w, self.t
+        out = self.out.cpu().numpy()
+        layers = sorted({l for (l, _, _) in self.units})
+        exports = {l: self.ctx.export(l, resolve=True) for l in layers}
+        rep = self.report
+        for l in layers:
+            ex = exports[l]
+            for b in range(w.B):
+                for h in range(w.Hkv):
+                    check_invariants(ex, b * w.Hkv + h, w.partitions(b), t, f"step {t} unit {(l, b, h)}")
+        for (l, b, h), u in self.oracle.items():
+            ex = exports[l]
+            ul = b * w.Hkv + h
+            where = f"step {t} unit {(l, b, h)}"
+            q = np.ascontiguousarray(qb[l, b, h * w.G:(h + 1) * w.G])
+            g_out = out[l, b, h * w.G:(h + 1) * w.G]
+            rep.compared_units += 1
+            if u.P == 0:
+                assert np.all(g_out == 0), f"{where}: empty request must give zeros"
+                continue
+            sc = O.scores(u.summ, q)
+            sel_o = O.topk(sc, w.topk)
+            keff = int(ex["keff"][ul])
+            sel_g = ex["sel"][ul][:keff].copy()
+            same = check_selection(sc, sel_o, sel_g, where)
+            key = (l, b, h)
+            if same and key not in self.diverged:
+                ss, hit, vic, mo = u.manage(sel_o, t)
+                o_out = u.attend(sel_o, ss, q)
+                assert mo.error == 0, f"{where}: oracle page pool error"
+                info = ex["unit_info"][ul]
+                assert np.array_equal(ex["sel_slot"][ul][:keff], ss), f"{where}: slots differ"
+                assert np.array_equal(ex["sel_hit"][ul][:keff].astype(bool), hit), f"{where}: hits differ"
+                assert (info[0], info[1], info[2], info[3], info[4], info[5]) == (
+                    mo.hits, mo.misses, mo.resident_before, mo.demand, mo.cutoff, mo.evicted), (
+                    f"{where}: manager record differs: gpu {info[:6].tolist()} oracle "
+                    f"{[mo.hits, mo.misses, mo.resident_before, mo.demand, mo.cutoff, mo.evicted]}")
+                sp, lu, rs = u.export()
+                assert np.array_equal(ex["slot_part"][ul], sp), f"{where}: slot map differs"
+                assert np.array_equal(ex["last_use"][ul], lu), f"{where}: timestamps differ"
+                assert np.array_equal(ex["resolve"][ul][:u.P], rs), f"{where}: page table differs"
+                assert ex["live_segs"][ul] == u.live_segments(), f"{where}: live segments differ"
+                rep.exact_units += 1
+                rep.evictions += mo.evicted
+                rep.misses += mo.misses
+                rep.hits += mo.hits
+            else:
+                if key not in self.diverged:
+                    self.diverged.add(key)
+                    rep.tie_divergences += 1
+                    rep.notes.append(f"{where}: tie-band divergence")
+                match = None
+                for cand in valid_sets(sc, sel_o):
+                    if np.array_equal(cand, sel_g):
+                        match = cand
+                        break
+                assert match is not None, f"{where}: GPU set is not one of the valid tie-band sets"
+                fresh = O.Unit(u.ntok, self.fresh_cap)
+                fresh.summ, fresh.host_pages = u.summ, u.host_pages
+                ss, _, _, _ = fresh.manage(match, 0)
+                o_out = fresh.attend(match, ss, q)
+            err = float(np.abs(g_out - o_out).max())
+            rep.max_out_err = max(rep.max_out_err, err)
+            assert err <= OUT_TOL, f"{where}: output max-abs error {err} > {OUT_TOL}"
+
+
+def sample_units(w: W.Workload, n: int, seed: int = 0) -> List[Tuple[int, int, int]]:
+    rng = np.random.default_rng(seed)
+    allu = [(l, b, h) for l in range(w.L) for b in range(w.B) for h in range(w.Hkv)]
+    idx = rng.choice(len(allu), size=min(n, len(allu)), replace=False)
+    return sorted(allu[i] for i in idx)

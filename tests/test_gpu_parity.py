@@ -1,0 +1,226 @@
+"""GPU path (through the C ABI) against the oracle, element by element.
+
+Bars: selected-partition sets and page state bit-exact (outside the 1e-5
+relative tie band of the oracle's scores), outputs within max-abs 2e-3.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workload as W
+from parity import OUT_TOL, Lockstep, sample_units
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, units=None, steps=None, **kw):
+    ls = Lockstep(w, units=units, **kw)
+    try:
+        for _ in range(steps if steps is not None else w.steps):
+            ls.step()
+        st = ls.ctx.stats()
+        assert st["device_error"] == 0
+        return ls.report, st
+    finally:
+        ls.close()
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_lockstep(seed):
+    rep, st = _run(W.tiny(seed))
+    assert rep.compared_units == 4 * 16
+    assert rep.max_out_err <= OUT_TOL
+    assert st["misses"] > 0 and st["hits"] > 0
+
+
+def test_mixed_shapes_ragged_gqa5():
+    """GQA 5, two layers, ragged last partitions, context shorter than a segment, evictions (2x buffer)."""
+    w = W.Workload("mixed", B=3, L=2, Hq=10, Hkv=2, ctx_len=[1000, 4113, 130], topk=8, buf_mult=2,
+                   drift_a=0.8, drift_c=0.2, steps=24, seed=5)
+    rep, st = _run(w)
+    assert rep.evictions > 0 and st["evictions"] > 0
+    assert rep.max_out_err <= OUT_TOL
+
+
+def test_gqa8_no_buffering():
+    """GQA 8 with capacity = k (1x): every changed partition evicts."""
+    w = W.Workload("gqa8", B=2, L=1, Hq=16, Hkv=2, ctx_len=[8192, 3000], topk=16, buf_mult=1,
+                   drift_a=0.7, drift_c=0.3, steps=20, seed=7)
+    rep, st = _run(w)
+    assert st["evictions"] > 0 and rep.evictions > 0
+
+
+def test_empty_short_and_k_above_partitions():
+    """An empty request (zero output), one-partition and few-partition requests (k > P)."""
+    w = W.Workload("edge", B=4, L=1, Hq=8, Hkv=2, ctx_len=[0, 64, 200, 5000], topk=8, buf_mult=2,
+                   drift_a=0.9, drift_c=0.1, steps=10, seed=9)
+    rep, st = _run(w)
+    assert rep.max_out_err <= OUT_TOL
+
+
+def test_many_segments_long_unit():
+    """A unit with 40 directory entries and a large top-k (P = 2560, k = 96, 3x buffer)."""
+    w = W.Workload("wide", B=1, L=1, Hq=8, Hkv=1, ctx_len=[2560 * 64], topk=96, buf_mult=3,
+                   drift_a=0.8, drift_c=0.2, steps=12, seed=13)
+    rep, st = _run(w)
+    assert st["live_segments"] > 1
+
+
+def test_summaries_match_oracle_index():
+    w = W.Workload("summ", B=2, L=2, Hq=4, Hkv=2, ctx_len=[777, 4096], topk=4, buf_mult=1,
+                   drift_a=0.9, drift_c=0.1, steps=1, seed=3)
+    from sparse_attention_tiered_gb300 import SpinContext
+    with SpinContext.for_workload(w) as ctx:
+        kv = {}
+        for l in range(w.L):
+            for b in range(w.B):
+                kv[(l, b)] = w.request_kv(l, b)
+                ctx.index_offload_host(b, l, *kv[(l, b)])
+        torch.cuda.synchronize()
+        for (l, b), (k, v) in kv.items():
+            for h in range(w.Hkv):
+                got = ctx.summaries(l, b, h).astype(np.float64)
+                ref = O.index(k[h])
+                # fp32 sum of bf16 values then one division: within a few fp32 ulps of the exact mean
+                assert np.allclose(got, ref, rtol=4e-7, atol=1e-7), np.abs(got - ref).max()
+
+
+def test_device_offload_equals_host_offload():
+    w = W.Workload("devoff", B=2, L=1, Hq=8, Hkv=2, ctx_len=[3000, 640], topk=4, buf_mult=2,
+                   drift_a=0.9, drift_c=0.1, steps=4, seed=17)
+    from sparse_attention_tiered_gb300 import SpinContext
+    outs = []
+    summs = []
+    for from_dev in (False, True):
+        ls = Lockstep(w, offload_from_device=from_dev)
+        try:
+            for _ in range(w.steps):
+                ls.step(check=True)
+            outs.append(ls.out.cpu().numpy())
+            summs.append([ls.ctx.summaries(0, b, h) for b in range(w.B) for h in range(w.Hkv)])
+        finally:
+            ls.close()
+    assert np.array_equal(outs[0], outs[1])
+    for a, b in zip(*summs):
+        assert np.array_equal(a, b)
+
+
+def test_resident_pages_byte_exact():
+    """Retrieve: every resident HBM page equals the oracle's host page byte for byte."""
+    w = W.Workload("bytes", B=1, L=1, Hq=4, Hkv=2, ctx_len=[64 * 50 + 9], topk=6, buf_mult=2,
+                   drift_a=0.7, drift_c=0.3, steps=6, seed=19)
+    ls = Lockstep(w)
+    try:
+        for _ in range(w.steps):
+            ls.step()
+        ex = ls.ctx.export(0)
+        for h in range(w.Hkv):
+            u = ls.oracle[(0, 0, h)]
+            for s, p in enumerate(ex["slot_part"][h]):
+                if p < 0:
+                    continue
+                page = ls.ctx.read_page(0, 0, h, s)
+                assert np.array_equal(page, u.host_pages[p]), f"slot {s} (partition {p}) differs"
+    finally:
+        ls.close()
+
+
+def test_host_buffer_entry_point_matches_device():
+    w = W.Workload("hostep", B=2, L=2, Hq=10, Hkv=2, ctx_len=[2048, 1500], topk=6, buf_mult=2,
+                   drift_a=0.9, drift_c=0.1, steps=5, seed=23)
+    from sparse_attention_tiered_gb300 import SpinContext
+    results = []
+    for use_host in (False, True):
+        with SpinContext.for_workload(w) as ctx:
+            for l in range(w.L):
+                for b in range(w.B):
+                    k, v = w.request_kv(l, b)
+                    ctx.index_offload_host(b, l, k, v)
+                    torch.cuda.synchronize()
+            qs = w.queries()
+            outs = []
+            q_pin = torch.empty((w.B, w.Hq, 128), dtype=torch.int16).pin_memory()
+            o_pin = torch.empty((w.B, w.Hq, 128), dtype=torch.float32).pin_memory()
+            od = torch.empty((w.B, w.Hq, 128), dtype=torch.float32, device="cuda")
+            for t in range(w.steps):
+                qb = qs.bf16()
+                for l in range(w.L):
+                    if use_host:
+                        q_pin.copy_(torch.from_numpy(qb[l].view(np.int16)))
+                        ctx.decode_step_host(l, q_pin.data_ptr(), o_pin.data_ptr())
+                        torch.cuda.synchronize()
+                        outs.append(o_pin.numpy().copy())
+                    else:
+                        qd = torch.from_numpy(qb[l].view(np.int16)).cuda()
+                        ctx.decode_step(l, qd, od)
+                        torch.cuda.synchronize()
+                        outs.append(od.cpu().numpy())
+                qs.advance()
+            results.append(np.stack(outs))
+    assert np.array_equal(results[0], results[1])
+
+
+def test_segment_pool_exhaustion_reports_capacity():
+    w = W.Workload("cap", B=1, L=1, Hq=2, Hkv=2, ctx_len=[64 * 300], topk=8, buf_mult=2,
+                   drift_a=0.5, drift_c=0.5, steps=3, seed=29)
+    from sparse_attention_tiered_gb300 import SpinContext, SpinError
+    from sparse_attention_tiered_gb300._binding import SPIN_ERR_CAPACITY
+    with SpinContext.for_workload(w, seg_pool_segments=2) as ctx:
+        k, v = w.request_kv(0, 0)
+        ctx.index_offload_host(0, 0, k, v)
+        q = torch.from_numpy(w.queries().bf16()[0].view(np.int16)).cuda()
+        out = torch.empty((1, 2, 128), dtype=torch.float32, device="cuda")
+        ctx.decode_step(0, q, out)
+        st = ctx.stats(check=False)
+        assert st["rc"] == SPIN_ERR_CAPACITY
+        with pytest.raises(SpinError):
+            ctx.decode_step(0, q, out)
+
+
+def test_invalid_arguments_and_order():
+    from sparse_attention_tiered_gb300 import SpinContext, SpinError
+    from sparse_attention_tiered_gb300._binding import SPIN_ERR_INVALID, SPIN_ERR_STATE
+    w = W.Workload("inv", B=2, L=1, Hq=4, Hkv=2, ctx_len=[128, 256], topk=2, buf_mult=1,
+                   drift_a=0.9, drift_c=0.1, steps=1, seed=0)
+    with SpinContext.for_workload(w) as ctx:
+        q = torch.zeros((2, 4, 128), dtype=torch.int16, device="cuda")
+        out = torch.empty((2, 4, 128), dtype=torch.float32, device="cuda")
+        with pytest.raises(SpinError) as e:
+            ctx.decode_step(0, q, out)          # nothing offloaded yet
+        assert e.value.code == SPIN_ERR_STATE
+        with pytest.raises(SpinError) as e:
+            ctx.decode_step(1, q, out)          # no such layer
+        assert e.value.code == SPIN_ERR_INVALID
+        k, v = w.request_kv(0, 0)
+        from sparse_attention_tiered_gb300 import spin_index_offload
+        with pytest.raises(SpinError) as e:      # wrong token count for request 1
+            spin_index_offload(ctx.h, 1, 0, k.ctypes.data, v.ctypes.data, 128, True)
+        assert e.value.code == SPIN_ERR_INVALID
+        with pytest.raises(SpinError) as e:      # misaligned source
+            spin_index_offload(ctx.h, 0, 0, k.ctypes.data + 2, v.ctypes.data, 128, True)
+        assert e.value.code == SPIN_ERR_INVALID
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: sampled units, the launch configuration the benchmark times.
+# ---------------------------------------------------------------------------
+FULL = [
+    ("qwen3_14b_32k", 24),
+    ("llama31_70b_128k", 16),
+    ("stress_m1", 24),
+    ("stress_m5", 24),
+    ("long_1m", 8),
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,nunits", FULL)
+def test_full_size_sampled(name, nunits):
+    w = W.by_name(name)
+    units = sample_units(w, nunits, seed=1)
+    rep, st = _run(w, units=units, gen_threads=0)
+    assert rep.max_out_err <= OUT_TOL
+    assert rep.tie_divergences <= max(1, rep.compared_units // 200), rep.notes
+    if name.startswith("stress"):
+        assert st["evictions"] > 0
