@@ -181,6 +181,31 @@ int spin_debug_read_page(spin_ctx* ctx, int32_t layer, int32_t b, int32_t h, int
 /* Synchronises, then copies the fp32 summaries [P_b][128] of unit (layer, b, h) to dst (host). */
 int spin_debug_summaries(spin_ctx* ctx, int32_t layer, int32_t b, int32_t h, float* dst);
 
+/* Allocation-free Select, for callers that cannot allocate device memory (code
+ * that runs while a CUDA graph is being captured, engines whose allocator owns all
+ * device memory, hosts that forbid run-time allocation); every other entry point
+ * needs the buffers spin_create allocates. No counterpart on the SPIN pages: this
+ * is the decode step's Select (fp32 score = (sum of the group's queries) . summary,
+ * per-unit top-k, equal scores to the lower index, ascending output) without the
+ * context. It calls no allocator of any kind.
+ *   summ  device fp32 [units][parts][128] partition summaries (16-byte aligned)
+ *   q     device bf16 [units][group][128] queries of each unit's query heads
+ *   sel   device int32 [units][topk] output: selected partitions, ascending, -1 padded
+ *         when parts < topk
+ * Limits: units * parts <= SPIN_NOALLOC_MAX_SCORES, parts <= 32768, group <= 16,
+ * topk <= 512; larger sizes return SPIN_ERR_INVALID. The scores live in one static
+ * device array of SPIN_NOALLOC_MAX_SCORES floats (4 MiB) that every GPU loading the
+ * library holds until exit. All calls share it and it keeps the last call's
+ * contents; calls whose work overlaps on the GPU (different streams, different
+ * host threads on one device) race on it and must be serialised by the caller.
+ * The first call on a device looks up that array's device address and sets a
+ * kernel attribute (once per device, on the current device); make that first call
+ * before any stream capture. Asynchronous on `stream`; on failure
+ * spin_last_error(NULL) gives the reason. */
+#define SPIN_NOALLOC_MAX_SCORES (1 << 20)
+int spin_select_noalloc(const float* summ, const uint16_t* q, int32_t units, int32_t parts, int32_t group,
+                        int32_t topk, int32_t* sel, spin_stream_t stream);
+
 /* Releases everything the context owns (synchronises first). NULL is a no-op. */
 void spin_destroy(spin_ctx* ctx);
 

@@ -31,10 +31,12 @@ SPIN_FLAG_TEST_FAIL_PINNED = 1 << 16
 HEAD_DIM = 128
 PART_TOKENS = 64
 PAGE_BYTES = 32768
+SPIN_NOALLOC_MAX_SCORES_DEFAULT = 1 << 20  # SPIN_NOALLOC_MAX_SCORES in include/spin.h
 
 # Every symbol include/spin.h declares.
 EXPORTS = ("spin_create", "spin_index_offload", "spin_decode_step", "spin_decode_step_host", "spin_stats",
-           "spin_debug_export", "spin_debug_read_page", "spin_debug_summaries", "spin_destroy", "spin_last_error")
+           "spin_debug_export", "spin_debug_read_page", "spin_debug_summaries", "spin_destroy", "spin_last_error",
+           "spin_select_noalloc")
 
 
 class SpinError(RuntimeError):
@@ -122,6 +124,8 @@ def load(build_if_missing: bool = True):
             L.spin_debug_summaries.restype = ctypes.c_int
             L.spin_destroy.argtypes = [vp]
             L.spin_destroy.restype = None
+            L.spin_select_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
+            L.spin_select_noalloc.restype = ctypes.c_int
             L.spin_last_error.argtypes = [vp]
             L.spin_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -176,6 +180,11 @@ def spin_debug_read_page(ctx: int, layer: int, b: int, h: int, slot: int, dst_pt
 
 def spin_debug_summaries(ctx: int, layer: int, b: int, h: int, dst_ptr: int):
     _check(load().spin_debug_summaries(ctx, layer, b, h, dst_ptr), ctx)
+
+
+def spin_select_noalloc(summ_ptr: int, q_ptr: int, units: int, parts: int, group: int, topk: int, sel_ptr: int,
+                        stream: int = 0):
+    _check(load().spin_select_noalloc(summ_ptr, q_ptr, units, parts, group, topk, sel_ptr, stream))
 
 
 def spin_destroy(ctx: int):

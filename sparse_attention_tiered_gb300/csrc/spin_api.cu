@@ -474,6 +474,11 @@ int check_layer(spin_ctx* c, int layer) {
 
 }  // namespace
 
+namespace spin {
+// Message for spin_last_error(NULL) from entry points that have no context.
+void set_global_error(const char* msg) { g_create_error = msg; }
+}  // namespace spin
+
 extern "C" {
 
 int spin_create(const spin_config* cfg, spin_ctx** out) {
