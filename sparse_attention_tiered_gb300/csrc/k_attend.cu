@@ -6,25 +6,37 @@
 // "Spin的核心设计" 1 and Figure 3, 2 and Figure 5 step 4; gist.science/pt section
 // 2A). The pages give no kernel design; everything below is this library's.
 //
+// One cooperative persistent kernel per layer step does both, one CTA per SM:
+//   * retriever warps walk the step's miss list (host page -> HBM slot, 16-byte
+//     zero-copy loads over the host link), and publish each copied page with a
+//     release store of the step tag into its ready flag;
+//   * a producer warp (one elected lane) streams pages through TMA into a 4-stage
+//     shared-memory ring guarded by mbarriers: first the resident pages (hits) in
+//     tasks of up to `ppt` pages of one unit, then the retrieved pages in miss-list
+//     order, each after an acquire of its ready flag;
+//   * four consumer warps run the attention math on every staged page.
+// So the attention over the hits (HBM bound) hides under the retrieval (host-link
+// bound) and each retrieved page is attended as soon as it lands (and from L2).
+//
 // Attention data layout. A page (32 KiB) holds K[64][128] then V[64][128] bf16.
 // A TMA tensor map views the whole HBM pool as a 2-D bf16 tensor of 128 columns
 // and (slots * 128) rows; a page is loaded as four 64x64 boxes (K left/right, V
-// left/right) with the 128-byte swizzle, so ldmatrix reads are bank-conflict free.
+// left/right) with the 128-byte swizzle, so ldmatrix reads are bank-conflict
+// free. The first page of a task also brings the unit's G query rows (bulk copy).
 //
-// Work split. One persistent CTA per SM: one producer warp (one elected lane
-// issues TMA loads into a 4-stage ring of pages, guarded by mbarriers) and four
-// consumer warps. A task is up to `ppt` consecutive selected pages of one unit;
-// tasks are taken from a device counter. Every consumer warp handles 16 of the
-// 64 tokens of each page for all G query heads of the unit:
-//   S[16 heads][16 tokens] = Q K^T      mma.m16n8k16 bf16 -> fp32 (heads padded to 16)
-//   online softmax in fp32 (base-2 exponent, scale log2(e)/sqrt(128))
-//   O[16][128] += P V                    P split into bf16 hi + lo parts, two mma each
+// Consumer math. Every consumer warp handles 16 of the 64 tokens of each page for
+// all G query heads of the unit, with tokens as the M dimension:
+//   S^T[16 tokens][8 heads] = K Q^T        mma.m16n8k16 bf16 -> fp32 (heads padded to 8)
+//   online softmax per head in fp32 (base-2 exponent, scale log2(e)/sqrt(128))
+//   O^T[128][8 heads] += V^T P             P transposed in registers (movmatrix) and
+//                                          split into bf16 hi + lo parts, two mma each
 // At the end of a task the four warps merge (m, l, O) in shared memory and write
 // one partial (m, l, acc[128]) per query head; the combine kernel merges the
 // partials of a unit into the output.
 //
-// Every wait on an mbarrier is bounded in time; a wait that runs out sets the
-// device error word, stops issuing work and drains the loads already issued.
+// Every wait (mbarrier or ready flag) is bounded in time; a wait that runs out
+// sets the device error word, stops issuing work and drains the copies already
+// issued.
 #include "spin_internal.cuh"
 
 namespace spin {
@@ -33,17 +45,26 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kCWarps = 4;
-constexpr int kAttnThreads = (kCWarps + 1) * 32;
-constexpr int kMergeFloats = 16 * kD + 32;  // O[16][128], m[16], l[16]
-constexpr float kScaleLog2 = 0.12751743074173449f;  // log2(e) / sqrt(128)
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
+// Retriever warps per CTA: 8 when the group fits one 8-head tile (140 registers a
+// thread), 4 for two tiles (the register file bounds threads x registers).
+template <int NT>
+struct Roles {
+  static constexpr int kRWarps = NT == 1 ? 8 : 4;
+  static constexpr int kThreads = (1 + kCWarps + kRWarps) * 32;
+};
+constexpr int kQBytes = kMaxGroup * kD * 2;            // query rows of one unit (<= 16 heads)
+constexpr int kStageBytes = kPageBytes + kQBytes;       // 36 KiB, a multiple of 1024
+constexpr int kMergeRow = kD + 4;                       // padded row of the merge buffer
+constexpr int kMergeFloats = 16 * kMergeRow + 32;       // O[16 heads][128+4], m[16], l[16]
+constexpr float kScaleLog2 = 0.12751743074173449f;      // log2(e) / sqrt(128)
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
 
 struct StageMeta {
-  int task, ul, j, valid;
+  int part, ul, valid, first;  // partial slot of the task, unit, valid tokens, first page of the task
 };
 
 struct AttnSmem {
-  uint8_t* ring;      // kStages x 32 KiB, 1024-aligned
+  uint8_t* ring;      // kStages x kStageBytes, 1024-aligned
   float* merge;       // kCWarps x kMergeFloats
   uint64_t* full;     // [kStages]
   uint64_t* empty;    // [kStages]
@@ -60,7 +81,7 @@ __host__ __device__ inline size_t attn_smem_layout(AttnSmem* s, uint8_t* base) {
     off += bytes;
     return p;
   };
-  uint8_t* ring = take((size_t)kStages * kPageBytes, 1024);
+  uint8_t* ring = take((size_t)kStages * kStageBytes, 1024);
   uint8_t* merge = take(sizeof(float) * kCWarps * kMergeFloats, 16);
   uint8_t* full = take(sizeof(uint64_t) * kStages, 8);
   uint8_t* empty = take(sizeof(uint64_t) * kStages, 8);
@@ -135,6 +156,29 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -170,15 +214,18 @@ __device__ __forceinline__ uint32_t swz(int r, int cd) {
 }
 
 // ---------------------------------------------------------------------------
-// Attention kernel
+// Retrieve + attention kernel. NT = number of 8-head tiles (G <= 8 * NT).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kAttnThreads, 1)
-attention_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_tasks) {
+template <int NT>
+__global__ void __launch_bounds__(Roles<NT>::kThreads, 1)
+attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_hit_tasks) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   AttnSmem sm;
   attn_smem_layout(&sm, base);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_miss = a.counters[kCtrMiss];
+  const int tag = a.counters[kCtrStep] + 1;  // ready-flag value of this step (flags are never reset)
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -193,52 +240,104 @@ attention_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_ta
   __syncthreads();
   volatile int* abort_flag = sm.abort_flag;
 
+  if (warp > kCWarps) {
+    // ------------------------------ retrievers ------------------------------
+    constexpr int kVec = kPageBytes / 16;  // 2048 x 16 B
+    constexpr int kUnroll = 16;            // 16 x 16 B in flight per lane
+    for (;;) {
+      int m = 0;
+      if (lane == 0) m = atomicAdd(&a.counters[kCtrRetrieve], 1);
+      m = __shfl_sync(0xffffffffu, m, 0);
+      if (m >= n_miss) break;
+      const uint4* src = reinterpret_cast<const uint4*>(a.host_store + a.miss_src[m] * kPageElems);
+      uint4* dst = reinterpret_cast<uint4*>(a.pool + a.miss_dst[m] * kPageElems);
+#pragma unroll 1
+      for (int c = 0; c < kVec; c += 32 * kUnroll) {
+        uint4 r[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) r[u] = __ldcs(src + c + u * 32 + lane);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) dst[c + u * 32 + lane] = r[u];
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release(a.ready + m, tag);
+    }
+    return;
+  }
+
   if (warp == kCWarps) {
     // ------------------------------ producer ------------------------------
     if (lane != 0) return;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+    const uint32_t qbytes = (uint32_t)a.G * kD * 2;
+    const int U = a.B * a.Hkv;
     int i = 0;
     bool ok = true;
-    for (;;) {
-      if (*abort_flag) { ok = false; break; }
-      const int task = atomicAdd(&a.counters[1], 1);
-      if (task >= n_tasks) break;
-      const int ul = task / a.n_chunks, c = task - ul * a.n_chunks;
-      const int keff = a.keff[ul];
-      const int j0 = c * a.ppt, j1 = min(keff, j0 + a.ppt);
-      const int b = ul / a.Hkv;
-      const int P = a.P_b[b], ntok = a.ntok_b[b];
-      const int64_t unit = a.unit_base + ul;
-      for (int j = j0; j < j1; ++j) {
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) { ok = false; break; }
-        const int p = a.sel[(int64_t)ul * a.k + j];
-        const int slot = a.sel_slot[(int64_t)ul * a.k + j];
-        StageMeta m;
-        m.task = task;
-        m.ul = ul;
-        m.j = j;
-        m.valid = (p == P - 1) ? ntok - p * kPart : kPart;
-        sm.meta[st] = m;
-        const uint32_t fb = smem_u32(&sm.full[st]);
-        mbar_arrive_expect_tx(fb, kPageBytes);
-        const int y = (int)((unit * a.cap + slot) * 128);
-        const uint32_t dst = smem_u32(sm.ring + (size_t)st * kPageBytes);
-        tma_load_2d(dst, &tmap, fb, 0, y);
-        tma_load_2d(dst + 8192, &tmap, fb, 64, y);
-        tma_load_2d(dst + 16384, &tmap, fb, 0, y + 64);
-        tma_load_2d(dst + 24576, &tmap, fb, 64, y + 64);
-        ++i;
+    // Stage one page into the ring. part = partial slot of its task.
+    auto issue = [&](int ul, int att, int part, bool first) -> bool {
+      const int st = i % kStages;
+      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      if (!mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) return false;
+      const int slot = a.att_slot[att];
+      StageMeta m;
+      m.part = part;
+      m.ul = ul;
+      m.valid = a.att_valid[att];
+      m.first = first;
+      sm.meta[st] = m;
+      const uint32_t fb = smem_u32(&sm.full[st]);
+      mbar_arrive_expect_tx(fb, kPageBytes + (first ? qbytes : 0u));
+      const int y = (int)(((a.unit_base + ul) * a.cap + slot) * 128);
+      const uint32_t dst = smem_u32(sm.ring + (size_t)st * kStageBytes);
+      tma_load_2d(dst, &tmap, fb, 0, y);
+      tma_load_2d(dst + 8192, &tmap, fb, 64, y);
+      tma_load_2d(dst + 16384, &tmap, fb, 0, y + 64);
+      tma_load_2d(dst + 24576, &tmap, fb, 64, y + 64);
+      if (first) {
+        const int b = ul / a.Hkv, h = ul - b * a.Hkv;
+        bulk_load(dst + kPageBytes, a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, qbytes, fb);
       }
-      if (!ok) break;
+      ++i;
+      return true;
+    };
+    // 1) resident pages: tasks of up to ppt pages of one unit
+    int next = atomicAdd(&a.counters[kCtrTaskHits], 1);
+    while (ok) {
+      const int task = next;
+      if (task >= n_hit_tasks) break;
+      next = atomicAdd(&a.counters[kCtrTaskHits], 1);  // prefetch the following task
+      if (*abort_flag) { ok = false; break; }
+      const int ul = task / a.n_chunks, c = task - ul * a.n_chunks;
+      const int nh = a.n_hit[ul];
+      const int j0 = c * a.ppt, j1 = min(nh, j0 + a.ppt);
+      for (int j = j0; j < j1 && ok; ++j) ok = issue(ul, ul * a.k + j, task, j == j0);
+    }
+    // 2) retrieved pages, in miss-list order, each once its copy is published
+    while (ok) {
+      const int m = atomicAdd(&a.counters[kCtrTaskMisses], 1);
+      if (m >= n_miss) break;
+      if (*abort_flag) { ok = false; break; }
+      bool ready = ld_acquire(a.ready + m) == tag;
+      if (!ready) {
+        const unsigned long long t0 = globaltimer_ns();
+        for (uint32_t it = 1; it < (1u << 30) && !ready; ++it) {
+          ready = ld_acquire(a.ready + m) == tag;
+          if (!ready && (it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
+        }
+      }
+      if (!ready) { ok = false; break; }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what the generic stores wrote
+      const int att = a.miss_att[m];
+      const int ul = att / a.k;
+      ok = issue(ul, att, U * a.n_chunks + att, true);
     }
     if (ok) {
       // sentinel: tells the consumers that no task follows
       const int st = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
       if (mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) {
-        sm.meta[st].task = -1;
+        sm.meta[st].part = -1;
         mbar_arrive(smem_u32(&sm.full[st]));
       } else {
         ok = false;
@@ -247,7 +346,7 @@ attention_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_ta
     if (!ok) {
       atomicOr(a.err, kErrTimeout);
       *abort_flag = 1;
-      // drain the loads already issued before leaving (bounded)
+      // drain the copies already issued before leaving (bounded)
       for (int m = max(0, i - kStages); m < i; ++m)
         (void)mbar_wait(smem_u32(&sm.full[m % kStages]), (uint32_t)(m / kStages) & 1u);
     }
@@ -258,15 +357,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_ta
   const int w = warp;               // tokens 16w .. 16w+15 of every page
   const int t0 = 16 * w;
   const int mi = lane >> 3, ri = lane & 7;
-  const int qr = lane >> 2, q4 = lane & 3;
-  const int tokK = t0 + ri + ((mi >> 1) << 3);
-  const int tokV = t0 + ri + ((mi & 1) << 3);
+  const int g4 = lane >> 2, q4 = lane & 3;
+  const int tokA = t0 + ri + ((mi & 1) << 3);   // K rows feeding the A operand
+  const int tokV = t0 + ri + ((mi >> 1) << 3);  // V rows feeding the transposed A operand
   float* mw = sm.merge + w * kMergeFloats;
 
-  uint32_t qa[8][4];
-  float o[16][4];
-  float mrow[2], lrow[2];
-  int cur = -1, cur_ul = -1;
+  uint32_t qb[NT][8][2];
+  float o[8][NT][4];
+  float mrow[NT][2], lrow[NT][2];
+  int cur = -1;
   uint32_t mph = 0;
   int i = 0;
 
@@ -279,24 +378,29 @@ attention_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_ta
       break;
     }
     const StageMeta m = sm.meta[st];
-    if (m.task != cur || m.task < 0) {
+    uint8_t* stage = sm.ring + (size_t)st * kStageBytes;
+    if (m.part != cur || m.part < 0) {
       if (cur >= 0) {
         // ---- finalize the previous task: merge the four warps, write partials ----
-        const float l0 = lrow[0] + __shfl_xor_sync(0xffffffffu, lrow[0], 1);
-        const float l0b = l0 + __shfl_xor_sync(0xffffffffu, l0, 2);
-        const float l1 = lrow[1] + __shfl_xor_sync(0xffffffffu, lrow[1], 1);
-        const float l1b = l1 + __shfl_xor_sync(0xffffffffu, l1, 2);
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-          *reinterpret_cast<float2*>(&mw[qr * kD + 8 * n + 2 * q4]) = make_float2(o[n][0], o[n][1]);
-          *reinterpret_cast<float2*>(&mw[(qr + 8) * kD + 8 * n + 2 * q4]) = make_float2(o[n][2], o[n][3]);
-        }
-        if (q4 == 0) {
-          mw[16 * kD + qr] = mrow[0];
-          mw[16 * kD + qr + 8] = mrow[1];
-          mw[16 * kD + 16 + qr] = l0b;
-          mw[16 * kD + 16 + qr + 8] = l1b;
-        }
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float l = lrow[nt][e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int hh = 8 * nt + 2 * q4 + e;
+#pragma unroll
+            for (int md = 0; md < 8; ++md) {
+              mw[hh * kMergeRow + 16 * md + g4] = o[md][nt][e];
+              mw[hh * kMergeRow + 16 * md + g4 + 8] = o[md][nt][2 + e];
+            }
+            if (g4 == 0) {
+              mw[16 * kMergeRow + hh] = mrow[nt][e];
+              mw[16 * kMergeRow + 16 + hh] = l;
+            }
+          }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sm.mrg[0]));
         if (!mbar_wait(smem_u32(&sm.mrg[0]), mph)) {
@@ -308,15 +412,15 @@ attention_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_ta
         for (int g = 0; g < a.G; ++g) {
           float M = -INFINITY;
 #pragma unroll
-          for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, sm.merge[ww * kMergeFloats + 16 * kD + g]);
+          for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, sm.merge[ww * kMergeFloats + 16 * kMergeRow + g]);
           float L = 0.f, acc = 0.f;
           if (M != -INFINITY) {
 #pragma unroll
             for (int ww = 0; ww < kCWarps; ++ww) {
               const float* src = sm.merge + ww * kMergeFloats;
-              const float sc = exp2f(src[16 * kD + g] - M);
-              L = fmaf(sc, src[16 * kD + 16 + g], L);
-              acc = fmaf(sc, src[g * kD + d], acc);
+              const float sc = exp2f(src[16 * kMergeRow + g] - M);
+              L = fmaf(sc, src[16 * kMergeRow + 16 + g], L);
+              acc = fmaf(sc, src[g * kMergeRow + d], acc);
             }
           }
           float* part = a.partials + ((int64_t)cur * a.G + g) * kPartialStride;
@@ -335,99 +439,84 @@ attention_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_ta
         }
         mph ^= 1u;
       }
-      if (m.task < 0) break;
-      cur = m.task;
-      if (m.ul != cur_ul) {
-        cur_ul = m.ul;
-        const int b = m.ul / a.Hkv, h = m.ul - b * a.Hkv;
-        const uint16_t* qb = a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD;
-        const bool r0 = qr < a.G, r1 = qr + 8 < a.G;
+      if (m.part < 0) break;
+      cur = m.part;
+      // query rows of the unit, brought with the task's first page: B operand fragments
+      const uint8_t* qs = stage + kPageBytes;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int head = 8 * nt + g4;
+        const bool live = head < a.G;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const int c0 = 16 * kk + 2 * q4;
-          qa[kk][0] = r0 ? *reinterpret_cast<const uint32_t*>(qb + qr * kD + c0) : 0u;
-          qa[kk][1] = r1 ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * kD + c0) : 0u;
-          qa[kk][2] = r0 ? *reinterpret_cast<const uint32_t*>(qb + qr * kD + c0 + 8) : 0u;
-          qa[kk][3] = r1 ? *reinterpret_cast<const uint32_t*>(qb + (qr + 8) * kD + c0 + 8) : 0u;
+          qb[nt][kk][0] = live ? *reinterpret_cast<const uint32_t*>(qs + head * 256 + (16 * kk + 2 * q4) * 2) : 0u;
+          qb[nt][kk][1] = live ? *reinterpret_cast<const uint32_t*>(qs + head * 256 + (16 * kk + 8 + 2 * q4) * 2)
+                               : 0u;
         }
-      }
+        mrow[nt][0] = mrow[nt][1] = -INFINITY;
+        lrow[nt][0] = lrow[nt][1] = 0.f;
 #pragma unroll
-      for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-      mrow[0] = mrow[1] = -INFINITY;
-      lrow[0] = lrow[1] = 0.f;
+        for (int md = 0; md < 8; ++md) o[md][nt][0] = o[md][nt][1] = o[md][nt][2] = o[md][nt][3] = 0.f;
+      }
     }
 
     // ---------------- one page: tokens t0..t0+15 ----------------
-    const uint32_t kb = smem_u32(sm.ring + (size_t)st * kPageBytes);
+    const uint32_t kb = smem_u32(stage);
     const uint32_t vb = kb + 16384;
-    float s[2][4];
+    float s[NT][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[0][e] = s[1][e] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(kb + swz(tokK, 2 * kk + (mi & 1)), b0, b1, b2, b3);
-      mma_bf16(s[0], qa[kk], b0, b1);
-      mma_bf16(s[1], qa[kk], b2, b3);
-    }
-    // online softmax (base 2)
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+      uint32_t af[4];
+      ldsm_x4(kb + swz(tokA, 2 * kk + (mi >> 1)), af[0], af[1], af[2], af[3]);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+    }
+    // online softmax per head (column), over this warp's 16 tokens (rows)
+    const bool v0 = (t0 + g4) < m.valid, v1 = (t0 + g4 + 8) < m.valid;
+    uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float p[4];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const bool valid = (t0 + 8 * nt + 2 * q4 + e) < m.valid;
-        s[nt][e] = valid ? s[nt][e] * kScaleLog2 : -INFINITY;
-        s[nt][2 + e] = valid ? s[nt][2 + e] * kScaleLog2 : -INFINITY;
-        mx0 = fmaxf(mx0, s[nt][e]);
-        mx1 = fmaxf(mx1, s[nt][2 + e]);
+        const float x0 = v0 ? s[nt][e] * kScaleLog2 : -INFINITY;
+        const float x1 = v1 ? s[nt][2 + e] * kScaleLog2 : -INFINITY;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mn = fmaxf(mrow[nt][e], mx);
+        const float al = (mn == -INFINITY) ? 1.f : exp2f(mrow[nt][e] - mn);
+        p[e] = (mn == -INFINITY) ? 0.f : exp2f(x0 - mn);
+        p[2 + e] = (mn == -INFINITY) ? 0.f : exp2f(x1 - mn);
+        lrow[nt][e] = fmaf(lrow[nt][e], al, p[e] + p[2 + e]);
+        mrow[nt][e] = mn;
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          o[md][nt][e] *= al;
+          o[md][nt][2 + e] *= al;
+        }
       }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(mrow[0], mx0), mn1 = fmaxf(mrow[1], mx1);
-    const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(mrow[0] - mn0);
-    const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(mrow[1] - mn1);
-    float pr[2][4];
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        pr[nt][e] = (mn0 == -INFINITY) ? 0.f : exp2f(s[nt][e] - mn0);
-        pr[nt][2 + e] = (mn1 == -INFINITY) ? 0.f : exp2f(s[nt][2 + e] - mn1);
-        ps0 += pr[nt][e];
-        ps1 += pr[nt][2 + e];
-      }
-    lrow[0] = fmaf(lrow[0], al0, ps0);
-    lrow[1] = fmaf(lrow[1], al1, ps1);
-    mrow[0] = mn0;
-    mrow[1] = mn1;
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-      o[n][0] *= al0;
-      o[n][1] *= al0;
-      o[n][2] *= al1;
-      o[n][3] *= al1;
+      // P^T fragments (token rows, head columns) -> B operand (head rows, token columns)
+      const uint32_t h0 = pack_bf16(p[0], p[1]), h1 = pack_bf16(p[2], p[3]);
+      const uint32_t l0 = pack_bf16(p[0] - bf16_lo_f(h0), p[1] - bf16_hi_f(h0));
+      const uint32_t l1 = pack_bf16(p[2] - bf16_lo_f(h1), p[3] - bf16_hi_f(h1));
+      bh[nt][0] = movmatrix_t(h0);
+      bh[nt][1] = movmatrix_t(h1);
+      bl[nt][0] = movmatrix_t(l0);
+      bl[nt][1] = movmatrix_t(l1);
     }
-    uint32_t ph_[4], pl_[4];
-    ph_[0] = pack_bf16(pr[0][0], pr[0][1]);
-    ph_[1] = pack_bf16(pr[0][2], pr[0][3]);
-    ph_[2] = pack_bf16(pr[1][0], pr[1][1]);
-    ph_[3] = pack_bf16(pr[1][2], pr[1][3]);
-    pl_[0] = pack_bf16(pr[0][0] - bf16_lo_f(ph_[0]), pr[0][1] - bf16_hi_f(ph_[0]));
-    pl_[1] = pack_bf16(pr[0][2] - bf16_lo_f(ph_[1]), pr[0][3] - bf16_hi_f(ph_[1]));
-    pl_[2] = pack_bf16(pr[1][0] - bf16_lo_f(ph_[2]), pr[1][1] - bf16_hi_f(ph_[2]));
-    pl_[3] = pack_bf16(pr[1][2] - bf16_lo_f(ph_[3]), pr[1][3] - bf16_hi_f(ph_[3]));
 #pragma unroll
-    for (int nd2 = 0; nd2 < 8; ++nd2) {
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vb + swz(tokV, 2 * nd2 + (mi >> 1)), v0, v1, v2, v3);
-      mma_bf16(o[2 * nd2], ph_, v0, v1);
-      mma_bf16(o[2 * nd2], pl_, v0, v1);
-      mma_bf16(o[2 * nd2 + 1], ph_, v2, v3);
-      mma_bf16(o[2 * nd2 + 1], pl_, v2, v3);
+    for (int md = 0; md < 8; ++md) {
+      uint32_t af[4];
+      ldsm_x4_t(vb + swz(tokV, 2 * md + (mi & 1)), af[0], af[1], af[2], af[3]);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_bf16(o[md][nt], af, bh[nt][0], bh[nt][1]);
+        mma_bf16(o[md][nt], af, bl[nt][0], bl[nt][1]);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
@@ -436,50 +525,33 @@ attention_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_ta
 }
 
 // ---------------------------------------------------------------------------
-// Retrieve: copy each missing page from the pinned host store into its HBM slot.
-// One warp per page, 16-byte loads over the host link, 8 in flight per lane.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) retrieve_kernel(LayerArgs a) {
-  const int n = a.counters[0];
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
-  constexpr int kVec = kPageBytes / 16;  // 2048
-  for (int m = gw; m < n; m += nw) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.host_store + a.miss_src[m] * kPageElems);
-    uint4* dst = reinterpret_cast<uint4*>(a.pool + a.miss_dst[m] * kPageElems);
-#pragma unroll 1
-    for (int c = 0; c < kVec; c += 32 * 8) {
-      uint4 r[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) r[u] = __ldcs(src + c + u * 32 + lane);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) dst[c + u * 32 + lane] = r[u];
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Combine: out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c over the
-// unit's task partials. One warp per query head, four columns per lane. Also
-// closes the step: resets the miss and task counters, advances t.
+// unit's partials (its hit tasks and its retrieved pages). One warp per query
+// head, four columns per lane. Also closes the step: resets the miss, task and
+// retrieve counters and advances t.
 // ---------------------------------------------------------------------------
 __global__ void combine_kernel(LayerArgs a) {
   const int ul = blockIdx.x;
   const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (g < a.G) {
     const int b = ul / a.Hkv, h = ul - b * a.Hkv;
-    const int keff = a.keff[ul];
-    const int nch = (keff + a.ppt - 1) / a.ppt;
+    const int keff = a.keff[ul], nh = a.n_hit[ul];
+    const int nc = (nh + a.ppt - 1) / a.ppt;
+    const int U = a.B * a.Hkv;
     float4* out = reinterpret_cast<float4*>(a.out + ((int64_t)b * a.Hq + (int64_t)h * a.G + g) * kD);
+    // partial slots: hit tasks ul * n_chunks + c (c < nc), retrieved pages U * n_chunks + ul * k + j (nh <= j < keff)
+    auto part_ptr = [&](int i) -> const float* {
+      const int64_t slot = i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.k + nh + (i - nc);
+      return a.partials + (slot * a.G + g) * kPartialStride;
+    };
+    const int n = nc + (keff - nh);
     float M = -INFINITY;
-    for (int c = 0; c < nch; ++c)
-      M = fmaxf(M, a.partials[(((int64_t)ul * a.n_chunks + c) * a.G + g) * kPartialStride]);
+    for (int i = 0; i < n; ++i) M = fmaxf(M, part_ptr(i)[0]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
     if (M != -INFINITY) {
-      for (int c = 0; c < nch; ++c) {
-        const float* part = a.partials + (((int64_t)ul * a.n_chunks + c) * a.G + g) * kPartialStride;
+      for (int i = 0; i < n; ++i) {
+        const float* part = part_ptr(i);
         const float sc = exp2f(part[0] - M);
         L = fmaf(sc, part[1], L);
         const float4 v = reinterpret_cast<const float4*>(part + 4)[lane];
@@ -493,9 +565,11 @@ __global__ void combine_kernel(LayerArgs a) {
     out[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
   if (ul == 0 && threadIdx.x == 0) {
-    a.counters[0] = 0;
-    a.counters[1] = 0;
-    a.counters[2] += 1;
+    a.counters[kCtrMiss] = 0;
+    a.counters[kCtrTaskHits] = 0;
+    a.counters[kCtrTaskMisses] = 0;
+    a.counters[kCtrRetrieve] = 0;
+    a.counters[kCtrStep] += 1;
   }
 }
 
@@ -504,19 +578,28 @@ __global__ void combine_kernel(LayerArgs a) {
 size_t attention_smem_bytes() { return attn_smem_layout(nullptr, nullptr) + 1024; }
 
 cudaError_t attention_configure() {
-  return cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)attention_smem_bytes());
+  const int kMaxShared = 100;  // cudaSharedmemCarveoutMaxShared
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(attend_retrieve_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)attention_smem_bytes())) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(attend_retrieve_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)attention_smem_bytes())) != cudaSuccess)
+    return e;
+  // The small kernels keep the SM in its largest shared-memory configuration, so the
+  // persistent CTAs never wait for a carveout switch.
+  return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMaxShared);
 }
 
-cudaError_t launch_attention(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st) {
-  const int n_tasks = a.B * a.Hkv * a.n_chunks;
-  attention_kernel<<<grid, kAttnThreads, attention_smem_bytes(), st>>>(*tmap, a, n_tasks);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_retrieve(const LayerArgs& a, int grid, cudaStream_t st) {
-  retrieve_kernel<<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_attend_retrieve(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st) {
+  int n_hit_tasks = a.B * a.Hkv * a.n_chunks;
+  LayerArgs args = a;
+  void* params[] = {const_cast<CUtensorMap*>(tmap), &args, &n_hit_tasks};
+  if (a.G <= 8)
+    return cudaLaunchCooperativeKernel((const void*)attend_retrieve_kernel<1>, dim3(grid),
+                                       dim3(Roles<1>::kThreads), params, attention_smem_bytes(), st);
+  return cudaLaunchCooperativeKernel((const void*)attend_retrieve_kernel<2>, dim3(grid), dim3(Roles<2>::kThreads),
+                                     params, attention_smem_bytes(), st);
 }
 
 cudaError_t launch_combine(const LayerArgs& a, cudaStream_t st) {

@@ -103,6 +103,7 @@ struct SelSmem {
   int32_t* sel;       // [k]
   int32_t* sslot;     // [k]
   int32_t* hit;       // [k]
+  int32_t* mrank;     // [k] misses before j (exclusive)
   int32_t* dirs;      // [D]
   uint32_t* whist;    // [kSelWarps][256]
   uint8_t* mand;      // [cap]
@@ -124,6 +125,7 @@ __host__ __device__ inline size_t sel_smem_layout(int P_max, int cap, int k, int
   uint8_t* sel = take(sizeof(int32_t) * k);
   uint8_t* ss = take(sizeof(int32_t) * k);
   uint8_t* hit = take(sizeof(int32_t) * k);
+  uint8_t* mrank = take(sizeof(int32_t) * k);
   uint8_t* dirs = take(sizeof(int32_t) * (D > 0 ? D : 1));
   uint8_t* wh = take(sizeof(uint32_t) * kSelWarps * 256);
   uint8_t* mand = take((size_t)cap);
@@ -135,6 +137,7 @@ __host__ __device__ inline size_t sel_smem_layout(int P_max, int cap, int k, int
     s->sel = (int32_t*)sel;
     s->sslot = (int32_t*)ss;
     s->hit = (int32_t*)hit;
+    s->mrank = (int32_t*)mrank;
     s->dirs = (int32_t*)dirs;
     s->whist = (uint32_t*)wh;
     s->mand = mand;
@@ -208,7 +211,7 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   const int k = a.k, cap = a.cap;
   const int keff = P < k ? P : k;
   const int64_t unit = a.unit_base + ul;
-  const int t = a.counters[2];
+  const int t = a.counters[kCtrStep];
   // After a pool or invariant error the page state is no longer trusted: leave it as is.
   if (*((volatile uint32_t*)a.err) & (kErrCapacity | kErrInternal)) return;
 
@@ -431,6 +434,7 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       int tot;
       const int ex = block_exclusive_scan(m, &tot, s_scan);
       if (m) sm.hit[j] = -1 - (base + ex);  // encode: hit = 1, miss = -1 - rank
+      if (j < keff) sm.mrank[j] = base + ex;
       base += tot;
     }
   }
@@ -472,9 +476,10 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       a.seg[(int64_t)sg * kSeg + (p & 63)] = s;
       atomicAdd(&a.seg_live[sg], 1);
     }
-    const int idx = atomicAdd(&a.counters[0], 1);
+    const int idx = atomicAdd(&a.counters[kCtrMiss], 1);
     a.miss_src[idx] = host_page_index(a, b, h, P, p);
     a.miss_dst[idx] = unit * cap + s;
+    a.miss_att[idx] = ul * k + hits + rank;  // misses follow the hits in attention order
   }
   __syncthreads();
 
@@ -490,7 +495,19 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
     a.sel_slot[(int64_t)ul * k + j] = v ? sm.sslot[j] : -1;
     a.sel_hit[(int64_t)ul * k + j] = v ? (uint8_t)(sm.hit[j] > 0) : 0;
   }
+  // attention order: hits (ascending partition) first, then this step's misses
+  {
+    const int ntok = a.ntok_b[b];
+    for (int j = tid; j < keff; j += kSelThreads) {
+      const int p = sm.sel[j];
+      const bool hit = sm.hit[j] > 0;
+      const int pos = hit ? j - sm.mrank[j] : hits + sm.mrank[j];
+      a.att_slot[(int64_t)ul * k + pos] = sm.sslot[j];
+      a.att_valid[(int64_t)ul * k + pos] = (p == P - 1) ? ntok - p * kPart : kPart;
+    }
+  }
   if (tid == 0) {
+    a.n_hit[ul] = hits;
     a.keff[ul] = keff;
     int32_t* info = a.unit_info + (int64_t)ul * 8;
     info[0] = hits;
@@ -546,7 +563,12 @@ cudaError_t launch_score(const LayerArgs& a, cudaStream_t st) {
 size_t select_manage_smem_bytes(const LayerArgs& a) { return sel_smem_layout(a.P_max, a.cap, a.k, a.D, nullptr, nullptr); }
 
 cudaError_t select_manage_configure(size_t smem) {
-  return cudaFuncSetAttribute(select_manage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(select_manage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int kMaxShared = 100;  // cudaSharedmemCarveoutMaxShared: no carveout switch before attention
+  e = cudaFuncSetAttribute(select_manage_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMaxShared);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(score_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMaxShared);
 }
 
 cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st) {

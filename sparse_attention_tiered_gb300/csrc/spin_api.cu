@@ -8,8 +8,8 @@
 //     entries point to 64-entry segments drawn on demand from one shared pool;
 //   * per-page state: slot -> partition, last-use step (bucketed-LRU timestamps);
 //   * fp32 partition summaries in HBM.
-// A decode step of one layer enqueues five kernels on the caller's stream:
-// score -> select+manage -> retrieve -> attention -> combine.
+// A decode step of one layer enqueues four kernels on the caller's stream:
+// score -> select+manage -> retrieve+attention (cooperative) -> combine.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -54,6 +54,11 @@ struct LayerBuf {
   int32_t* unit_info = nullptr;
   int64_t* miss_src = nullptr;
   int64_t* miss_dst = nullptr;
+  int32_t* miss_att = nullptr;
+  int32_t* ready = nullptr;
+  int32_t* att_slot = nullptr;
+  int32_t* att_valid = nullptr;
+  int32_t* n_hit = nullptr;
   int32_t* counters = nullptr;
   float* partials = nullptr;
   uint16_t* q_stage = nullptr;  // for the host-buffer entry point
@@ -63,8 +68,11 @@ struct LayerBuf {
 
 constexpr int kNumStages = 5;  // select, manage, retrieve, attention, combine
 
+// Events of one timed call: 0 start, 1 after score, 2 after select/manage,
+// 3 after retrieve + attention (one kernel), 4 after combine.
+constexpr int kTimedEvents = 5;
 struct TimedCall {
-  cudaEvent_t ev[kNumStages + 1];
+  cudaEvent_t ev[kTimedEvents];
 };
 
 }  // namespace
@@ -174,10 +182,15 @@ int sync_ctx(spin_ctx* c) {
   SPIN_CUDA(c, cudaDeviceSynchronize(), "synchronising the device");
   // fold finished stage timings
   for (auto& t : c->pending) {
-    for (int s = 0; s < kNumStages; ++s) {
+    auto el = [&](int x, int y) {
       float ms = 0.f;
-      if (cudaEventElapsedTime(&ms, t.ev[s], t.ev[s + 1]) == cudaSuccess) c->ms[s] += ms;
-    }
+      return cudaEventElapsedTime(&ms, t.ev[x], t.ev[y]) == cudaSuccess ? (double)ms : 0.0;
+    };
+    c->ms[0] += el(0, 1);
+    c->ms[1] += el(1, 2);
+    c->ms[2] += el(2, 3);  // retrieve and attention share one kernel: both report its time
+    c->ms[3] += el(2, 3);
+    c->ms[4] += el(3, 4);
     for (auto e : t.ev) c->spare_events.push_back(e);
   }
   c->pending.clear();
@@ -277,6 +290,11 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.unit_info = lb.unit_info;
   a.miss_src = lb.miss_src;
   a.miss_dst = lb.miss_dst;
+  a.miss_att = lb.miss_att;
+  a.ready = lb.ready;
+  a.att_slot = lb.att_slot;
+  a.att_valid = lb.att_valid;
+  a.n_hit = lb.n_hit;
   a.counters = lb.counters;
   a.partials = lb.partials;
   a.stats = c->d_stats;
@@ -401,9 +419,16 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     ALLOC(lb.unit_info, Ul * 8, "allocating layer scratch");
     ALLOC(lb.miss_src, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.miss_dst, Ul * c->k, "allocating layer scratch");
-    ALLOC(lb.counters, 4, "allocating layer scratch");
-    ALLOC(lb.partials, Ul * c->n_chunks * c->G * kPartialStride, "allocating layer scratch");
-    SPIN_CUDA(nullptr, cudaMemset(lb.counters, 0, 16), "initialising layer counters");
+    ALLOC(lb.att_slot, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.att_valid, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.n_hit, Ul, "allocating layer scratch");
+    ALLOC(lb.miss_att, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.ready, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.counters, kNumCtr, "allocating layer scratch");
+    ALLOC(lb.partials, Ul * (c->n_chunks + c->k) * c->G * kPartialStride, "allocating layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.n_hit, 0, Ul * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.ready, 0, Ul * c->k * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.counters, 0, kNumCtr * 4), "initialising layer counters");
     SPIN_CUDA(nullptr, cudaMemset(lb.keff, 0, Ul * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.sel, 0xff, Ul * c->k * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.sel_slot, 0xff, Ul * c->k * 4), "initialising layer scratch");
@@ -426,7 +451,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   return SPIN_OK;
 }
 
-// Enqueue one layer's step. q/out are device pointers.
+// Enqueue one layer's step on `st`: score -> select/manage -> retrieve+attention -> combine.
 int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStream_t st) {
   LayerBuf& lb = c->layers[layer];
   LayerArgs a = lb.args;
@@ -443,18 +468,15 @@ int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStre
   auto mark = [&](int i) {
     if (timed) cudaEventRecord(tc.ev[i], st);
   };
-  const int retrieve_grid = 2 * c->sm_count;
   mark(0);
   SPIN_CUDA(c, launch_score(a, st), "launching score");
   mark(1);
   SPIN_CUDA(c, launch_select_manage(a, st), "launching select/manage");
   mark(2);
-  SPIN_CUDA(c, launch_retrieve(a, retrieve_grid, st), "launching retrieve");
+  SPIN_CUDA(c, launch_attend_retrieve(a, &c->tmap, c->sm_count, st), "launching retrieve + attention");
   mark(3);
-  SPIN_CUDA(c, launch_attention(a, &c->tmap, c->sm_count, st), "launching attention");
-  mark(4);
   SPIN_CUDA(c, launch_combine(a, st), "launching combine");
-  mark(5);
+  mark(4);
   if (timed) {
     c->pending.push_back(tc);
     c->timed_calls += 1;
@@ -561,8 +583,8 @@ int spin_index_offload(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k,
 int spin_decode_step(spin_ctx* c, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream) {
   if (!c) return fail(nullptr, SPIN_ERR_INVALID, "ctx is NULL");
   if (!q || !out) return fail(c, SPIN_ERR_INVALID, "q or out is NULL");
-  if ((reinterpret_cast<uintptr_t>(q) & 3) || (reinterpret_cast<uintptr_t>(out) & 15))
-    return fail(c, SPIN_ERR_INVALID, "q must be 4-byte and out 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return fail(c, SPIN_ERR_INVALID, "q and out must be 16-byte aligned");
   int rc = check_layer(c, layer);
   if (rc) return rc;
   DeviceGuard g(c->device);

@@ -49,10 +49,15 @@ struct LayerArgs {
   uint8_t* sel_hit;          // [U_l][k]
   int32_t* keff;             // [U_l]
   int32_t* unit_info;        // [U_l][8]
-  int64_t* miss_src;         // [U_l * k] host page index
-  int64_t* miss_dst;         // [U_l * k] pool slot index
-  int32_t* counters;         // [4]: miss count, attention task counter, step t, spare
-  float* partials;           // [U_l * n_chunks][G][kPartialStride]
+  int64_t* miss_src;         // [U_l * k] host page index of each miss (miss list, append order)
+  int64_t* miss_dst;         // [U_l * k] pool slot index of each miss
+  int32_t* miss_att;         // [U_l * k] ul * k + attention position of each miss
+  int32_t* ready;            // [U_l * k] per miss-list entry: step tag once its page is in HBM
+  int32_t* att_slot;         // [U_l][k] slots in attention order: hits first, then misses
+  int32_t* att_valid;        // [U_l][k] valid tokens of those pages
+  int32_t* n_hit;            // [U_l] hits of the step (pages [0, n_hit) of att_slot)
+  int32_t* counters;         // [4]: see kCtr*
+  float* partials;           // hits [U_l][n_chunks][G][132], then misses [U_l][k][G][132]
   unsigned long long* stats; // [8] device counters
   uint32_t* err;             // device error word
   const uint16_t* q;         // [B][Hq][128] bf16 (device)
@@ -63,6 +68,9 @@ struct LayerArgs {
 __host__ __device__ inline int64_t host_page_index(const LayerArgs& a, int b, int h, int64_t P, int64_t p) {
   return a.layer_page_base + (int64_t)a.Hkv * a.poff_b[b] + (int64_t)h * P + p;
 }
+
+// Per-layer device counters.
+enum : int { kCtrMiss = 0, kCtrTaskHits = 1, kCtrTaskMisses = 2, kCtrStep = 3, kCtrRetrieve = 4, kNumCtr = 8 };
 
 // Device stats slots.
 enum : int { kStatHits = 0, kStatMisses = 1, kStatEvictions = 2, kStatLruRounds = 3, kStatSelected = 4 };
@@ -75,8 +83,8 @@ cudaError_t launch_summarize_offload(const uint16_t* k, const uint16_t* v, int64
                                      uint16_t* host_unit0, int64_t unit_pages, cudaStream_t st);
 cudaError_t launch_score(const LayerArgs& a, cudaStream_t st);
 cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st);
-cudaError_t launch_retrieve(const LayerArgs& a, int grid, cudaStream_t st);
-cudaError_t launch_attention(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st);
+// Retrieve + attention in one cooperative persistent launch (one CTA per SM).
+cudaError_t launch_attend_retrieve(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st);
 cudaError_t launch_combine(const LayerArgs& a, cudaStream_t st);
 cudaError_t launch_resolve_all(const LayerArgs& a, int32_t* resolve, int32_t* live_segs, cudaStream_t st);
 size_t select_manage_smem_bytes(const LayerArgs& a);
