@@ -249,10 +249,13 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       if (lane == 0) m = atomicAdd(&a.counters[kCtrRetrieve], 1);
       m = __shfl_sync(0xffffffffu, m, 0);
       if (m >= n_miss) break;
-      const uint4* src = reinterpret_cast<const uint4*>(a.host_store + a.miss_src[m] * kPageElems);
-      uint4* dst = reinterpret_cast<uint4*>(a.pool + a.miss_dst[m] * kPageElems);
+      const int64_t sp = a.miss_src[m], dp = a.miss_dst[m];
+      const bool in_range = sp >= 0 && sp < a.host_pages && dp >= 0 && dp < a.pool_slots;
+      if (!in_range && lane == 0) atomicOr(a.err, kErrIndex);  // never expected: skip the copy
+      const uint4* src = reinterpret_cast<const uint4*>(a.host_store + sp * kPageElems);
+      uint4* dst = reinterpret_cast<uint4*>(a.pool + dp * kPageElems);
 #pragma unroll 1
-      for (int c = 0; c < kVec; c += 32 * kUnroll) {
+      for (int c = 0; in_range && c < kVec; c += 32 * kUnroll) {
         uint4 r[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) r[u] = __ldcs(src + c + u * 32 + lane);
@@ -279,7 +282,11 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       const int st = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
       if (!mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) return false;
-      const int slot = a.att_slot[att];
+      int slot = a.att_slot[att];
+      if (slot < 0 || slot >= a.cap) {  // never expected: stage slot 0 instead and report
+        atomicOr(a.err, kErrIndex);
+        slot = 0;
+      }
       StageMeta m;
       m.part = part;
       m.ul = ul;
@@ -328,7 +335,11 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       }
       if (!ready) { ok = false; break; }
       asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what the generic stores wrote
-      const int att = a.miss_att[m];
+      int att = a.miss_att[m];
+      if (att < 0 || att >= U * a.k) {  // never expected
+        atomicOr(a.err, kErrIndex);
+        att = 0;
+      }
       const int ul = att / a.k;
       ok = issue(ul, att, U * a.n_chunks + att, true);
     }

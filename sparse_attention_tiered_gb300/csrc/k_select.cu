@@ -52,15 +52,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(LayerArgs a) {
   const int p_base = blockIdx.x * kScoreChunk;
   if (p_base >= P) return;
   __shared__ __align__(16) float qs[kD];
-  if (threadIdx.x < kD) {
-    const uint16_t* q = a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD + threadIdx.x;
-    float s = 0.f;
-    for (int g = 0; g < a.G; ++g) s += bf16_bits_to_float(q[g * kD]);
-    qs[threadIdx.x] = s;
-  }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float4 qv = reinterpret_cast<const float4*>(qs)[lane];
+  // the summary loads do not depend on the query: issue them first
   const float4* su = reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, P, 0) * kD);
   const int p0 = p_base + warp * kScorePerWarp;
   float4 sv[kScorePerWarp];
@@ -69,6 +62,14 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(LayerArgs a) {
     const int p = p0 + i;
     sv[i] = p < P ? __ldg(su + (int64_t)p * (kD / 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  if (threadIdx.x < kD) {
+    const uint16_t* q = a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD + threadIdx.x;
+    float s = 0.f;
+    for (int g = 0; g < a.G; ++g) s += bf16_bits_to_float(q[g * kD]);
+    qs[threadIdx.x] = s;
+  }
+  __syncthreads();
+  const float4 qv = reinterpret_cast<const float4*>(qs)[lane];
   float d[kScorePerWarp];
 #pragma unroll
   for (int i = 0; i < kScorePerWarp; ++i) {
@@ -169,8 +170,21 @@ __device__ __forceinline__ void release_segment(const LayerArgs& a, int sg) {
   atomicAnd(&a.seg_bitmap[sg >> 5], ~(1u << (sg & 31)));
 }
 
-// Block-wide exclusive scan of one int per thread; returns the exclusive prefix, *total = sum.
-__device__ int block_exclusive_scan(int v, int* total, int* wsum) {
+// Barrier over the first NT threads of the CTA (one warp: __syncwarp; otherwise a
+// named barrier, so the warps that left after scoring are not waited for).
+template <int NT>
+__device__ __forceinline__ void group_sync() {
+  if constexpr (NT == 32) {
+    __syncwarp();
+  } else {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+  }
+}
+
+// Exclusive scan of one int per thread over the first NT threads; *total = sum.
+template <int NT>
+__device__ int group_exclusive_scan(int v, int* total, int* wsum) {
+  constexpr int kW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -178,25 +192,40 @@ __device__ int block_exclusive_scan(int v, int* total, int* wsum) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kSelWarps ? wsum[lane] : 0;
+  if constexpr (kW == 1) {
+    *total = __shfl_sync(0xffffffffu, x, 31);
+    return x - v;
+  } else {
+    if (lane == 31) wsum[warp] = x;
+    group_sync<NT>();
+    if (warp == 0) {
+      int w = lane < kW ? wsum[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < kW) wsum[lane] = w;  // inclusive
     }
-    if (lane < kSelWarps) wsum[lane] = w;  // inclusive
+    group_sync<NT>();
+    const int before = (warp > 0 ? wsum[warp - 1] : 0) + x - v;
+    *total = wsum[kW - 1];
+    group_sync<NT>();
+    return before;
   }
-  __syncthreads();
-  const int before = (warp > 0 ? wsum[warp - 1] : 0) + x - v;
-  *total = wsum[kSelWarps - 1];
-  __syncthreads();
-  return before;
 }
 
+// One CTA (512 threads) per unit.
+// kFusedScore: the CTA computes its unit's scores itself (same arithmetic as
+// score_kernel: per partition, lane l holds dims 4l..4l+3, one mul and three fma,
+// then a butterfly sum) instead of reading them from the score kernel's output.
+// Used when there are enough units per layer to keep HBM busy with one CTA each.
+// NT: threads that run top-k and the page manager after the keys are in shared
+// memory (32 = one warp with warp-level primitives only, for small units; 512 =
+// the whole CTA, for large ones).
+template <int NT, bool kFusedScore>
 __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a) {
+  constexpr int kW = NT / 32;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ int s_bin, s_above, s_cnt_hits, s_cnt_res, s_cutoff, s_evicted;
   __shared__ int s_wgt[kSelWarps], s_weq[kSelWarps], s_wpos[kSelWarps], s_wtake[kSelWarps];
@@ -213,28 +242,83 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   const int64_t unit = a.unit_base + ul;
   const int t = a.counters[kCtrStep];
   // After a pool or invariant error the page state is no longer trusted: leave it as is.
-  if (*((volatile uint32_t*)a.err) & (kErrCapacity | kErrInternal)) return;
+  if (*((volatile uint32_t*)a.err) & (kErrCapacity | kErrInternal | kErrSelCount | kErrSegId | kErrIndex)) return;
+
+  // ---------------- scores -> order-preserving keys ----------------
+  if constexpr (kFusedScore) {
+    __shared__ __align__(16) float s_qs[kD];
+    constexpr int kPer = 8;  // partitions in flight per warp
+    const float4* su = reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, P, 0) * kD);
+    float4 sv[kPer];
+    int p0 = warp * kPer;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      sv[i] = (p0 + i < P) ? __ldg(su + (int64_t)(p0 + i) * (kD / 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid < kD) {
+      const uint16_t* q = a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD + tid;
+      float s = 0.f;
+      for (int g = 0; g < a.G; ++g) s += bf16_bits_to_float(q[g * kD]);
+      s_qs[tid] = s;
+    }
+    __syncthreads();
+    const float4 qv = reinterpret_cast<const float4*>(s_qs)[lane];
+    for (; p0 < P; p0 += kSelWarps * kPer) {
+      float d[kPer];
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        float x = sv[i].x * qv.x;
+        x = fmaf(sv[i].y, qv.y, x);
+        x = fmaf(sv[i].z, qv.z, x);
+        x = fmaf(sv[i].w, qv.w, x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        d[i] = x;
+      }
+      const int pn = p0 + kSelWarps * kPer;  // prefetch the warp's next partitions
+#pragma unroll
+      for (int i = 0; i < kPer; ++i)
+        sv[i] = (pn + i < P) ? __ldg(su + (int64_t)(pn + i) * (kD / 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane < kPer) {
+        float x = d[0];
+#pragma unroll
+        for (int i = 1; i < kPer; ++i) x = (lane == i) ? d[i] : x;
+        const int p = p0 + lane;
+        if (p < P) {
+          x = (x == 0.f) ? 0.f : x;  // -0 -> +0
+          a.scores[(int64_t)ul * a.P_max + p] = x;
+          sm.keys[p] = float_key(x);
+        }
+      }
+    }
+    __syncthreads();
+  } else {
+    for (int p = tid; p < P; p += kSelThreads) sm.keys[p] = float_key(a.scores[(int64_t)ul * a.P_max + p]);
+  }
+
+  __syncthreads();  // keys complete for every thread
+  if (tid >= NT) return;
 
   // ---------------- top-k: radix select on order-preserving keys ----------------
-  for (int p = tid; p < P; p += kSelThreads) sm.keys[p] = float_key(a.scores[(int64_t)ul * a.P_max + p]);
   uint32_t prefix = 0, mask = 0;
   int krem = keff;
   if (keff > 0) {
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      for (int i = tid; i < kSelWarps * 256; i += kSelThreads) sm.whist[i] = 0;
-      __syncthreads();
-      for (int p = tid; p < P; p += kSelThreads) {
+      for (int i = tid; i < kW * 256; i += NT) sm.whist[i] = 0;
+      group_sync<NT>();
+      for (int p = tid; p < P; p += NT) {
         const uint32_t key = sm.keys[p];
         if ((key & mask) == prefix) atomicAdd(&sm.whist[warp * 256 + ((key >> shift) & 255u)], 1u);
       }
-      __syncthreads();
-      if (tid < 256) {
-        uint32_t s = 0;
-        for (int w = 0; w < kSelWarps; ++w) s += sm.whist[w * 256 + tid];
-        sm.whist[tid] = s;  // row 0 now holds the merged histogram (each thread owns its column)
+      group_sync<NT>();
+      if constexpr (kW > 1) {
+        for (int i = tid; i < 256; i += NT) {
+          uint32_t s = 0;
+          for (int w = 0; w < kW; ++w) s += sm.whist[w * 256 + i];
+          sm.whist[i] = s;  // row 0 now holds the merged histogram (each thread owns its column)
+        }
       }
-      __syncthreads();
+      group_sync<NT>();
       if (warp == 0) {
         // lane l owns bins 255-8l down to 248-8l (the top bins first)
         int c[8], lsum = 0;
@@ -263,18 +347,18 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
           }
         }
       }
-      __syncthreads();
+      group_sync<NT>();
       prefix |= (uint32_t)s_bin << shift;
       mask |= 0xFFu << shift;
       krem -= s_above;
-      __syncthreads();
+      group_sync<NT>();
     }
   }
   const uint32_t T = prefix;  // the k-th largest key; krem = equal keys still to take
 
   // ---------------- compaction in ascending partition order ----------------
   {
-    const int chunk = ((P + kSelThreads - 1) / kSelThreads) * 32;
+    const int chunk = ((P + NT - 1) / NT) * 32;
     const int wb = warp * chunk, we = min(P, wb + chunk);
     int gt = 0, eq = 0;
     if (keff > 0)
@@ -288,18 +372,23 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       s_wgt[warp] = gt;
       s_weq[warp] = eq;
     }
-    __syncthreads();
+    group_sync<NT>();
     if (tid == 0) {
       int eq_before = 0, pos = 0;
-      for (int w = 0; w < kSelWarps; ++w) {
+      for (int w = 0; w < kW; ++w) {
         const int take = max(0, min(krem - eq_before, s_weq[w]));
         s_wpos[w] = pos;
         s_wtake[w] = take;
         pos += s_wgt[w] + take;
         eq_before += s_weq[w];
       }
+      s_bin = pos;  // total selected (reuses the radix scratch)
     }
-    __syncthreads();
+    group_sync<NT>();
+    if (s_bin != keff) {  // never expected: leave the unit untouched and report
+      if (tid == 0) atomicOr(a.err, kErrSelCount);
+      return;
+    }
     int pos = s_wpos[warp], eq_left = s_wtake[warp];
     if (keff > 0)
       for (int base = wb; base < we; base += 32) {
@@ -310,7 +399,7 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
         const uint32_t meq = __ballot_sync(0xffffffffu, iseq);
         const bool take = isgt || (iseq && __popc(meq & lanemask_lt()) < eq_left);
         const uint32_t msel = __ballot_sync(0xffffffffu, take);
-        if (take) sm.sel[pos + __popc(msel & lanemask_lt())] = p;
+        if (take && pos + __popc(msel & lanemask_lt()) < keff) sm.sel[pos + __popc(msel & lanemask_lt())] = p;
         pos += __popc(msel);
         eq_left -= min(eq_left, __popc(meq));
       }
@@ -319,40 +408,48 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   // ---------------- load the unit's page state ----------------
   int32_t* g_sp = a.slot_part + unit * cap;
   int32_t* g_lu = a.last_use + unit * cap;
-  for (int s = tid; s < cap; s += kSelThreads) {
+  for (int s = tid; s < cap; s += NT) {
     sm.sp[s] = g_sp[s];
     sm.lu[s] = g_lu[s];
     sm.mand[s] = 0;
   }
-  for (int d = tid; d < a.D; d += kSelThreads) sm.dirs[d] = a.dir[unit * a.D + d];
+  for (int d = tid; d < a.D; d += NT) sm.dirs[d] = a.dir[unit * a.D + d];
   if (tid == 0) {
     s_cnt_hits = 0;
     s_cnt_res = 0;
     s_cutoff = -1;
     s_evicted = 0;
   }
-  __syncthreads();
+  group_sync<NT>();
 
   // ---------------- 1. residency check through the two-level table; 2. bump ----------------
-  for (int j = tid; j < keff; j += kSelThreads) {
+  for (int j = tid; j < keff; j += NT) {
     const int p = sm.sel[j];
-    const int sg = sm.dirs[p >> 6];
+    int sg = sm.dirs[p >> 6];
+    if (sg >= a.S) {
+      atomicOr(a.err, kErrSegId);
+      sg = -1;
+    }
     const int slot = sg < 0 ? -1 : a.seg[(int64_t)sg * kSeg + (p & 63)];
+    if (slot >= cap) atomicOr(a.err, kErrIndex);
     sm.sslot[j] = slot;
     sm.hit[j] = slot >= 0;
-    if (slot >= 0) {
+    if (slot >= 0 && slot < cap) {
       sm.lu[slot] = t;
       sm.mand[slot] = 1;
       atomicAdd(&s_cnt_hits, 1);
+    } else if (slot >= cap) {
+      sm.sslot[j] = -1;
+      sm.hit[j] = 0;
     }
   }
   {
     int res = 0;
-    for (int s = tid; s < cap; s += kSelThreads) res += sm.sp[s] >= 0;
+    for (int s = tid; s < cap; s += NT) res += sm.sp[s] >= 0;
     res = __reduce_add_sync(0xffffffffu, res);
     if (lane == 0 && res) atomicAdd(&s_cnt_res, res);
   }
-  __syncthreads();
+  group_sync<NT>();
   const int hits = s_cnt_hits;
   const int misses = keff - hits;
   const int resident = s_cnt_res;
@@ -361,15 +458,15 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   // ---------------- 3. bucketed LRU ----------------
   if (demand > 0) {
     uint32_t* hist = sm.whist;  // 64 bins
-    if (tid < kBuckets) hist[tid] = 0;
-    __syncthreads();
-    for (int s = tid; s < cap; s += kSelThreads) {
+    for (int i = tid; i < kBuckets; i += NT) hist[i] = 0;
+    group_sync<NT>();
+    for (int s = tid; s < cap; s += NT) {
       if (sm.sp[s] < 0 || sm.mand[s]) continue;
       const int age = t - sm.lu[s];
       const int bucket = kBuckets - 1 - min(kBuckets - 1, age);
       atomicAdd(&hist[bucket], 1u);
     }
-    __syncthreads();
+    group_sync<NT>();
     if (warp == 0) {
       // lane l owns buckets 2l, 2l+1 (oldest first)
       const int c0 = (int)hist[2 * lane], c1 = (int)hist[2 * lane + 1];
@@ -384,9 +481,9 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       const uint32_t m = __ballot_sync(0xffffffffu, excl < demand && incl >= demand);
       if (lane == __ffs(m) - 1) s_cutoff = (excl + c0 >= demand) ? 2 * lane : 2 * lane + 1;
     }
-    __syncthreads();
+    group_sync<NT>();
     const int cutoff = s_cutoff;
-    for (int s = tid; s < cap; s += kSelThreads) {
+    for (int s = tid; s < cap; s += NT) {
       const int p = sm.sp[s];
       if (p < 0 || sm.mand[s]) continue;
       const int age = t - sm.lu[s];
@@ -394,7 +491,9 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       if (bucket > cutoff) continue;
       // clear the table entry; the last page of a segment returns it to the pool
       const int sg = sm.dirs[p >> 6];
-      if (sg >= 0) {
+      if (sg >= a.S) {
+        atomicOr(a.err, kErrSegId);
+      } else if (sg >= 0) {
         a.seg[(int64_t)sg * kSeg + (p & 63)] = -1;
         __threadfence();
         if (atomicSub(&a.seg_live[sg], 1) == 1) {
@@ -407,7 +506,7 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       sm.sp[s] = -1;
       atomicAdd(&s_evicted, 1);
     }
-    __syncthreads();
+    group_sync<NT>();
   }
 
   // ---------------- 4. assign free slots to misses, allocate segments ----------------
@@ -415,11 +514,11 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   __shared__ int s_nfree;
   {
     int base = 0;
-    for (int r = 0; r < cap; r += kSelThreads) {
+    for (int r = 0; r < cap; r += NT) {
       const int s = r + tid;
       const int f = (s < cap && sm.sp[s] < 0) ? 1 : 0;
       int tot;
-      const int ex = block_exclusive_scan(f, &tot, s_scan);
+      const int ex = group_exclusive_scan<NT>(f, &tot, s_scan);
       if (f) sm.flist[base + ex] = s;
       base += tot;
     }
@@ -428,18 +527,18 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   // rank of each miss among the misses (ascending partition = ascending j)
   {
     int base = 0;
-    for (int r = 0; r < keff; r += kSelThreads) {
+    for (int r = 0; r < keff; r += NT) {
       const int j = r + tid;
       const int m = (j < keff && !sm.hit[j]) ? 1 : 0;
       int tot;
-      const int ex = block_exclusive_scan(m, &tot, s_scan);
+      const int ex = group_exclusive_scan<NT>(m, &tot, s_scan);
       if (m) sm.hit[j] = -1 - (base + ex);  // encode: hit = 1, miss = -1 - rank
       if (j < keff) sm.mrank[j] = base + ex;
       base += tot;
     }
   }
   // one segment per 64-range that receives its first page
-  for (int j = tid; j < keff; j += kSelThreads) {
+  for (int j = tid; j < keff; j += NT) {
     if (sm.hit[j] > 0) continue;
     const int r = sm.sel[j] >> 6;
     if (sm.dirs[r] >= 0) continue;
@@ -456,8 +555,8 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       }
     }
   }
-  __syncthreads();
-  for (int j = tid; j < keff; j += kSelThreads) {
+  group_sync<NT>();
+  for (int j = tid; j < keff; j += NT) {
     const int code = sm.hit[j];
     if (code > 0) continue;
     const int rank = -1 - code;
@@ -472,24 +571,30 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
     sm.sslot[j] = s;
     sm.hit[j] = 0;
     const int sg = sm.dirs[p >> 6];
-    if (sg >= 0) {
+    if (sg >= a.S) {
+      atomicOr(a.err, kErrSegId);
+    } else if (sg >= 0) {
       a.seg[(int64_t)sg * kSeg + (p & 63)] = s;
       atomicAdd(&a.seg_live[sg], 1);
     }
     const int idx = atomicAdd(&a.counters[kCtrMiss], 1);
+    if (idx >= a.B * a.Hkv * k) {
+      atomicOr(a.err, kErrIndex);
+      continue;
+    }
     a.miss_src[idx] = host_page_index(a, b, h, P, p);
     a.miss_dst[idx] = unit * cap + s;
     a.miss_att[idx] = ul * k + hits + rank;  // misses follow the hits in attention order
   }
-  __syncthreads();
+  group_sync<NT>();
 
   // ---------------- write back ----------------
-  for (int s = tid; s < cap; s += kSelThreads) {
+  for (int s = tid; s < cap; s += NT) {
     g_sp[s] = sm.sp[s];
     g_lu[s] = sm.lu[s];
   }
-  for (int d = tid; d < a.D; d += kSelThreads) a.dir[unit * a.D + d] = sm.dirs[d] < 0 ? -1 : sm.dirs[d];
-  for (int j = tid; j < k; j += kSelThreads) {
+  for (int d = tid; d < a.D; d += NT) a.dir[unit * a.D + d] = sm.dirs[d] < 0 ? -1 : sm.dirs[d];
+  for (int j = tid; j < k; j += NT) {
     const bool v = j < keff;
     a.sel[(int64_t)ul * k + j] = v ? sm.sel[j] : -1;
     a.sel_slot[(int64_t)ul * k + j] = v ? sm.sslot[j] : -1;
@@ -498,7 +603,7 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   // attention order: hits (ascending partition) first, then this step's misses
   {
     const int ntok = a.ntok_b[b];
-    for (int j = tid; j < keff; j += kSelThreads) {
+    for (int j = tid; j < keff; j += NT) {
       const int p = sm.sel[j];
       const bool hit = sm.hit[j] > 0;
       const int pos = hit ? j - sm.mrank[j] : hits + sm.mrank[j];
@@ -553,8 +658,10 @@ __global__ void resolve_all_kernel(LayerArgs a, int32_t* resolve, int32_t* live)
 
 }  // namespace
 
+bool select_fuses_score(const LayerArgs& a);
+
 cudaError_t launch_score(const LayerArgs& a, cudaStream_t st) {
-  if (a.P_max <= 0) return cudaSuccess;
+  if (a.P_max <= 0 || select_fuses_score(a)) return cudaSuccess;  // scored inside the select kernel
   dim3 grid((unsigned)((a.P_max + kScoreChunk - 1) / kScoreChunk), (unsigned)(a.B * a.Hkv));
   score_kernel<<<grid, kScoreThreads, 0, st>>>(a);
   return cudaGetLastError();
@@ -562,18 +669,35 @@ cudaError_t launch_score(const LayerArgs& a, cudaStream_t st) {
 
 size_t select_manage_smem_bytes(const LayerArgs& a) { return sel_smem_layout(a.P_max, a.cap, a.k, a.D, nullptr, nullptr); }
 
-cudaError_t select_manage_configure(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(select_manage_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+template <int NT, bool F>
+cudaError_t configure_one(size_t smem) {
   const int kMaxShared = 100;  // cudaSharedmemCarveoutMaxShared: no carveout switch before attention
-  e = cudaFuncSetAttribute(select_manage_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMaxShared);
+  cudaError_t e = cudaFuncSetAttribute(select_manage_kernel<NT, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(score_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMaxShared);
+  return cudaFuncSetAttribute(select_manage_kernel<NT, F>, cudaFuncAttributePreferredSharedMemoryCarveout, kMaxShared);
 }
+
+cudaError_t select_manage_configure(size_t smem) {
+  cudaError_t e;
+  if ((e = configure_one<32, false>(smem)) != cudaSuccess) return e;
+  if ((e = configure_one<32, true>(smem)) != cudaSuccess) return e;
+  if ((e = configure_one<kSelThreads, false>(smem)) != cudaSuccess) return e;
+  if ((e = configure_one<kSelThreads, true>(smem)) != cudaSuccess) return e;
+  return cudaFuncSetAttribute(score_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+}
+
+bool select_fuses_score(const LayerArgs& a) { return a.B * a.Hkv >= 64 && a.P_max <= 4096; }
+static bool select_single_warp(const LayerArgs& a) { return a.P_max <= 1024 && a.cap <= 1024 && a.k <= 256; }
 
 cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st) {
   const size_t smem = select_manage_smem_bytes(a);
-  select_manage_kernel<<<a.B * a.Hkv, kSelThreads, smem, st>>>(a);
+  const unsigned grid = (unsigned)(a.B * a.Hkv);
+  const bool f = select_fuses_score(a), w = select_single_warp(a);
+  if (w && f) select_manage_kernel<32, true><<<grid, kSelThreads, smem, st>>>(a);
+  else if (w) select_manage_kernel<32, false><<<grid, kSelThreads, smem, st>>>(a);
+  else if (f) select_manage_kernel<kSelThreads, true><<<grid, kSelThreads, smem, st>>>(a);
+  else select_manage_kernel<kSelThreads, false><<<grid, kSelThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -174,7 +174,7 @@ int check_device_error(spin_ctx* c) {
     return fail(c, SPIN_ERR_CAPACITY, "the shared second-level segment pool ran out (device error 0x%x)", c->sticky);
   if (c->sticky & kErrTimeout)
     return fail(c, SPIN_ERR_TIMEOUT, "a bounded device wait ran out (device error 0x%x)", c->sticky);
-  if (c->sticky) return fail(c, SPIN_ERR_CUDA, "device invariant error 0x%x", c->sticky);
+  if (c->sticky) return fail(c, SPIN_ERR_CUDA, "device invariant check failed (error word 0x%x)", c->sticky);
   return SPIN_OK;
 }
 
@@ -273,6 +273,8 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.poff_b = c->d_poff_b;
   a.layer_page_base = (int64_t)l * c->pages_per_layer;
   a.unit_base = (int64_t)l * c->B * c->Hkv;
+  a.host_pages = c->pages_per_layer * c->L;
+  a.pool_slots = c->units * c->cap;
   a.summ = c->d_summ;
   a.host_store = c->d_store;
   a.pool = c->d_pool;

@@ -24,6 +24,9 @@ enum : uint32_t {
   kErrCapacity = 1u,   // shared segment pool exhausted
   kErrTimeout = 2u,    // a bounded wait ran out
   kErrInternal = 4u,   // an invariant of the page state was found broken
+  kErrSelCount = 8u,   // the top-k produced a selection of the wrong size
+  kErrSegId = 16u,     // a directory entry held no valid segment id
+  kErrIndex = 32u,     // a miss-list, slot or partial index was out of range (access skipped)
 };
 
 // Per-layer arguments of the decode-step kernels (passed by value).
@@ -34,6 +37,8 @@ struct LayerArgs {
   const int64_t* poff_b;     // [B] sum of P over earlier requests
   int64_t layer_page_base;   // first page of this layer in the host store / summaries
   int64_t unit_base;         // first global unit of this layer = layer * B * Hkv
+  int64_t host_pages;        // pages in the host store (all layers)
+  int64_t pool_slots;        // pages in the HBM pool (all units)
   const float* summ;         // [pages][128] fp32 summaries (all layers)
   const uint16_t* host_store;// mapped pinned pages [pages][16384] (device-usable address)
   uint16_t* pool;            // HBM pages [units * cap][16384]
