@@ -52,6 +52,49 @@ def parse():
     return ap.parse_args()
 
 
+class Ranks:
+    """One process per GPU (torchrun env). Shards are independent batches: rank r runs
+    the workload drawn with seed r, so per-GPU work is fixed as ranks are added
+    (weak scaling). The only collectives are a barrier and max-over-ranks timing."""
+
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dev = None
+
+    def init(self, backend: str, device=None):
+        self.dev = device
+        if self.world > 1:
+            import torch.distributed as dist
+            kw = {"device_id": device} if (backend == "nccl" and device is not None) else {}
+            dist.init_process_group(backend, **kw)
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return float(x)
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.dev if self.dev is not None else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the tokens of all ranks over the slowest rank's time."""
+    return tokens_per_rank * world / (max_ms * 1e-3)
+
+
 def make_workload(args, rank=0):
     w = W.by_name(args.workload, seed=rank)
     if args.layers:
@@ -225,21 +268,17 @@ def bench_reference(args):
 
 def bench_spin(args):
     import torch
-    import torch.distributed as dist
     from sparse_attention_tiered_gb300 import SpinContext
     from sparse_attention_tiered_gb300._binding import SPIN_FLAG_STAGE_TIMING
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    R = Ranks()
+    world, rank, local = R.world, R.rank, R.local
     torch.cuda.set_device(local)
     dev = torch.device(f"cuda:{local}")
+    R.init("nccl", dev)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        R.barrier()
         torch.cuda.synchronize()
 
     w = make_workload(args, rank)
@@ -296,14 +335,10 @@ def bench_spin(args):
     e1.record()
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
+    ms_rank = e0.elapsed_time(e1)
     st1 = ctx.stats()
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    tokens = w.B * K * world
-    value = tokens / (ms * 1e-3)
+    ms = R.max(ms_rank)
+    value = job_tokens_per_s(w.B * K, world, ms)
 
     d = {k2: st1[k2] - st0[k2] for k2 in ("hits", "misses", "evictions", "retrieved_bytes", "selected_bytes",
                                           "timed_calls", "ms_select", "ms_manage", "ms_retrieve", "ms_attention",
@@ -318,7 +353,7 @@ def bench_spin(args):
     traffic = attention_traffic(sel_bytes_per_launch)
     combined_ideal_s = d["selected_bytes"] / (hbm_gbs * 1e9) + d["retrieved_bytes"] / (host_gbs * 1e9)
     summ_ideal_s = K * w.summary_bytes_per_step() / (hbm_gbs * 1e9)
-    gpu_launches = K * w.L * 4
+    gpu_launches = K * w.L * (2 if (w.B * w.Hkv >= 64 and w.p_max <= 4096) else 3)
 
     # ---- end to end through the host-buffer entry point ----
     e2e = None
@@ -332,12 +367,8 @@ def bench_spin(args):
                 ctx.decode_step_host(l, q_host[t, l].data_ptr(), o_host[l].data_ptr(), stream)
         a1.record()
         barrier()
-        ms_e2e = a0.elapsed_time(a1)
-        if world > 1:
-            tt = torch.tensor([ms_e2e], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms_e2e = float(tt.item())
-        e2e = {"value": w.B * K * world / (ms_e2e * 1e-3), "unit": "tokens/s",
+        ms_e2e = R.max(a0.elapsed_time(a1))
+        e2e = {"value": job_tokens_per_s(w.B * K, world, ms_e2e), "unit": "tokens/s",
                "h2d_bytes_per_step": int(q_host[0].numel() * 2), "d2h_bytes_per_step": int(o_host.numel() * 4)}
     st2 = ctx.stats()
     ctx.close()
@@ -369,8 +400,8 @@ def bench_spin(args):
                          "hbm": {"achieved": hbm_achieved, "peak": hbm_gbs, "frac": hbm_achieved / hbm_gbs},
                          "host_link": {"achieved": host_achieved, "peak": host_gbs, "frac": host_achieved / host_gbs},
                          "avg_launch_ms": att_ms},
-            "combined_roofline": {"frac": combined_ideal_s / (ms * 1e-3) * world if ms else None,
-                                  "frac_with_summaries": (combined_ideal_s + summ_ideal_s) / (ms * 1e-3) * world,
+            "combined_roofline": {"frac": combined_ideal_s / (ms * 1e-3) if ms else None,
+                                  "frac_with_summaries": (combined_ideal_s + summ_ideal_s) / (ms * 1e-3),
                                   "hbm_gbs": hbm_gbs, "host_link_gbs": host_gbs,
                                   "selected_bytes": d["selected_bytes"], "retrieved_bytes": d["retrieved_bytes"],
                                   "definition": "(selected KV bytes / HBM GB/s + retrieved bytes / pinned H2D GB/s) "
@@ -385,8 +416,7 @@ def bench_spin(args):
             "setup_s": setup_s,
         }
         print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    R.close()
     return 0
 
 

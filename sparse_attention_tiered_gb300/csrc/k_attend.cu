@@ -31,12 +31,14 @@
 //   O^T[128][8 heads] += V^T P             P transposed in registers (movmatrix) and
 //                                          split into bf16 hi + lo parts, two mma each
 // At the end of a task the four warps merge (m, l, O) in shared memory and write
-// one partial (m, l, acc[128]) per query head; the combine kernel merges the
-// partials of a unit into the output.
+// one partial (m, l, acc[128]) per query head. When every CTA has finished its
+// pages (an arrival counter; all CTAs are co-resident under the cooperative
+// launch), the consumer warps combine the partials of each unit into the output:
+//   out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
 //
-// Every wait (mbarrier or ready flag) is bounded in time; a wait that runs out
-// sets the device error word, stops issuing work and drains the copies already
-// issued.
+// Every wait (mbarrier, ready flag, arrival counter) is bounded in time; a wait
+// that runs out sets the device error word, stops issuing work and drains the
+// copies already issued.
 #include "spin_internal.cuh"
 
 namespace spin {
@@ -214,6 +216,63 @@ __device__ __forceinline__ uint32_t swz(int r, int cd) {
 }
 
 // ---------------------------------------------------------------------------
+// Combine of one unit: out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c
+// over the unit's partials (its hit tasks and its retrieved pages). Consumer
+// warp w takes heads w, w+4, ...; four columns per lane. One pass: the lanes
+// fetch the (m, l) of up to 32 partials at a time in parallel, the max and the
+// sum are warp reductions, and the accumulator loads are independent.
+// ---------------------------------------------------------------------------
+__device__ void combine_unit(const LayerArgs& a, int ul, int w, int lane) {
+  const int b = ul / a.Hkv, h = ul - b * a.Hkv;
+  const int keff = a.keff[ul], nh = a.n_hit[ul];
+  const int nc = (nh + a.ppt - 1) / a.ppt;
+  const int U = a.B * a.Hkv;
+  const int n = nc + (keff - nh);
+  for (int g = w; g < a.G; g += kCWarps) {
+    float4* out = reinterpret_cast<float4*>(a.out + ((int64_t)b * a.Hq + (int64_t)h * a.G + g) * kD);
+    // partial slots: hit tasks ul * n_chunks + c (c < nc), retrieved pages U * n_chunks + ul * k + j (nh <= j < keff)
+    auto part_ptr = [&](int i) -> const float* {
+      const int64_t slot =
+          i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.k + nh + (i - nc);
+      return a.partials + (slot * a.G + g) * kPartialStride;
+    };
+    float M = -INFINITY;
+    for (int i0 = 0; i0 < n; i0 += 32)
+      if (i0 + lane < n) M = fmaxf(M, __ldcg(part_ptr(i0 + lane)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (M != -INFINITY) {
+      for (int i0 = 0; i0 < n; i0 += 32) {
+        float sc_l = 0.f, l_l = 0.f;
+        if (i0 + lane < n) {
+          const float* pp = part_ptr(i0 + lane);
+          sc_l = exp2f(__ldcg(pp) - M);
+          l_l = __ldcg(pp + 1);
+        }
+        float ls = sc_l * l_l;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+        L += ls;
+        const int cnt = min(32, n - i0);
+#pragma unroll 4
+        for (int i = 0; i < cnt; ++i) {
+          const float sc = __shfl_sync(0xffffffffu, sc_l, i);
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(part_ptr(i0 + i) + 4) + lane);
+          acc.x = fmaf(sc, v.x, acc.x);
+          acc.y = fmaf(sc, v.y, acc.y);
+          acc.z = fmaf(sc, v.z, acc.z);
+          acc.w = fmaf(sc, v.w, acc.w);
+        }
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    out[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Retrieve + attention kernel. NT = number of 8-head tiles (G <= 8 * NT).
 // ---------------------------------------------------------------------------
 template <int NT>
@@ -242,6 +301,7 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
 
   if (warp > kCWarps) {
     // ------------------------------ retrievers ------------------------------
+    if (warp - kCWarps - 1 >= a.retr_warps) return;  // fewer host loads in flight per SM
     constexpr int kVec = kPageBytes / 16;  // 2048 x 16 B
     constexpr int kUnroll = 16;            // 16 x 16 B in flight per lane
     for (;;) {
@@ -533,55 +593,31 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
     if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
     ++i;
   }
-}
 
-// ---------------------------------------------------------------------------
-// Combine: out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c over the
-// unit's partials (its hit tasks and its retrieved pages). One warp per query
-// head, four columns per lane. Also closes the step: resets the miss, task and
-// retrieve counters and advances t.
-// ---------------------------------------------------------------------------
-__global__ void combine_kernel(LayerArgs a) {
-  const int ul = blockIdx.x;
-  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (g < a.G) {
-    const int b = ul / a.Hkv, h = ul - b * a.Hkv;
-    const int keff = a.keff[ul], nh = a.n_hit[ul];
-    const int nc = (nh + a.ppt - 1) / a.ppt;
-    const int U = a.B * a.Hkv;
-    float4* out = reinterpret_cast<float4*>(a.out + ((int64_t)b * a.Hq + (int64_t)h * a.G + g) * kD);
-    // partial slots: hit tasks ul * n_chunks + c (c < nc), retrieved pages U * n_chunks + ul * k + j (nh <= j < keff)
-    auto part_ptr = [&](int i) -> const float* {
-      const int64_t slot = i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.k + nh + (i - nc);
-      return a.partials + (slot * a.G + g) * kPartialStride;
-    };
-    const int n = nc + (keff - nh);
-    float M = -INFINITY;
-    for (int i = 0; i < n; ++i) M = fmaxf(M, part_ptr(i)[0]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-    if (M != -INFINITY) {
-      for (int i = 0; i < n; ++i) {
-        const float* part = part_ptr(i);
-        const float sc = exp2f(part[0] - M);
-        L = fmaf(sc, part[1], L);
-        const float4 v = reinterpret_cast<const float4*>(part + 4)[lane];
-        acc.x = fmaf(sc, v.x, acc.x);
-        acc.y = fmaf(sc, v.y, acc.y);
-        acc.z = fmaf(sc, v.z, acc.z);
-        acc.w = fmaf(sc, v.w, acc.w);
-      }
+  // ---------------- all pages of all CTAs done: combine the partials ----------------
+  asm volatile("bar.sync 2, %0;" ::"n"(kCWarps * 32) : "memory");
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(&a.counters[kCtrArrive], 1);
+    const int target = (int)gridDim.x * tag;  // the counter grows by gridDim.x every step
+    bool done = ld_acquire(&a.counters[kCtrArrive]) >= target;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 30) && !done; ++it) {
+      done = ld_acquire(&a.counters[kCtrArrive]) >= target;
+      if (!done && (it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    out[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (!done) atomicOr(a.err, kErrTimeout);
+    if (blockIdx.x == 0) {  // the step's counters are no longer read by anyone
+      a.counters[kCtrMiss] = 0;
+      a.counters[kCtrTaskHits] = 0;
+      a.counters[kCtrTaskMisses] = 0;
+      a.counters[kCtrRetrieve] = 0;
+      a.counters[kCtrStep] += 1;
+    }
   }
-  if (ul == 0 && threadIdx.x == 0) {
-    a.counters[kCtrMiss] = 0;
-    a.counters[kCtrTaskHits] = 0;
-    a.counters[kCtrTaskMisses] = 0;
-    a.counters[kCtrRetrieve] = 0;
-    a.counters[kCtrStep] += 1;
-  }
+  asm volatile("bar.sync 2, %0;" ::"n"(kCWarps * 32) : "memory");
+  const int U = a.B * a.Hkv;
+  for (int ul = blockIdx.x; ul < U; ul += gridDim.x) combine_unit(a, ul, w, lane);
 }
 
 }  // namespace
@@ -597,9 +633,8 @@ cudaError_t attention_configure() {
   if ((e = cudaFuncSetAttribute(attend_retrieve_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)attention_smem_bytes())) != cudaSuccess)
     return e;
-  // The small kernels keep the SM in its largest shared-memory configuration, so the
-  // persistent CTAs never wait for a carveout switch.
-  return cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, kMaxShared);
+  (void)kMaxShared;
+  return cudaSuccess;
 }
 
 cudaError_t launch_attend_retrieve(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st) {
@@ -613,9 +648,5 @@ cudaError_t launch_attend_retrieve(const LayerArgs& a, const CUtensorMap* tmap, 
                                      params, attention_smem_bytes(), st);
 }
 
-cudaError_t launch_combine(const LayerArgs& a, cudaStream_t st) {
-  combine_kernel<<<a.B * a.Hkv, a.G * 32, 0, st>>>(a);
-  return cudaGetLastError();
-}
 
 }  // namespace spin

@@ -8,14 +8,16 @@
 //     entries point to 64-entry segments drawn on demand from one shared pool;
 //   * per-page state: slot -> partition, last-use step (bucketed-LRU timestamps);
 //   * fp32 partition summaries in HBM.
-// A decode step of one layer enqueues four kernels on the caller's stream:
-// score -> select+manage -> retrieve+attention (cooperative) -> combine.
+// A decode step of one layer enqueues up to three kernels on the caller's stream:
+// score (only for narrow layers) -> select+manage -> retrieve+attention+combine
+// (cooperative).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -69,8 +71,8 @@ struct LayerBuf {
 constexpr int kNumStages = 5;  // select, manage, retrieve, attention, combine
 
 // Events of one timed call: 0 start, 1 after score, 2 after select/manage,
-// 3 after retrieve + attention (one kernel), 4 after combine.
-constexpr int kTimedEvents = 5;
+// 3 after retrieve + attention + combine (one kernel).
+constexpr int kTimedEvents = 4;
 struct TimedCall {
   cudaEvent_t ev[kTimedEvents];
 };
@@ -83,6 +85,8 @@ struct spin_ctx {
   uint32_t flags = 0;
   int B = 0, L = 0, Hq = 0, Hkv = 0, G = 0, k = 0, cap = 0, D = 0, P_max = 0, ppt = 1, n_chunks = 1;
   int sm_count = 0;
+  int select_group = 0;  // SPIN_SELECT_GROUP: threads of the top-k/manager group (0 = by unit size)
+  int retr_warps = 2;  // SPIN_RETRIEVE_WARPS (1..8): retriever warps per attend CTA
   std::vector<int64_t> ctx_len;
   std::vector<int32_t> P_b, ntok_b;
   std::vector<int64_t> poff_b;
@@ -188,9 +192,9 @@ int sync_ctx(spin_ctx* c) {
     };
     c->ms[0] += el(0, 1);
     c->ms[1] += el(1, 2);
-    c->ms[2] += el(2, 3);  // retrieve and attention share one kernel: both report its time
-    c->ms[3] += el(2, 3);
-    c->ms[4] += el(3, 4);
+    c->ms[2] += el(2, 3);  // retrieve, attention and combine share one kernel: retrieve and
+    c->ms[3] += el(2, 3);  // attention both report its time, combine reports none
+
     for (auto e : t.ev) c->spare_events.push_back(e);
   }
   c->pending.clear();
@@ -268,6 +272,8 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.n_chunks = c->n_chunks;
   a.ppt = c->ppt;
   a.S = (int32_t)c->S;
+  a.retr_warps = c->retr_warps;
+  a.select_group = c->select_group;
   a.P_b = c->d_P_b;
   a.ntok_b = c->d_ntok_b;
   a.poff_b = c->d_poff_b;
@@ -404,6 +410,13 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   SPIN_CUDA(nullptr, cudaMemset(c->d_stats, 0, 8 * 8), "initialising counters");
   SPIN_CUDA(nullptr, cudaMemset(c->d_err, 0, 4), "initialising counters");
 
+  if (const char* env = getenv("SPIN_RETRIEVE_WARPS")) {
+    const int v = atoi(env);
+    if (v >= 1 && v <= 8) c->retr_warps = v;
+  }
+  if (c->G > 8) c->retr_warps = std::min(c->retr_warps, 4);  // the two-tile kernel has four retriever warps
+  if (const char* env = getenv("SPIN_SELECT_GROUP")) c->select_group = atoi(env);  // 0 auto, 32, 512
+
   // attention work split: pages per task
   const int64_t pages_layer = (int64_t)c->B * c->Hkv * c->k;
   c->ppt = (int)std::max<int64_t>(1, std::min<int64_t>(8, pages_layer / (4 * std::max(1, c->sm_count))));
@@ -453,7 +466,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   return SPIN_OK;
 }
 
-// Enqueue one layer's step on `st`: score -> select/manage -> retrieve+attention -> combine.
+// Enqueue one layer's step on `st`: score -> select/manage -> retrieve+attention+combine.
 int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStream_t st) {
   LayerBuf& lb = c->layers[layer];
   LayerArgs a = lb.args;
@@ -477,8 +490,6 @@ int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStre
   mark(2);
   SPIN_CUDA(c, launch_attend_retrieve(a, &c->tmap, c->sm_count, st), "launching retrieve + attention");
   mark(3);
-  SPIN_CUDA(c, launch_combine(a, st), "launching combine");
-  mark(4);
   if (timed) {
     c->pending.push_back(tc);
     c->timed_calls += 1;

@@ -32,6 +32,8 @@ enum : uint32_t {
 // Per-layer arguments of the decode-step kernels (passed by value).
 struct LayerArgs {
   int32_t layer, B, Hq, Hkv, G, k, cap, D, P_max, n_chunks, ppt, S;
+  int32_t retr_warps;        // retriever warps active per CTA of the attend kernel
+  int32_t select_group;      // 0 = choose by unit size, else 32 or 512 threads for top-k + manager
   const int32_t* P_b;        // [B] partitions of request b
   const int32_t* ntok_b;     // [B] tokens of request b
   const int64_t* poff_b;     // [B] sum of P over earlier requests
@@ -75,7 +77,11 @@ __host__ __device__ inline int64_t host_page_index(const LayerArgs& a, int b, in
 }
 
 // Per-layer device counters.
-enum : int { kCtrMiss = 0, kCtrTaskHits = 1, kCtrTaskMisses = 2, kCtrStep = 3, kCtrRetrieve = 4, kNumCtr = 8 };
+enum : int {
+  kCtrMiss = 0, kCtrTaskHits = 1, kCtrTaskMisses = 2, kCtrStep = 3, kCtrRetrieve = 4,
+  kCtrArrive = 5,  // CTAs of the attend kernel done with their pages (grows by grid size every step)
+  kNumCtr = 8
+};
 
 // Device stats slots.
 enum : int { kStatHits = 0, kStatMisses = 1, kStatEvictions = 2, kStatLruRounds = 3, kStatSelected = 4 };
@@ -90,7 +96,6 @@ cudaError_t launch_score(const LayerArgs& a, cudaStream_t st);
 cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st);
 // Retrieve + attention in one cooperative persistent launch (one CTA per SM).
 cudaError_t launch_attend_retrieve(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st);
-cudaError_t launch_combine(const LayerArgs& a, cudaStream_t st);
 cudaError_t launch_resolve_all(const LayerArgs& a, int32_t* resolve, int32_t* live_segs, cudaStream_t st);
 size_t select_manage_smem_bytes(const LayerArgs& a);
 size_t attention_smem_bytes();
