@@ -74,7 +74,9 @@ typedef enum spin_status {
 typedef enum spin_flags {
   SPIN_FLAG_STAGE_TIMING = 1u << 0, /* record CUDA events around every stage; read via spin_stats */
   SPIN_FLAG_NO_GRAPH = 1u << 1,     /* launch the step's kernels directly instead of replaying a CUDA graph */
-  SPIN_FLAG_TEST_FAIL_PINNED = 1u << 16 /* test hook: the pinned host allocation reports failure */
+  SPIN_FLAG_TEST_FAIL_PINNED = 1u << 16, /* test hook: the pinned host allocation reports failure */
+  SPIN_FLAG_TEST_NO_RETRIEVE = 1u << 17  /* test hook: no page is retrieved, so the bounded wait for the
+                                            first missing page runs out and the step reports SPIN_ERR_TIMEOUT */
 } spin_flags;
 
 /* Configuration of one context. All counts are per context. */

@@ -690,7 +690,7 @@ cudaError_t select_manage_configure(size_t smem) {
 bool select_fuses_score(const LayerArgs& a) { return a.B * a.Hkv >= 64 && a.P_max <= 4096; }
 static bool select_single_warp(const LayerArgs& a) {
   if (a.select_group == 32 || a.select_group == kSelThreads) return a.select_group == 32;
-  return a.P_max <= 1024 && a.cap <= 1024 && a.k <= 256;
+  return a.P_max <= 128 && a.cap <= 1024 && a.k <= 256;  // measured: 512 threads win from P = 512 up
 }
 
 cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st) {

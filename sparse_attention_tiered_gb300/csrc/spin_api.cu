@@ -415,6 +415,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     if (v >= 1 && v <= 8) c->retr_warps = v;
   }
   if (c->G > 8) c->retr_warps = std::min(c->retr_warps, 4);  // the two-tile kernel has four retriever warps
+  if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = 0;    // nothing publishes a retrieved page
   if (const char* env = getenv("SPIN_SELECT_GROUP")) c->select_group = atoi(env);  // 0 auto, 32, 512
 
   // attention work split: pages per task

@@ -224,3 +224,30 @@ def test_full_size_sampled(name, nunits):
     assert rep.tie_divergences <= max(1, rep.compared_units // 200), rep.notes
     if name.startswith("stress"):
         assert st["evictions"] > 0
+
+
+def test_bounded_wait_reports_timeout():
+    """Failure detection without a GPU fault: with the retriever warps disabled nothing ever
+    publishes a missing page, so the producer's bounded wait runs out (about 2 s); the step
+    finishes, the device error word says so, and the context keeps reporting SPIN_ERR_TIMEOUT."""
+    import time
+    from sparse_attention_tiered_gb300 import SpinContext, SpinError
+    from sparse_attention_tiered_gb300._binding import SPIN_ERR_TIMEOUT, SPIN_FLAG_TEST_NO_RETRIEVE
+    w = W.Workload("timeout", B=1, L=1, Hq=4, Hkv=2, ctx_len=[64 * 40], topk=4, buf_mult=2,
+                   drift_a=0.9, drift_c=0.1, steps=1, seed=37)
+    with SpinContext.for_workload(w, flags=SPIN_FLAG_TEST_NO_RETRIEVE) as ctx:
+        k, v = w.request_kv(0, 0)
+        ctx.index_offload_host(0, 0, k, v)
+        q = torch.from_numpy(w.queries().bf16()[0].view(np.int16)).cuda()
+        out = torch.empty((1, 4, 128), dtype=torch.float32, device="cuda")
+        t0 = time.time()
+        ctx.decode_step(0, q, out)
+        st = ctx.stats(check=False)
+        assert st["rc"] == SPIN_ERR_TIMEOUT and st["device_error"] & 2
+        assert time.time() - t0 < 60
+        with pytest.raises(SpinError) as e:
+            ctx.decode_step(0, q, out)
+        assert e.value.code == SPIN_ERR_TIMEOUT
+    # the CUDA context is still usable afterwards
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum()) == 8.0
