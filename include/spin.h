@@ -73,7 +73,9 @@ typedef enum spin_status {
 
 typedef enum spin_flags {
   SPIN_FLAG_STAGE_TIMING = 1u << 0, /* record CUDA events around every stage; read via spin_stats */
-  SPIN_FLAG_NO_GRAPH = 1u << 1,     /* launch the step's kernels directly instead of replaying a CUDA graph */
+  SPIN_FLAG_TIER_SPLIT = 1u << 2,   /* tier-split metadata ([XT] §3, [GS] §2C): the second-level segment
+                                       entries live in pinned host memory; the directory, the segments'
+                                       live counts and the allocation bitmap stay in HBM */
   SPIN_FLAG_TEST_FAIL_PINNED = 1u << 16, /* test hook: the pinned host allocation reports failure */
   SPIN_FLAG_TEST_NO_RETRIEVE = 1u << 17  /* test hook: no page is retrieved, so the bounded wait for the
                                             first missing page runs out and the step reports SPIN_ERR_TIMEOUT */
@@ -107,7 +109,8 @@ typedef struct spin_stats_t {
   int64_t selected_bytes;    /* selected pages * SPIN_PAGE_BYTES (bytes attention read) */
   int64_t live_segments;     /* second-level segments currently allocated */
   int64_t pool_segments;     /* segments in the shared pool */
-  int64_t metadata_bytes;    /* HBM bytes of the page metadata: directory + segment pool + per-page state */
+  int64_t metadata_bytes;    /* HBM bytes of the page metadata: directory + segment pool (unless tier
+                                split) + live counts + bitmap + per-page state */
   int64_t flat_table_bytes;  /* HBM bytes of a flat [unit][max partitions] table plus the same per-page state */
   int64_t hbm_pool_bytes;    /* HBM page pool */
   int64_t host_store_bytes;  /* pinned host page store */

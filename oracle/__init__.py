@@ -90,6 +90,11 @@ def _bind(L):
     L.oracle_unit_export.argtypes = [vp, vp, vp, vp]
     L.oracle_unit_slot.argtypes = [vp, i32]
     L.oracle_unit_slot.restype = vp
+    L.oracle_unit_create_tail.argtypes = [i32, i32, i32]
+    L.oracle_unit_create_tail.restype = vp
+    L.oracle_unit_grow.argtypes = [vp]
+    L.oracle_unit_grow.restype = i32
+    L.oracle_attend_tail.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, vp]
     return L
 
 
@@ -261,3 +266,88 @@ def step_units_parallel(units, qs, k: int, t: int, threads: int = 0, lib=None):
                         sel.ctypes.data, ss.ctypes.data, sh.ctypes.data, None, out.ctypes.data)
     used = lib.oracle_step_units(handles, ios, n, threads)
     return used, keep
+
+
+class TailUnit:
+    """Oracle unit with KV append: complete 64-token partitions are selectable; the tail
+    (fewer than 64 newest tokens) is attended at every step and becomes a partition
+    (summarised and offloaded) when it fills."""
+
+    def __init__(self, k_bits: np.ndarray, v_bits: np.ndarray, cap: int, append_max: int, lib=None):
+        self.lib = lib or load()
+        n = k_bits.shape[0]
+        self.cap = cap
+        self.ntok = n
+        Pc = n // PART
+        P_cap = (n + append_max + PART - 1) // PART
+        self.P_cap = P_cap
+        self.h = self.lib.oracle_unit_create_tail(Pc, max(P_cap, 1), cap)
+        self.summ = index(k_bits[:Pc * PART], self.lib) if Pc else np.zeros((0, D))
+        self.host_pages = offload(k_bits[:Pc * PART], v_bits[:Pc * PART], self.lib) if Pc else \
+            np.zeros((0, 2, PART, D), np.uint16)
+        self.tail = np.zeros((2, PART, D), np.uint16)
+        self.tail_n = n - Pc * PART
+        self.tail[0, :self.tail_n] = k_bits[Pc * PART:]
+        self.tail[1, :self.tail_n] = v_bits[Pc * PART:]
+
+    @property
+    def P(self) -> int:
+        return self.summ.shape[0]
+
+    def __del__(self):
+        h = getattr(self, "h", None)
+        if h:
+            self.lib.oracle_unit_destroy(h)
+            self.h = None
+
+    def append(self, k_row: np.ndarray, v_row: np.ndarray):
+        """One new token (bf16 bits [128] each)."""
+        self.tail[0, self.tail_n] = k_row
+        self.tail[1, self.tail_n] = v_row
+        self.tail_n += 1
+        self.ntok += 1
+        if self.tail_n == PART:
+            self.summ = np.concatenate([self.summ, index(self.tail[0], self.lib)])
+            self.host_pages = np.concatenate([self.host_pages, self.tail[None].copy()])
+            assert self.lib.oracle_unit_grow(self.h) == 0, "append beyond the unit's capacity"
+            self.tail_n = 0
+
+    def export(self):
+        sp = np.empty(self.cap, np.int32)
+        lu = np.empty(self.cap, np.int32)
+        rs = np.empty(max(self.P_cap, 1), np.int32)
+        self.lib.oracle_unit_export(self.h, _p(sp), _p(lu), _p(rs))
+        return sp, lu, rs[:self.P]
+
+    def live_segments(self) -> int:
+        return self.lib.oracle_live_segments(self.h)
+
+    def manage(self, sel: np.ndarray, t: int):
+        sel = np.ascontiguousarray(sel, np.int32)
+        k = sel.shape[0]
+        sel_slot = np.empty(max(k, 1), np.int32)
+        sel_hit = np.empty(max(k, 1), np.uint8)
+        victims = np.empty(self.cap, np.int32)
+        mo = ManageOut()
+        pages = np.ascontiguousarray(self.host_pages) if self.P else np.zeros((1, 2, PART, D), np.uint16)
+        self.lib.oracle_manage(self.h, _p(sel), k, t, _p(pages), _p(sel_slot), _p(sel_hit), _p(victims),
+                               ctypes.byref(mo))
+        return sel_slot[:k].copy(), sel_hit[:k].astype(bool), victims[:mo.evicted].copy(), mo
+
+    def attend(self, sel: np.ndarray, sel_slot: np.ndarray, q_bits: np.ndarray) -> np.ndarray:
+        sel = np.ascontiguousarray(sel, np.int32)
+        sel_slot = np.ascontiguousarray(sel_slot, np.int32)
+        q_bits = np.ascontiguousarray(q_bits, np.uint16)
+        G = q_bits.shape[0]
+        out = np.empty((G, D), np.float64)
+        self.lib.oracle_attend_tail(self.h, _p(sel), _p(sel_slot), sel.shape[0], _p(q_bits), G,
+                                    _p(self.tail), self.tail_n, _p(out))
+        return out
+
+    def step(self, q_bits: np.ndarray, k: int, t: int) -> dict:
+        """Select over the complete partitions -> Manage/Retrieve -> Attention (with the tail)."""
+        sc = scores(self.summ, q_bits, self.lib) if self.P else np.zeros(0)
+        sel = topk(sc, k, self.lib) if self.P else np.zeros(0, np.int32)
+        ss, hit, vic, mo = self.manage(sel, t)
+        out = self.attend(sel, ss, q_bits)
+        return dict(scores=sc, sel=sel, sel_slot=ss, sel_hit=hit, victims=vic, mo=mo, out=out)

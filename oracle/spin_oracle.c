@@ -142,7 +142,8 @@ int32_t oracle_topk(const double* sc, int64_t P, int32_t k, int32_t* sel) {
 /* partitions; entry = resident slot or -1.                                    */
 /* ------------------------------------------------------------------------- */
 typedef struct oracle_unit {
-  int32_t P;           /* partitions of the unit */
+  int32_t P;           /* partitions of the unit (in tail mode: the complete ones) */
+  int32_t P_cap;       /* partitions the unit may grow to (tail mode), else P */
   int32_t ntok;        /* valid tokens (last partition may be short) */
   int32_t cap;         /* resident capacity in pages (mandatory + buffer) */
   int32_t D;           /* directory entries = ceil(P / 64) */
@@ -160,6 +161,7 @@ oracle_unit* oracle_unit_create(int32_t ntok, int32_t cap) {
   u->ntok = ntok;
   u->P = (ntok + OPART - 1) / OPART;
   u->cap = cap;
+  u->P_cap = u->P;
   u->D = (u->P + OSEG - 1) / OSEG;
   u->S = u->D < cap ? u->D : cap;
   if (u->S < 1) u->S = 1;
@@ -176,6 +178,27 @@ oracle_unit* oracle_unit_create(int32_t ntok, int32_t cap) {
     u->last_use[i] = 0;
   }
   return u;
+}
+
+/* ------------------------------------------------------------------------- */
+/* KV append (tail mode). reading: new tokens go into a tail partition that is */
+/* attended at every step; it is not selectable until it holds 64 tokens, when */
+/* it is summarised, offloaded and becomes partition P (the caller appends its */
+/* summary and host page, then calls oracle_unit_grow). The two-level table is */
+/* sized for the partitions the unit may grow to.                              */
+/* ------------------------------------------------------------------------- */
+oracle_unit* oracle_unit_create_tail(int32_t P_complete, int32_t P_capacity, int32_t cap) {
+  oracle_unit* u = oracle_unit_create(P_capacity * OPART, cap);
+  u->P = P_complete;
+  u->ntok = P_complete * OPART;
+  return u;
+}
+
+int32_t oracle_unit_grow(oracle_unit* u) {
+  if (u->P >= u->P_cap) return -1;
+  u->P += 1;
+  u->ntok = u->P * OPART;
+  return 0;
 }
 
 void oracle_unit_destroy(oracle_unit* u) {
@@ -331,6 +354,68 @@ void oracle_manage(oracle_unit* u, const int32_t* sel, int32_t keff, int32_t t, 
 /* token of the selected partitions, read from their resident pages.           */
 /* out[g][i], double.                                                          */
 /* ------------------------------------------------------------------------- */
+/* Attention over the selected pages plus, when tail_n > 0, the first tail_n tokens of
+ * the tail page tail_kv ([2][64][128]: K rows then V rows). */
+void oracle_attend_tail(const oracle_unit* u, const int32_t* sel, const int32_t* sel_slot, int32_t keff,
+                        const uint16_t* q, int32_t G, const uint16_t* tail_kv, int32_t tail_n, double* out) {
+  int64_t n = tail_n;
+  for (int32_t j = 0; j < keff; ++j) {
+    int32_t p = sel[j];
+    n += (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+  }
+  double* x = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  const double scale = 1.0 / sqrt((double)OD);
+  for (int32_t g = 0; g < G; ++g) {
+    double* o = out + g * OD;
+    for (int i = 0; i < OD; ++i) o[i] = 0.0;
+    if (n == 0) continue;
+    /* scores of every attended token, pages in selection order, then the tail */
+    int64_t c = 0;
+    double m = -INFINITY;
+    for (int32_t j = 0; j <= keff; ++j) {
+      const uint16_t* K;
+      int32_t valid;
+      if (j < keff) {
+        int32_t p = sel[j];
+        valid = (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+        K = u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS;
+      } else {
+        valid = tail_n;
+        K = tail_kv;
+      }
+      for (int32_t r = 0; r < valid; ++r) {
+        double sdot = 0.0;
+        for (int i = 0; i < OD; ++i) sdot += bf(q[g * OD + i]) * bf(K[r * OD + i]);
+        x[c] = sdot * scale;
+        if (x[c] > m) m = x[c];
+        ++c;
+      }
+    }
+    double l = 0.0;
+    c = 0;
+    for (int32_t j = 0; j <= keff; ++j) {
+      const uint16_t* V;
+      int32_t valid;
+      if (j < keff) {
+        int32_t p = sel[j];
+        valid = (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+        V = u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS + OPART * OD;
+      } else {
+        valid = tail_n;
+        V = tail_kv + OPART * OD;
+      }
+      for (int32_t r = 0; r < valid; ++r) {
+        double w = exp(x[c] - m);
+        l += w;
+        for (int i = 0; i < OD; ++i) o[i] += w * bf(V[r * OD + i]);
+        ++c;
+      }
+    }
+    for (int i = 0; i < OD; ++i) o[i] /= l;
+  }
+  free(x);
+}
+
 void oracle_attend(const oracle_unit* u, const int32_t* sel, const int32_t* sel_slot, int32_t keff,
                    const uint16_t* q, int32_t G, double* out) {
   int64_t n = 0;

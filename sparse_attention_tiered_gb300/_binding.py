@@ -25,7 +25,7 @@ SPIN_ERR_STATE = 6
 STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "CUDA", 3: "OOM", 4: "CAPACITY", 5: "TIMEOUT", 6: "STATE"}
 
 SPIN_FLAG_STAGE_TIMING = 1 << 0
-SPIN_FLAG_NO_GRAPH = 1 << 1
+SPIN_FLAG_TIER_SPLIT = 1 << 2
 SPIN_FLAG_TEST_FAIL_PINNED = 1 << 16
 SPIN_FLAG_TEST_NO_RETRIEVE = 1 << 17
 

@@ -100,6 +100,7 @@ struct spin_ctx {
   int32_t *d_P_b = nullptr, *d_ntok_b = nullptr;
   int64_t* d_poff_b = nullptr;
   int32_t *d_dir = nullptr, *d_seg = nullptr, *d_seg_live = nullptr;
+  int32_t* h_seg = nullptr;  // tier split: the segment entries in pinned host memory (d_seg maps it)
   uint32_t* d_bitmap = nullptr;
   int32_t *d_slot_part = nullptr, *d_last_use = nullptr;
   unsigned long long* d_stats = nullptr;
@@ -160,6 +161,8 @@ void free_all(spin_ctx* c) {
   c->dev_allocs.clear();
   if (c->h_store) cudaFreeHost(c->h_store);
   c->h_store = nullptr;
+  if (c->h_seg) cudaFreeHost(c->h_seg);
+  c->h_seg = nullptr;
   for (auto& t : c->pending)
     for (auto e : t.ev) cudaEventDestroy(e);
   c->pending.clear();
@@ -383,7 +386,24 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   ALLOC(c->d_ntok_b, c->B, "allocating request tables");
   ALLOC(c->d_poff_b, c->B, "allocating request tables");
   ALLOC(c->d_dir, c->units * c->D, "allocating the directory");
-  ALLOC(c->d_seg, c->S * kSeg, "allocating the segment pool");
+  if (c->flags & SPIN_FLAG_TIER_SPLIT) {
+    // Tier split: the capacity-heavy second-level entries go to host memory, read and
+    // written by the manager kernel with plain loads and stores over the host link; the
+    // directory, live counts and allocation bitmap (touched by atomics) stay in HBM.
+    void* hs = nullptr;
+    e = cudaHostAlloc(&hs, (size_t)c->S * kSeg * 4, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(nullptr, SPIN_ERR_OOM, "pinned allocation of the segment pool failed: %s", cudaGetErrorString(e));
+    }
+    c->h_seg = static_cast<int32_t*>(hs);
+    memset(c->h_seg, 0xff, (size_t)c->S * kSeg * 4);
+    void* ds = nullptr;
+    if ((e = cudaHostGetDevicePointer(&ds, hs, 0)) != cudaSuccess) return cuda_fail(nullptr, e, "mapping the segment pool");
+    c->d_seg = static_cast<int32_t*>(ds);
+  } else {
+    ALLOC(c->d_seg, c->S * kSeg, "allocating the segment pool");
+  }
   ALLOC(c->d_seg_live, c->S, "allocating the segment pool");
   const int64_t nwords = (c->S + 31) / 32;
   ALLOC(c->d_bitmap, nwords, "allocating the segment bitmap");
@@ -391,14 +411,15 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   ALLOC(c->d_last_use, slots, "allocating the page state");
   ALLOC(c->d_stats, 8, "allocating counters");
   ALLOC(c->d_err, 1, "allocating counters");
-  c->bytes_meta = (c->units * c->D + c->S * kSeg + c->S + nwords + 2 * slots) * 4;
+  c->bytes_meta = (c->units * c->D + (c->h_seg ? 0 : c->S * kSeg) + c->S + nwords + 2 * slots) * 4;
   c->bytes_flat = (c->units * (int64_t)c->P_max + 2 * slots) * 4;
 
   SPIN_CUDA(nullptr, cudaMemcpy(c->d_P_b, c->P_b.data(), 4 * c->B, cudaMemcpyHostToDevice), "uploading tables");
   SPIN_CUDA(nullptr, cudaMemcpy(c->d_ntok_b, c->ntok_b.data(), 4 * c->B, cudaMemcpyHostToDevice), "uploading tables");
   SPIN_CUDA(nullptr, cudaMemcpy(c->d_poff_b, c->poff_b.data(), 8 * c->B, cudaMemcpyHostToDevice), "uploading tables");
   SPIN_CUDA(nullptr, cudaMemset(c->d_dir, 0xff, (size_t)c->units * c->D * 4), "initialising the directory");
-  SPIN_CUDA(nullptr, cudaMemset(c->d_seg, 0xff, (size_t)c->S * kSeg * 4), "initialising the segment pool");
+  if (!c->h_seg)
+    SPIN_CUDA(nullptr, cudaMemset(c->d_seg, 0xff, (size_t)c->S * kSeg * 4), "initialising the segment pool");
   SPIN_CUDA(nullptr, cudaMemset(c->d_seg_live, 0, (size_t)c->S * 4), "initialising the segment pool");
   {
     std::vector<uint32_t> bm(nwords, 0u);

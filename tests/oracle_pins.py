@@ -306,5 +306,38 @@ def check_step_consistency(lib):
         qs.advance()
 
 
+def check_append_tail(lib):
+    """KV append (tail mode): the tail is attended; with every complete partition selected
+    the output is dense attention over all tokens (torch SDPA, float64); appending tokens
+    one by one gives the same state as building the unit from all of them; a tail-only
+    unit attends its tail."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(12)
+    for n0, n_app, G in ((200, 90, 3), (30, 20, 2), (128, 64, 5)):
+        n = n0 + n_app
+        k, v = rand_kv(rng, n, scale=1.3)
+        q = f32_to_bf16_bits(rng.standard_normal((G, D)).astype(np.float32))
+        a = O.TailUnit(k[:n0], v[:n0], cap=8, append_max=n_app, lib=lib)
+        for r in range(n0, n):
+            a.append(k[r], v[r])
+        b = O.TailUnit(k, v, cap=8, append_max=0, lib=lib)
+        assert a.P == b.P == n // 64 and a.tail_n == b.tail_n == n % 64
+        assert np.array_equal(a.summ, b.summ) and np.array_equal(a.host_pages, b.host_pages)
+        assert np.array_equal(a.tail[:, :a.tail_n], b.tail[:, :b.tail_n])
+        ra = a.step(q, k=max(a.P, 1), t=0)
+        rb = b.step(q, k=max(b.P, 1), t=0)
+        assert np.array_equal(ra["out"], rb["out"])
+        qt = torch.from_numpy(bf(q)).view(1, G, 1, D)
+        kt = torch.from_numpy(bf(k)).view(1, 1, n, D).expand(1, G, n, D)
+        vt = torch.from_numpy(bf(v)).view(1, 1, n, D).expand(1, G, n, D)
+        ref = F.scaled_dot_product_attention(qt, kt, vt).view(G, D).numpy()
+        assert np.abs(ra["out"] - ref).max() <= 1e-12, "tail mode must attend every token once"
+        # partitions created by appends resolve through the table like the others: the same
+        # query again hits every page it just retrieved
+        ra2 = a.step(q, k=max(a.P, 1), t=1)
+        assert ra2["mo"].hits == min(max(a.P, 1), a.P) == len(ra2["sel"]) and ra2["mo"].misses == 0
+
+
 ALL_CHECKS = [check_dense_attention, check_attention_closed_forms, check_scores_probe, check_topk_bruteforce,
-              check_index, check_lru_invariants, check_lru_hand_trace, check_step_consistency]
+              check_index, check_lru_invariants, check_lru_hand_trace, check_step_consistency, check_append_tail]

@@ -251,3 +251,17 @@ def test_bounded_wait_reports_timeout():
     # the CUDA context is still usable afterwards
     x = torch.ones(4, device="cuda")
     assert float((x * 2).sum()) == 8.0
+
+
+def test_tier_split_metadata_same_results_less_hbm():
+    """Second-level segments in pinned host memory: identical lockstep results, and the
+    page metadata left in HBM shrinks by the segment pool."""
+    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_TIER_SPLIT
+    w = W.Workload("tier", B=3, L=2, Hq=10, Hkv=2, ctx_len=[1000, 4113, 9000], topk=8, buf_mult=2,
+                   drift_a=0.8, drift_c=0.2, steps=16, seed=41)
+    rep_a, st_a = _run(w)
+    rep_b, st_b = _run(w, flags=SPIN_FLAG_TIER_SPLIT)
+    assert rep_b.max_out_err <= OUT_TOL and rep_b.evictions == rep_a.evictions
+    for key in ("hits", "misses", "evictions", "live_segments"):
+        assert st_a[key] == st_b[key], key
+    assert st_b["metadata_bytes"] == st_a["metadata_bytes"] - st_a["pool_segments"] * 64 * 4

@@ -26,10 +26,11 @@ MUTANTS = {
                        "if (x->s > y->s) return 1;\n  if (x->s < y->s) return -1;"),
     "ties_to_higher_index": ("return (x->p > y->p) - (x->p < y->p);", "return (x->p < y->p) - (x->p > y->p);"),
     "index_divides_by_64": ("summ[p * OD + i] = s / (double)(t1 - t0);", "summ[p * OD + i] = s / (double)OPART;"),
-    "softmax_scale_1_over_d": ("const double scale = 1.0 / sqrt((double)OD);", "const double scale = 1.0 / (double)OD;"),
+    # the next three anchors occur in both attention routines (with and without the tail); both are mutated
+    "softmax_scale_1_over_d": ("const double scale = 1.0 / sqrt((double)OD);", "const double scale = 1.0 / (double)OD;", 2),
     "attention_values_from_keys": ("u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS + OPART * OD;",
-                                   "u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS;"),
-    "attention_drops_max_shift": ("double w = exp(x[c] - m);", "double w = exp(x[c] - m) * (c == 0 ? 0.5 : 1.0);"),
+                                   "u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS;", 2),
+    "attention_drops_max_shift": ("double w = exp(x[c] - m);", "double w = exp(x[c] - m) * (c == 0 ? 0.5 : 1.0);", 2),
     # (Dropping the mandatory-page exclusion alone is an equivalent mutant: hits are
     # stamped with the current step first, so they sit in the newest bucket, which
     # the cutoff never reaches because cap >= k. It is therefore not listed.)
@@ -42,6 +43,8 @@ MUTANTS = {
                             "int32_t bucket = (age < OBUCKETS - 1 ? age : OBUCKETS - 1);\n      hist"),
     "segment_never_freed": ("if (u->seg_live[s] == 0) {", "if (u->seg_live[s] == -7) {"),
     "miss_copies_wrong_page": ("host_pages + (int64_t)p * OPAGE_ELEMS,", "host_pages + (int64_t)(p / 2) * OPAGE_ELEMS,"),
+    "append_tail_not_attended": ("        valid = tail_n;\n        K = tail_kv;", "        valid = 0;\n        K = tail_kv;"),
+    "append_no_growth": ("  u->P += 1;\n  u->ntok = u->P * OPART;", "  u->ntok = u->P * OPART;"),
     "offload_drops_tail_token": ("for (int64_t t = 0; t < ntok; ++t) {\n    int64_t p = t / OPART",
                                  "for (int64_t t = 0; t < ntok - 1; ++t) {\n    int64_t p = t / OPART"),
 }
