@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
+    ap.add_argument("--host-alloc", default="cuda", choices=["cuda", "hugepages"],
+                    help="pinned host page store: cudaHostAlloc (default) or huge-page mmap + cudaHostRegister")
     return ap.parse_args()
 
 
@@ -269,7 +271,7 @@ def bench_reference(args):
 def bench_spin(args):
     import torch
     from sparse_attention_tiered_gb300 import SpinContext
-    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_STAGE_TIMING
+    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_HOST_HUGEPAGES, SPIN_FLAG_STAGE_TIMING
 
     R = Ranks()
     world, rank, local = R.world, R.rank, R.local
@@ -286,7 +288,8 @@ def bench_spin(args):
 
     # ---- set-up (untimed): Index + Offload of every request and layer ----
     t_setup = time.perf_counter()
-    ctx = SpinContext.for_workload(w, device=local, flags=SPIN_FLAG_STAGE_TIMING)
+    flags = SPIN_FLAG_STAGE_TIMING | (SPIN_FLAG_HOST_HUGEPAGES if args.host_alloc == "hugepages" else 0)
+    ctx = SpinContext.for_workload(w, device=local, flags=flags)
     kbuf = vbuf = None
     keep = []
     for l in range(w.L):
@@ -386,7 +389,9 @@ def bench_spin(args):
             "config": {"workload": workload_desc(w), "l2": "inputs larger than L2 (selected KV per layer "
                        f"{w.selected_kv_bytes_per_step() // w.L / 2**20:.0f} MiB > 129 MB)",
                        "parallelism": f"dp{world} (independent requests per GPU)", "timed_decode_steps": K,
-                       "first_timed_step": Wm},
+                       "first_timed_step": Wm,
+                       "host_store": ("cudaHostAlloc" if args.host_alloc == "cuda"
+                                      else "huge-page mmap + cudaHostRegister")},
             "roofline": {"bound": "host_link" if host_bound else "hbm", "kernel": "attend_retrieve_kernel",
                          "achieved": host_achieved if host_bound else hbm_achieved,
                          "peak": host_gbs if host_bound else hbm_gbs, "unit": "GB/s",

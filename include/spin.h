@@ -76,6 +76,10 @@ typedef enum spin_flags {
   SPIN_FLAG_TIER_SPLIT = 1u << 2,   /* tier-split metadata ([XT] §3, [GS] §2C): the second-level segment
                                        entries live in pinned host memory; the directory, the segments'
                                        live counts and the allocation bitmap stay in HBM */
+  SPIN_FLAG_HOST_HUGEPAGES = 1u << 3, /* allocate the pinned host page store as an anonymous mapping aligned to
+                                        and advised for transparent huge pages, registered with
+                                        cudaHostRegister, instead of with cudaHostAlloc (falls back to
+                                        cudaHostAlloc when mapping or registering fails) */
   SPIN_FLAG_TEST_FAIL_PINNED = 1u << 16, /* test hook: the pinned host allocation reports failure */
   SPIN_FLAG_TEST_NO_RETRIEVE = 1u << 17  /* test hook: no page is retrieved, so the bounded wait for the
                                             first missing page runs out and the step reports SPIN_ERR_TIMEOUT */
@@ -96,6 +100,11 @@ typedef struct spin_config {
   int64_t seg_pool_segments; /* segments in the shared second-level pool; 0 = enough for any page state */
   int32_t device;            /* CUDA device ordinal */
   uint32_t flags;            /* spin_flags */
+  int32_t append_tokens;     /* 0: fixed context. > 0: KV-append (tail) mode, each request may grow by up to
+                                this many tokens through spin_append_kv. In tail mode only complete 64-token
+                                partitions are selectable; the newest ctx % 64 tokens form the request's tail,
+                                which every decode step attends in full, and a tail that reaches 64 tokens is
+                                summarised, offloaded and becomes the next partition. */
 } spin_config;
 
 /* Counters since spin_create. */
@@ -122,11 +131,14 @@ typedef struct spin_stats_t {
   double ms_attention;
   double ms_combine;
   uint32_t device_error;     /* raw device error word (0 = none) */
+  int64_t appended_tokens;   /* tokens appended through spin_append_kv (all layers, all requests) */
+  int64_t tail_flushes;      /* tails that filled and became partitions (per layer and request) */
 } spin_stats_t;
 
 /* Host-side view filled by spin_debug_export; any pointer may be NULL. Shapes use
  * U = batch * kv_heads units of the layer (unit ul = b * kv_heads + h), k = topk,
- * cap = buf_mult * topk, Pmax = the largest partition count of any request. */
+ * cap = buf_mult * topk, Pmax = the largest partition count of any request (in tail
+ * mode: the largest count a request can reach, ceil((ctx_len + append_tokens) / 64)). */
 typedef struct spin_state_view {
   int32_t* keff;       /* [U] partitions selected in the last step = min(k, P_b) */
   int32_t* sel;        /* [U][k] selected partitions of the last step, ascending, -1 padded */
@@ -156,11 +168,25 @@ int spin_create(const spin_config* cfg, spin_ctx** out);
 int spin_index_offload(spin_ctx* ctx, int32_t b, int32_t layer, const uint16_t* k, const uint16_t* v,
                        int64_t n_tokens, int32_t src_is_host, spin_stream_t stream);
 
+/* KV append ([XT] §1, Figure 3: Index and Offload also run for the tokens decode
+ * produces; the pages leave the mechanics open). Appends ONE token to every request
+ * of `layer`: k_new, v_new are device bf16 [batch][kv_heads][128], 16-byte aligned.
+ * The token goes into the request's tail page in HBM (one per unit); when that tail
+ * holds 64 tokens it is summarised (fp32 mean key), written into the pinned host
+ * store as the request's next partition and emptied, all on the device. Needs a
+ * context created with append_tokens > 0 (else SPIN_ERR_STATE) whose requests of
+ * `layer` have all been offloaded; a request that would grow past
+ * ctx_len[b] + append_tokens tokens returns SPIN_ERR_CAPACITY and nothing is
+ * enqueued. Asynchronous on `stream`; the appends and decode steps of one layer must
+ * be ordered on one stream. In a decode loop the token of step t is appended before
+ * that step's spin_decode_step, which then attends it. */
+int spin_append_kv(spin_ctx* ctx, int32_t layer, const uint16_t* k_new, const uint16_t* v_new, spin_stream_t stream);
+
 /* One decode step of one layer for the whole batch ([XT] §2 and Fig 5 steps 1-4,
  * §3; [GS] §2B-C). q: device bf16 [batch][q_heads][128]; out: device fp32
  * [batch][q_heads][128] = softmax(q K_sel^T / sqrt(128)) V_sel over the tokens of
- * the k selected partitions of the query head's KV head (zeros for an empty
- * request). Asynchronous on `stream`; the layer's step counter t advances by one
+ * the k selected partitions of the query head's KV head, plus, in tail mode, the
+ * request's tail tokens (zeros for an empty request). Asynchronous on `stream`; the layer's step counter t advances by one
  * per call. Requires every request of `layer` to have been offloaded. */
 int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream);
 
@@ -180,10 +206,12 @@ int spin_stats(spin_ctx* ctx, spin_stats_t* out);
 int spin_debug_export(spin_ctx* ctx, int32_t layer, spin_state_view* view);
 
 /* Synchronises, then copies the 32768-byte HBM page in slot `slot` of unit
- * (layer, b, h) to dst (host). */
+ * (layer, b, h) to dst (host). In tail mode slot == buf_mult * topk names the
+ * unit's tail page. */
 int spin_debug_read_page(spin_ctx* ctx, int32_t layer, int32_t b, int32_t h, int32_t slot, uint16_t* dst);
 
-/* Synchronises, then copies the fp32 summaries [P_b][128] of unit (layer, b, h) to dst (host). */
+/* Synchronises, then copies the fp32 summaries [P_b][128] of unit (layer, b, h) to dst (host);
+ * P_b = the request's current partition count (in tail mode: its complete partitions). */
 int spin_debug_summaries(spin_ctx* ctx, int32_t layer, int32_t b, int32_t h, float* dst);
 
 /* Allocation-free Select, for callers that cannot allocate device memory (code

@@ -344,6 +344,15 @@ class TailUnit:
                                     _p(self.tail), self.tail_n, _p(out))
         return out
 
+    def clone_empty(self, cap: int) -> "TailUnit":
+        """A unit with the same partitions, summaries, host pages and tail, and nothing resident."""
+        c = TailUnit.__new__(TailUnit)
+        c.lib, c.cap, c.ntok, c.P_cap = self.lib, cap, self.ntok, self.P_cap
+        c.h = self.lib.oracle_unit_create_tail(self.P, max(self.P_cap, 1), cap)
+        c.summ, c.host_pages = self.summ, self.host_pages
+        c.tail, c.tail_n = self.tail.copy(), self.tail_n
+        return c
+
     def step(self, q_bits: np.ndarray, k: int, t: int) -> dict:
         """Select over the complete partitions -> Manage/Retrieve -> Attention (with the tail)."""
         sc = scores(self.summ, q_bits, self.lib) if self.P else np.zeros(0)

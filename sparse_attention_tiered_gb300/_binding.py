@@ -26,6 +26,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "CUDA", 3: "OOM", 4: "CAPACITY", 5: "T
 
 SPIN_FLAG_STAGE_TIMING = 1 << 0
 SPIN_FLAG_TIER_SPLIT = 1 << 2
+SPIN_FLAG_HOST_HUGEPAGES = 1 << 3
 SPIN_FLAG_TEST_FAIL_PINNED = 1 << 16
 SPIN_FLAG_TEST_NO_RETRIEVE = 1 << 17
 
@@ -35,7 +36,7 @@ PAGE_BYTES = 32768
 SPIN_NOALLOC_MAX_SCORES_DEFAULT = 1 << 20  # SPIN_NOALLOC_MAX_SCORES in include/spin.h
 
 # Every symbol include/spin.h declares.
-EXPORTS = ("spin_create", "spin_index_offload", "spin_decode_step", "spin_decode_step_host", "spin_stats",
+EXPORTS = ("spin_create", "spin_index_offload", "spin_append_kv", "spin_decode_step", "spin_decode_step_host", "spin_stats",
            "spin_debug_export", "spin_debug_read_page", "spin_debug_summaries", "spin_destroy", "spin_last_error",
            "spin_select_noalloc")
 
@@ -61,6 +62,7 @@ class spin_config(ctypes.Structure):
         ("seg_pool_segments", ctypes.c_int64),
         ("device", ctypes.c_int32),
         ("flags", ctypes.c_uint32),
+        ("append_tokens", ctypes.c_int32),
     ]
 
 
@@ -70,7 +72,7 @@ class spin_stats_t(ctypes.Structure):
         "live_segments", "pool_segments", "metadata_bytes", "flat_table_bytes", "hbm_pool_bytes",
         "host_store_bytes", "summary_bytes", "timed_calls")] + [
         (n, ctypes.c_double) for n in ("ms_select", "ms_manage", "ms_retrieve", "ms_attention", "ms_combine")] + [
-        ("device_error", ctypes.c_uint32)]
+        ("device_error", ctypes.c_uint32), ("appended_tokens", ctypes.c_int64), ("tail_flushes", ctypes.c_int64)]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -111,6 +113,8 @@ def load(build_if_missing: bool = True):
             L.spin_create.restype = ctypes.c_int
             L.spin_index_offload.argtypes = [vp, i32, i32, vp, vp, i64, i32, vp]
             L.spin_index_offload.restype = ctypes.c_int
+            L.spin_append_kv.argtypes = [vp, i32, vp, vp, vp]
+            L.spin_append_kv.restype = ctypes.c_int
             L.spin_decode_step.argtypes = [vp, i32, vp, vp, vp]
             L.spin_decode_step.restype = ctypes.c_int
             L.spin_decode_step_host.argtypes = [vp, i32, vp, vp, vp]
@@ -152,6 +156,10 @@ def spin_create(cfg: spin_config) -> int:
 def spin_index_offload(ctx: int, b: int, layer: int, k_ptr: int, v_ptr: int, n_tokens: int, src_is_host: bool,
                        stream: int = 0):
     _check(load().spin_index_offload(ctx, b, layer, k_ptr, v_ptr, n_tokens, 1 if src_is_host else 0, stream), ctx)
+
+
+def spin_append_kv(ctx: int, layer: int, k_ptr: int, v_ptr: int, stream: int = 0):
+    _check(load().spin_append_kv(ctx, layer, k_ptr, v_ptr, stream), ctx)
 
 
 def spin_decode_step(ctx: int, layer: int, q_ptr: int, out_ptr: int, stream: int = 0):

@@ -21,18 +21,30 @@ class SpinContext:
     """Owns one library context: configuration, offload, decode steps, stats, state export."""
 
     def __init__(self, batch: int, layers: int, q_heads: int, kv_heads: int, ctx_len: Sequence[int], topk: int,
-                 buf_mult: int, device: int = 0, seg_pool_segments: int = 0, flags: int = 0):
+                 buf_mult: int, device: int = 0, seg_pool_segments: int = 0, flags: int = 0,
+                 append_tokens: int = 0):
         self.B, self.L, self.Hq, self.Hkv = batch, layers, q_heads, kv_heads
         self.G = q_heads // kv_heads
         self.ctx_len = [int(x) for x in ctx_len]
         self.k, self.buf_mult = topk, buf_mult
         self.cap = topk * buf_mult
-        self.P = [(n + B.PART_TOKENS - 1) // B.PART_TOKENS for n in self.ctx_len]
-        self.P_max = max(self.P) if self.P else 0
+        self.append_tokens = int(append_tokens)
+        self.tail_mode = self.append_tokens > 0
+        PT = B.PART_TOKENS
+        if self.tail_mode:
+            # complete partitions per (layer, request); the rest of the context is the tail
+            self.P = [n // PT for n in self.ctx_len]
+            self.P_cap = [(n + self.append_tokens + PT - 1) // PT for n in self.ctx_len]
+        else:
+            self.P = [(n + PT - 1) // PT for n in self.ctx_len]
+            self.P_cap = list(self.P)
+        self.P_lb = [list(self.P) for _ in range(layers)]
+        self.tail_lb = [[(n % PT) if self.tail_mode else 0 for n in self.ctx_len] for _ in range(layers)]
+        self.P_max = max(self.P_cap) if self.P_cap else 0
         self.device = device
         self._ctx_arr = (ctypes.c_int64 * batch)(*self.ctx_len)
         cfg = B.spin_config(batch, layers, q_heads, kv_heads, B.HEAD_DIM, B.PART_TOKENS, topk, buf_mult,
-                            self._ctx_arr, 0, seg_pool_segments, device, flags)
+                            self._ctx_arr, 0, seg_pool_segments, device, flags, self.append_tokens)
         self.h = B.spin_create(cfg)
 
     @classmethod
@@ -67,6 +79,16 @@ class SpinContext:
         """k_dev, v_dev: contiguous CUDA tensors [Hkv][ctx_len[b]][128] of bf16 or int16 bits."""
         n = self.ctx_len[b]
         B.spin_index_offload(self.h, b, layer, k_dev.data_ptr(), v_dev.data_ptr(), n, False, stream)
+
+    # ---- KV append (tail mode) ----
+    def append_kv(self, layer: int, k_dev, v_dev, stream: int = 0):
+        """One new token per request: k_dev, v_dev CUDA bf16/int16 [B][Hkv][128]."""
+        B.spin_append_kv(self.h, layer, k_dev.data_ptr(), v_dev.data_ptr(), stream)
+        for b in range(self.B):
+            self.tail_lb[layer][b] += 1
+            if self.tail_lb[layer][b] == B.PART_TOKENS:
+                self.tail_lb[layer][b] = 0
+                self.P_lb[layer][b] += 1
 
     # ---- decode ----
     def decode_step(self, layer: int, q_dev, out_dev, stream: int = 0):
@@ -103,12 +125,17 @@ class SpinContext:
         B.spin_debug_export(self.h, layer, v)
         return out
 
+    def read_tail(self, layer: int, b: int, h: int) -> np.ndarray:
+        """The unit's tail page (tail mode): [2][64][128] bf16 bits."""
+        return self.read_page(layer, b, h, self.cap)
+
     def read_page(self, layer: int, b: int, h: int, slot: int) -> np.ndarray:
         dst = np.empty((2, B.PART_TOKENS, B.HEAD_DIM), np.uint16)
         B.spin_debug_read_page(self.h, layer, b, h, slot, _ptr(dst))
         return dst
 
     def summaries(self, layer: int, b: int, h: int) -> np.ndarray:
-        dst = np.empty((max(self.P[b], 1), B.HEAD_DIM), np.float32)
+        P = self.P_lb[layer][b]
+        dst = np.empty((max(P, 1), B.HEAD_DIM), np.float32)
         B.spin_debug_summaries(self.h, layer, b, h, _ptr(dst))
-        return dst[:self.P[b]]
+        return dst[:P]

@@ -224,16 +224,17 @@ __device__ __forceinline__ uint32_t swz(int r, int cd) {
 // ---------------------------------------------------------------------------
 __device__ void combine_unit(const LayerArgs& a, int ul, int w, int lane) {
   const int b = ul / a.Hkv, h = ul - b * a.Hkv;
-  const int keff = a.keff[ul], nh = a.n_hit[ul];
+  const int has_tail = (a.tail_n != nullptr && a.tail_n[b] > 0) ? 1 : 0;
+  const int keff = a.keff[ul] + has_tail, nh = a.n_hit[ul];  // attended pages; resident ones (tail included)
   const int nc = (nh + a.ppt - 1) / a.ppt;
   const int U = a.B * a.Hkv;
   const int n = nc + (keff - nh);
   for (int g = w; g < a.G; g += kCWarps) {
     float4* out = reinterpret_cast<float4*>(a.out + ((int64_t)b * a.Hq + (int64_t)h * a.G + g) * kD);
-    // partial slots: hit tasks ul * n_chunks + c (c < nc), retrieved pages U * n_chunks + ul * k + j (nh <= j < keff)
+    // partial slots: hit tasks ul * n_chunks + c (c < nc), retrieved pages U * n_chunks + ul * ka + j (nh <= j < keff)
     auto part_ptr = [&](int i) -> const float* {
       const int64_t slot =
-          i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.k + nh + (i - nc);
+          i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.ka + nh + (i - nc);
       return a.partials + (slot * a.G + g) * kPartialStride;
     };
     float M = -INFINITY;
@@ -343,7 +344,8 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
       if (!mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) return false;
       int slot = a.att_slot[att];
-      if (slot < 0 || slot >= a.cap) {  // never expected: stage slot 0 instead and report
+      const bool tail = a.tail_n != nullptr && slot == a.cap;  // the unit's tail page
+      if (!tail && (slot < 0 || slot >= a.cap)) {  // never expected: stage slot 0 instead and report
         atomicOr(a.err, kErrIndex);
         slot = 0;
       }
@@ -355,7 +357,8 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       sm.meta[st] = m;
       const uint32_t fb = smem_u32(&sm.full[st]);
       mbar_arrive_expect_tx(fb, kPageBytes + (first ? qbytes : 0u));
-      const int y = (int)(((a.unit_base + ul) * a.cap + slot) * 128);
+      const int y = tail ? (int)((a.pool_slots + a.unit_base + ul) * 128)
+                         : (int)(((a.unit_base + ul) * a.cap + slot) * 128);
       const uint32_t dst = smem_u32(sm.ring + (size_t)st * kStageBytes);
       tma_load_2d(dst, &tmap, fb, 0, y);
       tma_load_2d(dst + 8192, &tmap, fb, 64, y);
@@ -378,7 +381,7 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       const int ul = task / a.n_chunks, c = task - ul * a.n_chunks;
       const int nh = a.n_hit[ul];
       const int j0 = c * a.ppt, j1 = min(nh, j0 + a.ppt);
-      for (int j = j0; j < j1 && ok; ++j) ok = issue(ul, ul * a.k + j, task, j == j0);
+      for (int j = j0; j < j1 && ok; ++j) ok = issue(ul, ul * a.ka + j, task, j == j0);
     }
     // 2) retrieved pages, in miss-list order, each once its copy is published
     while (ok) {
@@ -396,11 +399,11 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       if (!ready) { ok = false; break; }
       asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what the generic stores wrote
       int att = a.miss_att[m];
-      if (att < 0 || att >= U * a.k) {  // never expected
+      if (att < 0 || att >= U * a.ka) {  // never expected
         atomicOr(a.err, kErrIndex);
         att = 0;
       }
-      const int ul = att / a.k;
+      const int ul = att / a.ka;
       ok = issue(ul, att, U * a.n_chunks + att, true);
     }
     if (ok) {

@@ -58,7 +58,82 @@ summarize_offload_kernel(const uint16_t* __restrict__ k, const uint16_t* __restr
   }
 }
 
+// KV append, one CTA per request of the layer. The new token of every KV head goes
+// into row tail_n[b] of the unit's tail page (HBM, after the page pool). When the
+// tail holds 64 tokens it becomes partition P = P_b[b]: its fp32 mean key (same
+// arithmetic as summarize_offload_kernel) goes to the summaries, the page to the
+// pinned host store, the tail page is cleared and the request's counts advance.
+constexpr int kAppendThreads = 256;
+
+__global__ void __launch_bounds__(kAppendThreads)
+append_kernel(LayerArgs a, const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new,
+              int32_t* P_b, int32_t* ntok_b, int32_t* tail_n, float* __restrict__ summ, uint16_t* host_store) {
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int tn = tail_n[b];
+  const int P = P_b[b];
+  const bool full = tn + 1 == kPart;
+  if (tn < 0 || tn >= kPart || (full && (P < 0 || P >= a.pstride_b[b]))) {  // the host never lets this happen
+    if (tid == 0) atomicOr(a.err, kErrIndex);
+    return;
+  }
+  const int64_t u0 = a.pool_slots + a.unit_base + (int64_t)b * a.Hkv;  // pool page of head 0's tail
+  constexpr int kRowVec = kD / 8;                                       // 16-byte vectors per row
+  for (int i = tid; i < a.Hkv * 2 * kRowVec; i += kAppendThreads) {
+    const int h = i / (2 * kRowVec), half = (i / kRowVec) & 1, c = i % kRowVec;
+    const uint4* src = reinterpret_cast<const uint4*>((half ? v_new : k_new) + ((int64_t)b * a.Hkv + h) * kD);
+    uint4* dst = reinterpret_cast<uint4*>(a.pool + (u0 + h) * kPageElems + half * kPart * kD + (int64_t)tn * kD);
+    dst[c] = src[c];
+  }
+  if (!full) {
+    if (tid == 0) tail_n[b] = tn + 1;
+    return;
+  }
+  __syncthreads();  // the new rows are visible to the whole CTA
+  for (int i = tid; i < a.Hkv * kD; i += kAppendThreads) {
+    const int h = i / kD, d = i % kD;
+    const uint16_t* K = a.pool + (u0 + h) * kPageElems;
+    float s = 0.f;
+    for (int r = 0; r < kPart; ++r) s += bf16_bits_to_float(K[r * kD + d]);
+    summ[host_page_index(a, b, h, P) * kD + d] = s / (float)kPart;
+  }
+  constexpr int kPageVec = kPageElems / 8;
+  for (int i = tid; i < a.Hkv * kPageVec; i += kAppendThreads) {
+    const int h = i / kPageVec, c = i % kPageVec;
+    const uint4* src = reinterpret_cast<const uint4*>(a.pool + (u0 + h) * kPageElems);
+    reinterpret_cast<uint4*>(host_store + host_page_index(a, b, h, P) * kPageElems)[c] = src[c];
+  }
+  __syncthreads();  // every read of the tail pages is done
+  for (int i = tid; i < a.Hkv * kPageVec; i += kAppendThreads)
+    reinterpret_cast<uint4*>(a.pool + (u0 + i / kPageVec) * kPageElems)[i % kPageVec] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) {
+    P_b[b] = P + 1;
+    ntok_b[b] = (P + 1) * kPart;
+    tail_n[b] = 0;
+    atomicAdd(&a.stats[kStatFlushes], 1ull);
+  }
+}
+
+__global__ void set_request_kernel(int32_t* P_b, int32_t* ntok_b, int32_t* tail_n, int32_t P, int32_t ntok,
+                                   int32_t tail) {
+  *P_b = P;
+  *ntok_b = ntok;
+  if (tail_n) *tail_n = tail;
+}
+
 }  // namespace
+
+cudaError_t launch_append(const LayerArgs& a, const uint16_t* k_new, const uint16_t* v_new, int32_t* P_b,
+                          int32_t* ntok_b, int32_t* tail_n, cudaStream_t st) {
+  append_kernel<<<a.B, kAppendThreads, 0, st>>>(a, k_new, v_new, P_b, ntok_b, tail_n, const_cast<float*>(a.summ),
+                                               const_cast<uint16_t*>(a.host_store));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_set_request(int32_t* P_b, int32_t* ntok_b, int32_t* tail_n, int32_t P, int32_t ntok,
+                               int32_t tail, cudaStream_t st) {
+  set_request_kernel<<<1, 1, 0, st>>>(P_b, ntok_b, tail_n, P, ntok, tail);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_summarize_offload(const uint16_t* k, const uint16_t* v, int64_t head_stride, int32_t kv_heads,
                                      int64_t tok0, int64_t ntok_chunk, int64_t ntok_total, float* summ_unit0,

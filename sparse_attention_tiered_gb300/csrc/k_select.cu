@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(LayerArgs a) {
   __shared__ __align__(16) float qs[kD];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the summary loads do not depend on the query: issue them first
-  const float4* su = reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, P, 0) * kD);
+  const float4* su = reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, 0) * kD);
   const int p0 = p_base + warp * kScorePerWarp;
   float4 sv[kScorePerWarp];
 #pragma unroll
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   if constexpr (kFusedScore) {
     __shared__ __align__(16) float s_qs[kD];
     constexpr int kPer = 8;  // partitions in flight per warp
-    const float4* su = reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, P, 0) * kD);
+    const float4* su = reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, 0) * kD);
     float4 sv[kPer];
     int p0 = warp * kPer;
 #pragma unroll
@@ -452,6 +452,8 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   group_sync<NT>();
   const int hits = s_cnt_hits;
   const int misses = keff - hits;
+  // tail mode: the request's tail page is attended after the hits, before the misses
+  const int has_tail = (a.tail_n != nullptr && a.tail_n[b] > 0) ? 1 : 0;
   const int resident = s_cnt_res;
   const int demand = misses - (cap - resident);
 
@@ -582,9 +584,9 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       atomicOr(a.err, kErrIndex);
       continue;
     }
-    a.miss_src[idx] = host_page_index(a, b, h, P, p);
+    a.miss_src[idx] = host_page_index(a, b, h, p);
     a.miss_dst[idx] = unit * cap + s;
-    a.miss_att[idx] = ul * k + hits + rank;  // misses follow the hits in attention order
+    a.miss_att[idx] = ul * a.ka + hits + has_tail + rank;  // misses follow the hits and the tail
   }
   group_sync<NT>();
 
@@ -600,19 +602,24 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
     a.sel_slot[(int64_t)ul * k + j] = v ? sm.sslot[j] : -1;
     a.sel_hit[(int64_t)ul * k + j] = v ? (uint8_t)(sm.hit[j] > 0) : 0;
   }
-  // attention order: hits (ascending partition) first, then this step's misses
+  // attention order: hits (ascending partition) first, then the tail page (slot == cap),
+  // then this step's misses
   {
     const int ntok = a.ntok_b[b];
     for (int j = tid; j < keff; j += NT) {
       const int p = sm.sel[j];
       const bool hit = sm.hit[j] > 0;
-      const int pos = hit ? j - sm.mrank[j] : hits + sm.mrank[j];
-      a.att_slot[(int64_t)ul * k + pos] = sm.sslot[j];
-      a.att_valid[(int64_t)ul * k + pos] = (p == P - 1) ? ntok - p * kPart : kPart;
+      const int pos = hit ? j - sm.mrank[j] : hits + has_tail + sm.mrank[j];
+      a.att_slot[(int64_t)ul * a.ka + pos] = sm.sslot[j];
+      a.att_valid[(int64_t)ul * a.ka + pos] = (p == P - 1) ? ntok - p * kPart : kPart;
+    }
+    if (has_tail && tid == 0) {
+      a.att_slot[(int64_t)ul * a.ka + hits] = cap;
+      a.att_valid[(int64_t)ul * a.ka + hits] = a.tail_n[b];
     }
   }
   if (tid == 0) {
-    a.n_hit[ul] = hits;
+    a.n_hit[ul] = hits + has_tail;
     a.keff[ul] = keff;
     int32_t* info = a.unit_info + (int64_t)ul * 8;
     info[0] = hits;

@@ -14,6 +14,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <sys/mman.h>
+#include <unistd.h>
+
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
@@ -88,16 +91,25 @@ struct spin_ctx {
   int select_group = 0;  // SPIN_SELECT_GROUP: threads of the top-k/manager group (0 = by unit size)
   int retr_warps = 2;  // SPIN_RETRIEVE_WARPS (1..8): retriever warps per attend CTA
   std::vector<int64_t> ctx_len;
-  std::vector<int32_t> P_b, ntok_b;
+  std::vector<int32_t> P_b, ntok_b;  // fixed mode: partitions and tokens of each request
+  std::vector<int32_t> pstride_b;    // host-store pages per KV head of each request (its partition capacity)
   std::vector<int64_t> poff_b;
+  // tail mode (append_tokens > 0): per-(layer, request) complete partitions and tail tokens,
+  // mirrored on the host (every append adds exactly one token, so the host knows them)
+  bool tail_mode = false;
+  int64_t append_tokens = 0, appended = 0;
+  int ka = 0;  // attention entries per unit
+  std::vector<int32_t> P_lb, tail_lb;
   int64_t pages_per_layer = 0, units = 0, S = 0;
   // memory
   std::vector<void*> dev_allocs;
   uint16_t* h_store = nullptr;  // pinned host page store
+  size_t h_store_map_len = 0;   // > 0: h_store is a registered anonymous mapping of this length
   uint16_t* d_store = nullptr;  // its device-usable address
   uint16_t* d_pool = nullptr;
   float* d_summ = nullptr;
-  int32_t *d_P_b = nullptr, *d_ntok_b = nullptr;
+  int32_t *d_P_lb = nullptr, *d_ntok_lb = nullptr, *d_tail_lb = nullptr;  // [L][B]
+  int32_t* d_pstride_b = nullptr;
   int64_t* d_poff_b = nullptr;
   int32_t *d_dir = nullptr, *d_seg = nullptr, *d_seg_live = nullptr;
   int32_t* h_seg = nullptr;  // tier split: the segment entries in pinned host memory (d_seg maps it)
@@ -159,8 +171,16 @@ cudaError_t dalloc(spin_ctx* c, T** p, size_t count) {
 void free_all(spin_ctx* c) {
   for (void* p : c->dev_allocs) cudaFree(p);
   c->dev_allocs.clear();
-  if (c->h_store) cudaFreeHost(c->h_store);
+  if (c->h_store) {
+    if (c->h_store_map_len) {
+      cudaHostUnregister(c->h_store);
+      munmap(c->h_store, c->h_store_map_len);
+    } else {
+      cudaFreeHost(c->h_store);
+    }
+  }
   c->h_store = nullptr;
+  c->h_store_map_len = 0;
   if (c->h_seg) cudaFreeHost(c->h_seg);
   c->h_seg = nullptr;
   for (auto& t : c->pending)
@@ -168,6 +188,42 @@ void free_all(spin_ctx* c) {
   c->pending.clear();
   for (auto e : c->spare_events) cudaEventDestroy(e);
   c->spare_events.clear();
+}
+
+// Size of a transparent huge page (PMD size); 2 MiB when the kernel does not say.
+size_t thp_bytes() {
+  size_t v = 0;
+  if (FILE* f = fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+    unsigned long long x = 0;
+    if (fscanf(f, "%llu", &x) == 1) v = (size_t)x;
+    fclose(f);
+  }
+  return (v >= 4096 && (v & (v - 1)) == 0 && v <= ((size_t)1 << 30)) ? v : ((size_t)2 << 20);
+}
+
+// Pinned, device-mapped host memory from an anonymous mapping aligned to the huge-page
+// size and advised to use transparent huge pages, then registered with CUDA (large host
+// pages mean few address translations for the GPU's random page reads). nullptr when
+// any step fails.
+void* alloc_host_hugepages(size_t bytes, size_t* map_len) {
+  const size_t hp = thp_bytes();
+  const size_t len = (bytes + hp - 1) / hp * hp;
+  void* m = mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (m == MAP_FAILED) return nullptr;
+  const uintptr_t base = reinterpret_cast<uintptr_t>(m);
+  const uintptr_t aligned = (base + hp - 1) / hp * hp;
+  if (aligned > base) munmap(m, aligned - base);                       // leading remainder
+  const size_t tail = (base + len + hp) - (aligned + len);
+  if (tail) munmap(reinterpret_cast<void*>(aligned + len), tail);      // trailing remainder
+  void* p = reinterpret_cast<void*>(aligned);
+  (void)madvise(p, len, MADV_HUGEPAGE);  // advisory: no effect where huge pages are off
+  if (cudaHostRegister(p, len, cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess) {
+    cudaGetLastError();
+    munmap(p, len);
+    return nullptr;
+  }
+  *map_len = len;
+  return p;
 }
 
 int check_device_error(spin_ctx* c) {
@@ -210,7 +266,7 @@ int encode_tensor_map(spin_ctx* c) {
   cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
   if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
     return fail(c, SPIN_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const uint64_t slots = (uint64_t)c->units * (uint64_t)c->cap;
+  const uint64_t slots = (uint64_t)c->units * (uint64_t)c->cap + (c->tail_mode ? (uint64_t)c->units : 0u);
   cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)(slots * 128)};
   cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
   cuuint32_t box[2] = {64, 64};
@@ -248,15 +304,16 @@ int validate(const spin_config* cfg) {
   if (cfg->buf_mult < 1 || (int64_t)cfg->buf_mult * cfg->topk > 8192)
     return fail(nullptr, SPIN_ERR_INVALID, "buf_mult must be >= 1 with buf_mult * topk <= 8192");
   if (!cfg->ctx_len) return fail(nullptr, SPIN_ERR_INVALID, "ctx_len is NULL");
+  if (cfg->append_tokens < 0) return fail(nullptr, SPIN_ERR_INVALID, "append_tokens must be >= 0");
   for (int b = 0; b < cfg->batch; ++b) {
-    if (cfg->ctx_len[b] < 0 || cfg->ctx_len[b] > (int64_t)32768 * kPart)
-      return fail(nullptr, SPIN_ERR_INVALID, "ctx_len[%d] = %lld outside [0, %d]", b, (long long)cfg->ctx_len[b],
-                  32768 * kPart);
+    if (cfg->ctx_len[b] < 0 || cfg->ctx_len[b] + cfg->append_tokens > (int64_t)32768 * kPart)
+      return fail(nullptr, SPIN_ERR_INVALID, "ctx_len[%d] + append_tokens = %lld outside [0, %d]", b,
+                  (long long)(cfg->ctx_len[b] + cfg->append_tokens), 32768 * kPart);
   }
   if (cfg->seg_pool_segments < 0) return fail(nullptr, SPIN_ERR_INVALID, "seg_pool_segments must be >= 0");
   const int64_t units = (int64_t)cfg->batch * cfg->layers * cfg->kv_heads;
-  if (units * cfg->buf_mult * cfg->topk >= (int64_t)1 << 24)
-    return fail(nullptr, SPIN_ERR_INVALID, "units * capacity must stay below 2^24 pages");
+  if (units * ((int64_t)cfg->buf_mult * cfg->topk + 1) >= (int64_t)1 << 24)
+    return fail(nullptr, SPIN_ERR_INVALID, "units * (capacity + 1) must stay below 2^24 pages");
   return SPIN_OK;
 }
 
@@ -277,8 +334,11 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.S = (int32_t)c->S;
   a.retr_warps = c->retr_warps;
   a.select_group = c->select_group;
-  a.P_b = c->d_P_b;
-  a.ntok_b = c->d_ntok_b;
+  a.ka = c->ka;
+  a.P_b = c->d_P_lb + (int64_t)l * c->B;
+  a.ntok_b = c->d_ntok_lb + (int64_t)l * c->B;
+  a.tail_n = c->tail_mode ? c->d_tail_lb + (int64_t)l * c->B : nullptr;
+  a.pstride_b = c->d_pstride_b;
   a.poff_b = c->d_poff_b;
   a.layer_page_base = (int64_t)l * c->pages_per_layer;
   a.unit_base = (int64_t)l * c->B * c->Hkv;
@@ -324,8 +384,12 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   c->k = cfg->topk;
   c->cap = cfg->buf_mult * cfg->topk;
   c->ctx_len.assign(cfg->ctx_len, cfg->ctx_len + c->B);
+  c->append_tokens = cfg->append_tokens;
+  c->tail_mode = cfg->append_tokens > 0;
+  c->ka = c->k + (c->tail_mode ? 1 : 0);
   c->P_b.resize(c->B);
   c->ntok_b.resize(c->B);
+  c->pstride_b.resize(c->B);
   c->poff_b.resize(c->B);
   int64_t poff = 0;
   c->P_max = 0;
@@ -333,12 +397,18 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   for (int b = 0; b < c->B; ++b) {
     c->ntok_b[b] = (int32_t)c->ctx_len[b];
     c->P_b[b] = (int32_t)((c->ctx_len[b] + kPart - 1) / kPart);
+    // tail mode: room for every partition the request can reach
+    c->pstride_b[b] = c->tail_mode ? (int32_t)((c->ctx_len[b] + c->append_tokens + kPart - 1) / kPart) : c->P_b[b];
     c->poff_b[b] = poff;
-    poff += c->P_b[b];
-    c->P_max = std::max(c->P_max, c->P_b[b]);
-    const int64_t Du = (c->P_b[b] + kSeg - 1) / kSeg;
+    poff += c->pstride_b[b];
+    c->P_max = std::max(c->P_max, c->pstride_b[b]);
+    const int64_t Du = (c->pstride_b[b] + kSeg - 1) / kSeg;
     auto_S += std::min<int64_t>(Du, c->cap) * c->Hkv * c->L;
   }
+  c->P_lb.assign((size_t)c->L * c->B, 0);
+  c->tail_lb.assign((size_t)c->L * c->B, 0);
+  for (int l = 0; l < c->L && !c->tail_mode; ++l)
+    for (int b = 0; b < c->B; ++b) c->P_lb[(size_t)l * c->B + b] = c->P_b[b];
   c->D = std::max(1, (c->P_max + kSeg - 1) / kSeg);
   c->pages_per_layer = poff * c->Hkv;
   c->units = (int64_t)c->B * c->L * c->Hkv;
@@ -361,11 +431,15 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   c->bytes_store = total_pages * kPageBytes;
   if (total_pages > 0) {
     void* h = nullptr;
-    e = cudaHostAlloc(&h, (size_t)c->bytes_store, cudaHostAllocMapped | cudaHostAllocPortable);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      return fail(nullptr, SPIN_ERR_OOM, "pinned host allocation of %lld bytes failed: %s",
-                  (long long)c->bytes_store, cudaGetErrorString(e));
+    if (c->flags & SPIN_FLAG_HOST_HUGEPAGES) h = alloc_host_hugepages((size_t)c->bytes_store, &c->h_store_map_len);
+    if (!h) {
+      c->h_store_map_len = 0;
+      e = cudaHostAlloc(&h, (size_t)c->bytes_store, cudaHostAllocMapped | cudaHostAllocPortable);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(nullptr, SPIN_ERR_OOM, "pinned host allocation of %lld bytes failed: %s",
+                    (long long)c->bytes_store, cudaGetErrorString(e));
+      }
     }
     c->h_store = static_cast<uint16_t*>(h);
     void* d = nullptr;
@@ -376,14 +450,17 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
 
   // HBM
   const int64_t slots = c->units * c->cap;
-  c->bytes_pool = slots * kPageBytes;
+  const int64_t tail_pages = c->tail_mode ? c->units : 0;  // one tail page per unit, after the pool slots
+  c->bytes_pool = (slots + tail_pages) * kPageBytes;
   c->bytes_summ = total_pages * kD * 4;
 #define ALLOC(ptr, n, what) \
   if ((e = dalloc(c, &(ptr), (size_t)(n))) != cudaSuccess) return cuda_fail(nullptr, e, what)
-  ALLOC(c->d_pool, slots * kPageElems, "allocating the HBM page pool");
+  ALLOC(c->d_pool, (slots + tail_pages) * kPageElems, "allocating the HBM page pool");
   ALLOC(c->d_summ, total_pages * kD, "allocating the summaries");
-  ALLOC(c->d_P_b, c->B, "allocating request tables");
-  ALLOC(c->d_ntok_b, c->B, "allocating request tables");
+  ALLOC(c->d_P_lb, (int64_t)c->L * c->B, "allocating request tables");
+  ALLOC(c->d_ntok_lb, (int64_t)c->L * c->B, "allocating request tables");
+  ALLOC(c->d_tail_lb, (int64_t)c->L * c->B, "allocating request tables");
+  ALLOC(c->d_pstride_b, c->B, "allocating request tables");
   ALLOC(c->d_poff_b, c->B, "allocating request tables");
   ALLOC(c->d_dir, c->units * c->D, "allocating the directory");
   if (c->flags & SPIN_FLAG_TIER_SPLIT) {
@@ -414,9 +491,22 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   c->bytes_meta = (c->units * c->D + (c->h_seg ? 0 : c->S * kSeg) + c->S + nwords + 2 * slots) * 4;
   c->bytes_flat = (c->units * (int64_t)c->P_max + 2 * slots) * 4;
 
-  SPIN_CUDA(nullptr, cudaMemcpy(c->d_P_b, c->P_b.data(), 4 * c->B, cudaMemcpyHostToDevice), "uploading tables");
-  SPIN_CUDA(nullptr, cudaMemcpy(c->d_ntok_b, c->ntok_b.data(), 4 * c->B, cudaMemcpyHostToDevice), "uploading tables");
+  {
+    // fixed mode: every layer holds the request's partitions; tail mode: nothing until offload
+    std::vector<int32_t> ntok_lb((size_t)c->L * c->B, 0);
+    for (int l = 0; l < c->L && !c->tail_mode; ++l)
+      for (int b = 0; b < c->B; ++b) ntok_lb[(size_t)l * c->B + b] = c->ntok_b[b];
+    const size_t n = (size_t)c->L * c->B * 4;
+    SPIN_CUDA(nullptr, cudaMemcpy(c->d_P_lb, c->P_lb.data(), n, cudaMemcpyHostToDevice), "uploading tables");
+    SPIN_CUDA(nullptr, cudaMemcpy(c->d_ntok_lb, ntok_lb.data(), n, cudaMemcpyHostToDevice), "uploading tables");
+    SPIN_CUDA(nullptr, cudaMemset(c->d_tail_lb, 0, n), "uploading tables");
+  }
+  SPIN_CUDA(nullptr, cudaMemcpy(c->d_pstride_b, c->pstride_b.data(), 4 * c->B, cudaMemcpyHostToDevice),
+            "uploading tables");
   SPIN_CUDA(nullptr, cudaMemcpy(c->d_poff_b, c->poff_b.data(), 8 * c->B, cudaMemcpyHostToDevice), "uploading tables");
+  if (tail_pages)
+    SPIN_CUDA(nullptr, cudaMemset(c->d_pool + slots * kPageElems, 0, (size_t)tail_pages * kPageBytes),
+              "clearing the tail pages");
   SPIN_CUDA(nullptr, cudaMemset(c->d_dir, 0xff, (size_t)c->units * c->D * 4), "initialising the directory");
   if (!c->h_seg)
     SPIN_CUDA(nullptr, cudaMemset(c->d_seg, 0xff, (size_t)c->S * kSeg * 4), "initialising the segment pool");
@@ -442,7 +532,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   // attention work split: pages per task
   const int64_t pages_layer = (int64_t)c->B * c->Hkv * c->k;
   c->ppt = (int)std::max<int64_t>(1, std::min<int64_t>(8, pages_layer / (4 * std::max(1, c->sm_count))));
-  c->n_chunks = (c->k + c->ppt - 1) / c->ppt;
+  c->n_chunks = (c->ka + c->ppt - 1) / c->ppt;
 
   const int64_t Ul = (int64_t)c->B * c->Hkv;
   c->layers.resize(c->L);
@@ -456,13 +546,13 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     ALLOC(lb.unit_info, Ul * 8, "allocating layer scratch");
     ALLOC(lb.miss_src, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.miss_dst, Ul * c->k, "allocating layer scratch");
-    ALLOC(lb.att_slot, Ul * c->k, "allocating layer scratch");
-    ALLOC(lb.att_valid, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.att_slot, Ul * c->ka, "allocating layer scratch");
+    ALLOC(lb.att_valid, Ul * c->ka, "allocating layer scratch");
     ALLOC(lb.n_hit, Ul, "allocating layer scratch");
     ALLOC(lb.miss_att, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.ready, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.counters, kNumCtr, "allocating layer scratch");
-    ALLOC(lb.partials, Ul * (c->n_chunks + c->k) * c->G * kPartialStride, "allocating layer scratch");
+    ALLOC(lb.partials, Ul * (c->n_chunks + c->ka) * c->G * kPartialStride, "allocating layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.n_hit, 0, Ul * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.ready, 0, Ul * c->k * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.counters, 0, kNumCtr * 4), "initialising layer counters");
@@ -575,13 +665,39 @@ int spin_index_offload(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k,
   DeviceGuard g(c->device);
   if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t P = c->P_b[b];
+  const int64_t P = c->pstride_b[b];  // host-store pages per KV head of the request
   const int64_t page0 = (int64_t)layer * c->pages_per_layer + (int64_t)c->Hkv * c->poff_b[b];
   float* summ0 = c->d_summ + page0 * kD;
   uint16_t* host0 = c->d_store + page0 * kPageElems;
-  if (n_tokens > 0) {
+  // Tail mode: only the complete partitions are indexed and offloaded; the remaining
+  // n % 64 tokens go into the units' tail pages in HBM.
+  const int64_t n_part_tok = c->tail_mode ? n_tokens / kPart * kPart : n_tokens;
+  const int64_t rem = n_tokens - n_part_tok;
+  if (c->tail_mode) {
+    const size_t lb = (size_t)layer * c->B + b;
+    const int64_t unit0 = ((int64_t)layer * c->B + b) * c->Hkv;
+    uint16_t* tail0 = c->d_pool + (c->units * c->cap + unit0) * kPageElems;
+    SPIN_CUDA(c, cudaMemsetAsync(tail0, 0, (size_t)c->Hkv * kPageBytes, st), "clearing the tail pages");
+    if (rem > 0) {
+      for (int half = 0; half < 2; ++half)
+        SPIN_CUDA(c,
+                  cudaMemcpy2DAsync(tail0 + half * kPart * kD, kPageBytes, (half ? v : k) + n_part_tok * kD,
+                                    (size_t)n_tokens * kD * 2, (size_t)rem * kD * 2, (size_t)c->Hkv,
+                                    cudaMemcpyDefault, st),
+                  "copying the tail tokens");
+    }
+    const int32_t Pc = (int32_t)(n_part_tok / kPart);
+    SPIN_CUDA(c,
+              launch_set_request(c->d_P_lb + lb, c->d_ntok_lb + lb, c->d_tail_lb + lb, Pc, Pc * kPart, (int32_t)rem,
+                                 st),
+              "setting the request state");
+    c->P_lb[lb] = Pc;
+    c->tail_lb[lb] = (int32_t)rem;
+  }
+  if (n_part_tok > 0) {
     if (!src_is_host) {
-      SPIN_CUDA(c, launch_summarize_offload(k, v, n_tokens, c->Hkv, 0, n_tokens, n_tokens, summ0, host0, P, st),
+      SPIN_CUDA(c,
+                launch_summarize_offload(k, v, n_tokens, c->Hkv, 0, n_part_tok, n_part_tok, summ0, host0, P, st),
                 "launching summarize/offload");
     } else {
       // stage through HBM in chunks of whole partitions
@@ -594,8 +710,8 @@ int spin_index_offload(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k,
           return cuda_fail(c, e, "allocating the offload staging buffer");
         c->stage_tokens = chunk_tok;
       }
-      for (int64_t t0 = 0; t0 < n_tokens; t0 += chunk_tok) {
-        const int64_t nt = std::min(chunk_tok, n_tokens - t0);
+      for (int64_t t0 = 0; t0 < n_part_tok; t0 += chunk_tok) {
+        const int64_t nt = std::min(chunk_tok, n_part_tok - t0);
         SPIN_CUDA(c,
                   cudaMemcpy2DAsync(c->d_stage_k, (size_t)nt * kD * 2, k + t0 * kD, (size_t)n_tokens * kD * 2,
                                     (size_t)nt * kD * 2, (size_t)c->Hkv, cudaMemcpyHostToDevice, st),
@@ -605,13 +721,45 @@ int spin_index_offload(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k,
                                     (size_t)nt * kD * 2, (size_t)c->Hkv, cudaMemcpyHostToDevice, st),
                   "copying V to the staging buffer");
         SPIN_CUDA(c,
-                  launch_summarize_offload(c->d_stage_k, c->d_stage_v, nt, c->Hkv, t0, nt, n_tokens, summ0, host0,
+                  launch_summarize_offload(c->d_stage_k, c->d_stage_v, nt, c->Hkv, t0, nt, n_part_tok, summ0, host0,
                                            P, st),
                   "launching summarize/offload");
       }
     }
   }
   c->offloaded[(size_t)layer * c->B + b] = 1;
+  return SPIN_OK;
+}
+
+int spin_append_kv(spin_ctx* c, int32_t layer, const uint16_t* k_new, const uint16_t* v_new, spin_stream_t stream) {
+  if (!c) return fail(nullptr, SPIN_ERR_INVALID, "ctx is NULL");
+  if (!c->tail_mode) return fail(c, SPIN_ERR_STATE, "spin_append_kv needs a context created with append_tokens > 0");
+  if (!k_new || !v_new) return fail(c, SPIN_ERR_INVALID, "k_new or v_new is NULL");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)
+    return fail(c, SPIN_ERR_INVALID, "k_new and v_new must be 16-byte aligned");
+  int rc = check_layer(c, layer);
+  if (rc) return rc;
+  for (int b = 0; b < c->B; ++b) {
+    const size_t lb = (size_t)layer * c->B + b;
+    const int64_t have = (int64_t)c->P_lb[lb] * kPart + c->tail_lb[lb];
+    if (have + 1 > c->ctx_len[b] + c->append_tokens)
+      return fail(c, SPIN_ERR_CAPACITY, "request %d of layer %d would exceed ctx_len + append_tokens = %lld tokens", b,
+                  layer, (long long)(c->ctx_len[b] + c->append_tokens));
+  }
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  const size_t l0 = (size_t)layer * c->B;
+  SPIN_CUDA(c,
+            launch_append(c->layers[layer].args, k_new, v_new, c->d_P_lb + l0, c->d_ntok_lb + l0, c->d_tail_lb + l0,
+                          static_cast<cudaStream_t>(stream)),
+            "launching append");
+  for (int b = 0; b < c->B; ++b) {
+    if (++c->tail_lb[l0 + b] == kPart) {
+      c->tail_lb[l0 + b] = 0;
+      c->P_lb[l0 + b] += 1;
+    }
+  }
+  c->appended += c->B;
   return SPIN_OK;
 }
 
@@ -689,6 +837,8 @@ int spin_stats(spin_ctx* c, spin_stats_t* out) {
   out->ms_attention = c->ms[3];
   out->ms_combine = c->ms[4];
   out->device_error = c->sticky;
+  out->appended_tokens = c->appended;
+  out->tail_flushes = (int64_t)st[kStatFlushes];
   return rc;
 }
 
@@ -735,14 +885,15 @@ int spin_debug_export(spin_ctx* c, int32_t layer, spin_state_view* v) {
 
 int spin_debug_read_page(spin_ctx* c, int32_t layer, int32_t b, int32_t h, int32_t slot, uint16_t* dst) {
   if (!c || !dst) return fail(c, SPIN_ERR_INVALID, "ctx or dst is NULL");
-  if (layer < 0 || layer >= c->L || b < 0 || b >= c->B || h < 0 || h >= c->Hkv || slot < 0 || slot >= c->cap)
+  const int slot_end = c->cap + (c->tail_mode ? 1 : 0);  // slot == cap: the unit's tail page
+  if (layer < 0 || layer >= c->L || b < 0 || b >= c->B || h < 0 || h >= c->Hkv || slot < 0 || slot >= slot_end)
     return fail(c, SPIN_ERR_INVALID, "page coordinates out of range");
   DeviceGuard g(c->device);
   if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
   int rc = sync_ctx(c);
   const int64_t unit = ((int64_t)layer * c->B + b) * c->Hkv + h;
-  SPIN_CUDA(c, cudaMemcpy(dst, c->d_pool + (unit * c->cap + slot) * kPageElems, kPageBytes, cudaMemcpyDeviceToHost),
-            "copying a page");
+  const int64_t page = slot == c->cap ? c->units * c->cap + unit : unit * c->cap + slot;
+  SPIN_CUDA(c, cudaMemcpy(dst, c->d_pool + page * kPageElems, kPageBytes, cudaMemcpyDeviceToHost), "copying a page");
   return rc;
 }
 
@@ -753,9 +904,11 @@ int spin_debug_summaries(spin_ctx* c, int32_t layer, int32_t b, int32_t h, float
   DeviceGuard g(c->device);
   if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
   int rc = sync_ctx(c);
-  const int64_t page0 = (int64_t)layer * c->pages_per_layer + (int64_t)c->Hkv * c->poff_b[b] + (int64_t)h * c->P_b[b];
-  if (c->P_b[b] > 0)
-    SPIN_CUDA(c, cudaMemcpy(dst, c->d_summ + page0 * kD, (size_t)c->P_b[b] * kD * 4, cudaMemcpyDeviceToHost),
+  const int64_t page0 =
+      (int64_t)layer * c->pages_per_layer + (int64_t)c->Hkv * c->poff_b[b] + (int64_t)h * c->pstride_b[b];
+  const int32_t P = c->P_lb[(size_t)layer * c->B + b];
+  if (P > 0)
+    SPIN_CUDA(c, cudaMemcpy(dst, c->d_summ + page0 * kD, (size_t)P * kD * 4, cudaMemcpyDeviceToHost),
               "copying summaries");
   return rc;
 }

@@ -32,15 +32,18 @@ enum : uint32_t {
 // Per-layer arguments of the decode-step kernels (passed by value).
 struct LayerArgs {
   int32_t layer, B, Hq, Hkv, G, k, cap, D, P_max, n_chunks, ppt, S;
+  int32_t ka;                // attention entries per unit: k, plus one for the tail page in tail mode
   int32_t retr_warps;        // retriever warps active per CTA of the attend kernel
   int32_t select_group;      // 0 = choose by unit size, else 32 or 512 threads for top-k + manager
-  const int32_t* P_b;        // [B] partitions of request b
-  const int32_t* ntok_b;     // [B] tokens of request b
-  const int64_t* poff_b;     // [B] sum of P over earlier requests
+  const int32_t* P_b;        // [B] selectable partitions of request b in this layer (tail mode: complete ones)
+  const int32_t* ntok_b;     // [B] tokens held by those partitions
+  const int32_t* tail_n;     // [B] tokens in the request's tail page (tail mode), else nullptr
+  const int32_t* pstride_b;  // [B] host-store pages per KV head of request b (its partition capacity)
+  const int64_t* poff_b;     // [B] sum of pstride over earlier requests
   int64_t layer_page_base;   // first page of this layer in the host store / summaries
   int64_t unit_base;         // first global unit of this layer = layer * B * Hkv
   int64_t host_pages;        // pages in the host store (all layers)
-  int64_t pool_slots;        // pages in the HBM pool (all units)
+  int64_t pool_slots;        // pages in the HBM pool (all units); the tail page of unit u follows at pool_slots + u
   const float* summ;         // [pages][128] fp32 summaries (all layers)
   const uint16_t* host_store;// mapped pinned pages [pages][16384] (device-usable address)
   uint16_t* pool;            // HBM pages [units * cap][16384]
@@ -58,22 +61,23 @@ struct LayerArgs {
   int32_t* unit_info;        // [U_l][8]
   int64_t* miss_src;         // [U_l * k] host page index of each miss (miss list, append order)
   int64_t* miss_dst;         // [U_l * k] pool slot index of each miss
-  int32_t* miss_att;         // [U_l * k] ul * k + attention position of each miss
+  int32_t* miss_att;         // [U_l * k] ul * ka + attention position of each miss
   int32_t* ready;            // [U_l * k] per miss-list entry: step tag once its page is in HBM
-  int32_t* att_slot;         // [U_l][k] slots in attention order: hits first, then misses
-  int32_t* att_valid;        // [U_l][k] valid tokens of those pages
-  int32_t* n_hit;            // [U_l] hits of the step (pages [0, n_hit) of att_slot)
+  int32_t* att_slot;         // [U_l][ka] slots in attention order: hits, the tail (slot == cap), then misses
+  int32_t* att_valid;        // [U_l][ka] valid tokens of those pages
+  int32_t* n_hit;            // [U_l] resident pages of the step, tail included (pages [0, n_hit) of att_slot)
   int32_t* counters;         // [4]: see kCtr*
-  float* partials;           // hits [U_l][n_chunks][G][132], then misses [U_l][k][G][132]
+  float* partials;           // hits [U_l][n_chunks][G][132], then misses [U_l][ka][G][132]
   unsigned long long* stats; // [8] device counters
   uint32_t* err;             // device error word
   const uint16_t* q;         // [B][Hq][128] bf16 (device)
   float* out;                // [B][Hq][128] fp32 (device)
 };
 
-// Host page index of partition p of (b, h) in the layer described by a.
-__host__ __device__ inline int64_t host_page_index(const LayerArgs& a, int b, int h, int64_t P, int64_t p) {
-  return a.layer_page_base + (int64_t)a.Hkv * a.poff_b[b] + (int64_t)h * P + p;
+// Host page index of partition p of (b, h) in the layer described by a (also the
+// row of its summary).
+__device__ inline int64_t host_page_index(const LayerArgs& a, int b, int h, int64_t p) {
+  return a.layer_page_base + (int64_t)a.Hkv * a.poff_b[b] + (int64_t)h * a.pstride_b[b] + p;
 }
 
 // Per-layer device counters.
@@ -84,7 +88,9 @@ enum : int {
 };
 
 // Device stats slots.
-enum : int { kStatHits = 0, kStatMisses = 1, kStatEvictions = 2, kStatLruRounds = 3, kStatSelected = 4 };
+enum : int {
+  kStatHits = 0, kStatMisses = 1, kStatEvictions = 2, kStatLruRounds = 3, kStatSelected = 4, kStatFlushes = 5
+};
 
 // ---------------------------------------------------------------------------
 // Launchers (defined in the kernel translation units).
@@ -93,6 +99,12 @@ cudaError_t launch_summarize_offload(const uint16_t* k, const uint16_t* v, int64
                                      int64_t tok0, int64_t ntok_chunk, int64_t ntok_total, float* summ_unit0,
                                      uint16_t* host_unit0, int64_t unit_pages, cudaStream_t st);
 cudaError_t launch_score(const LayerArgs& a, cudaStream_t st);
+// KV append of one token per request of the layer (tail mode).
+cudaError_t launch_append(const LayerArgs& a, const uint16_t* k_new, const uint16_t* v_new, int32_t* P_b,
+                          int32_t* ntok_b, int32_t* tail_n, cudaStream_t st);
+// Sets the request's layer state (partitions, their tokens, tail tokens) on the device.
+cudaError_t launch_set_request(int32_t* P_b, int32_t* ntok_b, int32_t* tail_n, int32_t P, int32_t ntok,
+                               int32_t tail, cudaStream_t st);
 cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st);
 // Retrieve + attention in one cooperative persistent launch (one CTA per SM).
 cudaError_t launch_attend_retrieve(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st);

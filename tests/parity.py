@@ -21,6 +21,12 @@ Validity invariants checked for every unit of every exported layer: slots hold
 distinct partitions, resolve(p) = s iff slot s holds p, live segments equal the
 occupied 64-partition ranges, the selection is ascending and resident in the
 slots it names, those slots carry the current step.
+
+KV append (tail mode, ``append > 0``): each step first appends the request's next
+token (drawn by the generator beyond the initial context) on both sides, then
+decodes. The oracle's TailUnit supplies the expected partitions and tail; the
+compared units' tail pages must equal the oracle's tail byte for byte and the
+summaries of partitions made from full tails must match the oracle's means.
 """
 from __future__ import annotations
 
@@ -112,25 +118,33 @@ class Lockstep:
 
     def __init__(self, w: W.Workload, units: Optional[List[Tuple[int, int, int]]] = None, device: int = 0,
                  flags: int = 0, seg_pool_segments: int = 0, offload_from_device: bool = False,
-                 gen_threads: int = 0):
+                 gen_threads: int = 0, append: int = 0):
         import torch
         from sparse_attention_tiered_gb300 import SpinContext
         self.torch = torch
         self.w = w
+        self.append = append
         self.dev = torch.device(f"cuda:{device}")
         self.units = units if units is not None else [(l, b, h) for l in range(w.L) for b in range(w.B)
                                                       for h in range(w.Hkv)]
-        self.ctx = SpinContext.for_workload(w, device=device, flags=flags, seg_pool_segments=seg_pool_segments)
+        self.ctx = SpinContext.for_workload(w, device=device, flags=flags, seg_pool_segments=seg_pool_segments,
+                                            append_tokens=append)
         self.oracle: Dict[Tuple[int, int, int], O.Unit] = {}
         self.fresh_cap = max(w.topk, 1)
+        # tail mode: the generator draws each request's tokens past the initial context too;
+        # those are the appended tokens, [L][B] -> [Hkv][append][128]
+        wf = w.with_(ctx_len=[n + append for n in w.ctx_len]) if append else w
+        self.new_kv = {}
         want = {}
         for (l, b, h) in self.units:
             want.setdefault((l, b), []).append(h)
-        kbuf = vbuf = None
         for l in range(w.L):
             for b in range(w.B):
                 n = w.ctx_len[b]
-                k, v = w.request_kv(l, b, threads=gen_threads)
+                k, v = wf.request_kv(l, b, threads=gen_threads)
+                if append:
+                    self.new_kv[(l, b)] = (np.ascontiguousarray(k[:, n:]), np.ascontiguousarray(v[:, n:]))
+                    k, v = np.ascontiguousarray(k[:, :n]), np.ascontiguousarray(v[:, :n])
                 if offload_from_device:
                     kd = torch.from_numpy(k.view(np.int16)).to(self.dev)
                     vd = torch.from_numpy(v.view(np.int16)).to(self.dev)
@@ -141,7 +155,12 @@ class Lockstep:
                     self.ctx.index_offload_host(b, l, k, v)
                     torch.cuda.synchronize()  # the host arrays are reused/freed next
                 for h in want.get((l, b), []):
-                    self.oracle[(l, b, h)] = O.Unit(n, w.cap, np.ascontiguousarray(k[h]), np.ascontiguousarray(v[h]))
+                    if append:
+                        self.oracle[(l, b, h)] = O.TailUnit(np.ascontiguousarray(k[h]), np.ascontiguousarray(v[h]),
+                                                            w.cap, append)
+                    else:
+                        self.oracle[(l, b, h)] = O.Unit(n, w.cap, np.ascontiguousarray(k[h]),
+                                                        np.ascontiguousarray(v[h]))
         self.diverged = set()
         self.qs = w.queries()
         self.t = 0
@@ -156,6 +175,17 @@ class Lockstep:
         w = self.w
         qb = self.qs.bf16()
         qd = torch.from_numpy(qb.view(np.int16)).to(self.dev)
+        if self.append:
+            t = self.t
+            for l in range(w.L):
+                kn = np.stack([self.new_kv[(l, b)][0][:, t] for b in range(w.B)])  # [B][Hkv][128]
+                vn = np.stack([self.new_kv[(l, b)][1][:, t] for b in range(w.B)])
+                kd = torch.from_numpy(kn.view(np.int16)).to(self.dev)
+                vd = torch.from_numpy(vn.view(np.int16)).to(self.dev)
+                self.ctx.append_kv(l, kd, vd)
+                for (ll, b, h), u in self.oracle.items():
+                    if ll == l:
+                        u.append(kn[b, h], vn[b, h])
         for l in range(w.L):
             self.ctx.decode_step(l, qd[l], self.out[l])
         torch.cuda.synchronize()
@@ -175,7 +205,7 @@ class Lockstep:
             ex = exports[l]
             for b in range(w.B):
                 for h in range(w.Hkv):
-                    check_invariants(ex, b * w.Hkv + h, w.partitions(b), t, f"step {t} unit {(l, b, h)}")
+                    check_invariants(ex, b * w.Hkv + h, self.ctx.P_lb[l][b], t, f"step {t} unit {(l, b, h)}")
         for (l, b, h), u in self.oracle.items():
             ex = exports[l]
             ul = b * w.Hkv + h
@@ -183,7 +213,16 @@ class Lockstep:
             q = np.ascontiguousarray(qb[l, b, h * w.G:(h + 1) * w.G])
             g_out = out[l, b, h * w.G:(h + 1) * w.G]
             rep.compared_units += 1
-            if u.P == 0:
+            if self.append:
+                assert u.P == self.ctx.P_lb[l][b], f"{where}: partition count differs"
+                tail = self.ctx.read_tail(l, b, h)
+                assert np.array_equal(tail[:, :u.tail_n], u.tail[:, :u.tail_n]), f"{where}: tail page differs"
+                assert not tail[:, u.tail_n:].any(), f"{where}: tail page not clear past its tokens"
+                if u.P:
+                    gs = self.ctx.summaries(l, b, h).astype(np.float64)
+                    serr = float(np.abs(gs - u.summ).max())
+                    assert serr <= 1e-5, f"{where}: summaries differ by {serr}"
+            if u.P == 0 and not (self.append and u.tail_n):
                 assert np.all(g_out == 0), f"{where}: empty request must give zeros"
                 continue
             sc = O.scores(u.summ, q)
@@ -223,8 +262,11 @@ class Lockstep:
                         match = cand
                         break
                 assert match is not None, f"{where}: GPU set is not one of the valid tie-band sets"
-                fresh = O.Unit(u.ntok, self.fresh_cap)
-                fresh.summ, fresh.host_pages = u.summ, u.host_pages
+                if self.append:
+                    fresh = u.clone_empty(self.fresh_cap)
+                else:
+                    fresh = O.Unit(u.ntok, self.fresh_cap)
+                    fresh.summ, fresh.host_pages = u.summ, u.host_pages
                 ss, _, _, _ = fresh.manage(match, 0)
                 o_out = fresh.attend(match, ss, q)
             err = float(np.abs(g_out - o_out).max())

@@ -44,7 +44,8 @@ def _cfg(**kw):
 
 @pytest.mark.parametrize("bad", [dict(head_dim=64), dict(part_tokens=32), dict(q_heads=7), dict(topk=0),
                                  dict(topk=1000), dict(buf_mult=0), dict(batch=0), dict(seg_entries=16),
-                                 dict(q_heads=2 * 17, kv_heads=2), dict(seg_pool_segments=-1)])
+                                 dict(q_heads=2 * 17, kv_heads=2), dict(seg_pool_segments=-1),
+                                 dict(append_tokens=-1), dict(append_tokens=1 << 30)])
 def test_invalid_configs_are_rejected(bad):
     with pytest.raises(B.SpinError) as e:
         B.spin_create(_cfg(**bad))

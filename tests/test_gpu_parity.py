@@ -203,6 +203,74 @@ def test_invalid_arguments_and_order():
 
 
 # ---------------------------------------------------------------------------
+# KV append (tail mode): one token per request and layer before every decode step.
+# ---------------------------------------------------------------------------
+def test_append_tail_lockstep_narrow():
+    """Ragged initial contexts (tails of 40, 17, 2 and 0 tokens, one empty request), GQA 5, two
+    layers, 2x buffer: tails fill and become selectable partitions mid-run; the tail page, the
+    grown summaries, page state and outputs follow the oracle's tail mode."""
+    w = W.Workload("append", B=4, L=2, Hq=10, Hkv=2, ctx_len=[1000, 4113, 130, 0], topk=8, buf_mult=2,
+                   drift_a=0.8, drift_c=0.2, steps=80, seed=21)
+    ls = Lockstep(w, append=w.steps)
+    try:
+        for _ in range(w.steps):
+            ls.step()
+        st = ls.ctx.stats()
+        assert st["device_error"] == 0
+        assert st["appended_tokens"] == w.steps * w.B * w.L
+        # every request's tail filled at least once (40 + 24, 17 + 47, 2 + 62, 0 + 64 tokens)
+        assert st["tail_flushes"] >= w.B * w.L
+        assert ls.ctx.P_lb[0] == [(n + w.steps) // 64 for n in w.ctx_len]
+        assert ls.report.max_out_err <= OUT_TOL and st["evictions"] > 0
+    finally:
+        ls.close()
+
+
+@pytest.mark.parametrize("G", [8, 16])
+def test_append_tail_lockstep_wide(G):
+    """64 units per layer (the fused score path), GQA 8 and 16 (one and two head tiles)."""
+    w = W.Workload("append_wide", B=32, L=1, Hq=2 * G, Hkv=2, ctx_len=[1984 + 13 * b for b in range(32)], topk=6,
+                   buf_mult=3, drift_a=0.8, drift_c=0.2, steps=70, seed=43)
+    ls = Lockstep(w, append=w.steps, units=sample_units(w, 16, seed=3))
+    try:
+        for _ in range(w.steps):
+            ls.step()
+        st = ls.ctx.stats()
+        assert st["device_error"] == 0 and st["tail_flushes"] >= w.B
+        assert ls.report.max_out_err <= OUT_TOL
+    finally:
+        ls.close()
+
+
+def test_append_errors():
+    """Append on a fixed-context handle is out of order; growing past ctx_len + append_tokens is
+    refused before anything is enqueued, and the context stays usable."""
+    from sparse_attention_tiered_gb300 import SpinContext, SpinError
+    from sparse_attention_tiered_gb300._binding import SPIN_ERR_CAPACITY, SPIN_ERR_STATE
+    w = W.Workload("append_err", B=2, L=1, Hq=4, Hkv=2, ctx_len=[100, 64], topk=2, buf_mult=2,
+                   drift_a=0.9, drift_c=0.1, steps=1, seed=0)
+    kn = torch.zeros((2, 2, 128), dtype=torch.int16, device="cuda")
+    with SpinContext.for_workload(w) as ctx:
+        with pytest.raises(SpinError) as e:
+            ctx.append_kv(0, kn, kn)
+        assert e.value.code == SPIN_ERR_STATE
+    with SpinContext.for_workload(w, append_tokens=2) as ctx:
+        for b in range(w.B):
+            ctx.index_offload_host(b, 0, *w.request_kv(0, b))
+        ctx.append_kv(0, kn, kn)
+        ctx.append_kv(0, kn, kn)
+        with pytest.raises(SpinError) as e:
+            ctx.append_kv(0, kn, kn)
+        assert e.value.code == SPIN_ERR_CAPACITY
+        q = torch.from_numpy(w.queries().bf16()[0].view(np.int16)).cuda()
+        out = torch.empty((2, 4, 128), dtype=torch.float32, device="cuda")
+        ctx.decode_step(0, q, out)
+        st = ctx.stats()
+        assert st["appended_tokens"] == 4 and st["device_error"] == 0
+        assert ctx.P_lb[0] == [1, 1] and ctx.tail_lb[0] == [38, 2]
+
+
+# ---------------------------------------------------------------------------
 # Full-size workloads: sampled units, the launch configuration the benchmark times.
 # ---------------------------------------------------------------------------
 FULL = [
@@ -265,3 +333,15 @@ def test_tier_split_metadata_same_results_less_hbm():
     for key in ("hits", "misses", "evictions", "live_segments"):
         assert st_a[key] == st_b[key], key
     assert st_b["metadata_bytes"] == st_a["metadata_bytes"] - st_a["pool_segments"] * 64 * 4
+
+
+def test_hugepage_host_store_same_results():
+    """The page store as a huge-page mapping registered with CUDA: identical lockstep results."""
+    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_HOST_HUGEPAGES
+    w = W.Workload("huge", B=3, L=2, Hq=10, Hkv=2, ctx_len=[1000, 4113, 9000], topk=8, buf_mult=2,
+                   drift_a=0.8, drift_c=0.2, steps=12, seed=47)
+    rep_a, st_a = _run(w)
+    rep_b, st_b = _run(w, flags=SPIN_FLAG_HOST_HUGEPAGES)
+    assert rep_b.max_out_err <= OUT_TOL
+    for key in ("hits", "misses", "evictions", "live_segments", "host_store_bytes"):
+        assert st_a[key] == st_b[key], key
