@@ -73,6 +73,7 @@ struct AttnSmem {
   uint64_t* mrg;      // [2]: written, read
   StageMeta* meta;    // [kStages]
   int* abort_flag;
+  int* hits_done;     // set by the producer once this CTA's resident-page tasks are issued
 };
 
 __host__ __device__ inline size_t attn_smem_layout(AttnSmem* s, uint8_t* base) {
@@ -90,6 +91,7 @@ __host__ __device__ inline size_t attn_smem_layout(AttnSmem* s, uint8_t* base) {
   uint8_t* mrg = take(sizeof(uint64_t) * 2, 8);
   uint8_t* meta = take(sizeof(StageMeta) * kStages, 16);
   uint8_t* ab = take(sizeof(int), 4);
+  uint8_t* hd = take(sizeof(int), 4);
   if (s) {
     s->ring = ring;
     s->merge = (float*)merge;
@@ -98,6 +100,7 @@ __host__ __device__ inline size_t attn_smem_layout(AttnSmem* s, uint8_t* base) {
     s->mrg = (uint64_t*)mrg;
     s->meta = (StageMeta*)meta;
     s->abort_flag = (int*)ab;
+    s->hits_done = (int*)hd;
   }
   return off;
 }
@@ -165,10 +168,30 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
+__device__ __forceinline__ int ld_relaxed(const int* p) {
   int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Wait until *p reaches `want` (== when exact, else >=), bounded by kWaitNs. Polls with
+// relaxed loads and a short sleep, then one acquire fence: acquire loads and fences in a
+// tight loop hold up the SM's other memory traffic (the retrievers' host loads).
+__device__ __noinline__ bool wait_flag(const int* p, int want, bool exact) {
+  auto hit = [&](int v) { return exact ? v == want : v >= want; };
+  bool ok = hit(ld_relaxed(p));
+  if (!ok) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 30) && !ok; ++it) {
+      __nanosleep(128);
+      ok = hit(ld_relaxed(p));
+      if (!ok && (it & 63u) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
+    }
+  }
+  if (ok) fence_acq_rel();
+  return ok;
 }
 
 __device__ __forceinline__ void st_release(int* p, int v) {
@@ -295,6 +318,7 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
     mbar_init(smem_u32(&sm.mrg[0]), kCWarps);
     mbar_init(smem_u32(&sm.mrg[1]), kCWarps);
     *sm.abort_flag = 0;
+    *sm.hits_done = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -302,10 +326,22 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
 
   if (warp > kCWarps) {
     // ------------------------------ retrievers ------------------------------
-    if (warp - kCWarps - 1 >= a.retr_warps) return;  // fewer host loads in flight per SM
+    // retr_warps warps copy from the start; retr_late more join once this CTA's
+    // resident pages are issued (so they do not slow the HBM-bound hits); the rest idle.
+    const int rw = warp - kCWarps - 1;
+    bool active = rw < a.retr_warps;
+    if (!active && rw < a.retr_warps + a.retr_late) {
+      volatile int* hd = sm.hits_done;
+      const unsigned long long t0 = globaltimer_ns();
+      for (uint32_t it = 1; it < (1u << 30) && !*hd; ++it) {
+        __nanosleep(256);
+        if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
+      }
+      active = *hd != 0 && !*abort_flag;
+    }
     constexpr int kVec = kPageBytes / 16;  // 2048 x 16 B
     constexpr int kUnroll = 16;            // 16 x 16 B in flight per lane
-    for (;;) {
+    for (; active;) {
       int m = 0;
       if (lane == 0) m = atomicAdd(&a.counters[kCtrRetrieve], 1);
       m = __shfl_sync(0xffffffffu, m, 0);
@@ -323,293 +359,282 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) dst[c + u * 32 + lane] = r[u];
       }
-      __threadfence();
+      fence_acq_rel();  // each lane's stores of the page before the flag (acq_rel: no full sc fence)
       __syncwarp();
       if (lane == 0) st_release(a.ready + m, tag);
     }
-    return;
-  }
-
-  if (warp == kCWarps) {
+  } else if (warp == kCWarps) {
     // ------------------------------ producer ------------------------------
-    if (lane != 0) return;
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-    const uint32_t qbytes = (uint32_t)a.G * kD * 2;
-    const int U = a.B * a.Hkv;
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+      const uint32_t qbytes = (uint32_t)a.G * kD * 2;
+      const int U = a.B * a.Hkv;
+      int i = 0;
+      bool ok = true;
+      // Stage one page into the ring. part = partial slot of its task.
+      auto issue = [&](int ul, int att, int part, bool first) -> bool {
+        const int st = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (!mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) return false;
+        int slot = a.att_slot[att];
+        const bool tail = a.tail_n != nullptr && slot == a.cap;  // the unit's tail page
+        if (!tail && (slot < 0 || slot >= a.cap)) {  // never expected: stage slot 0 instead and report
+          atomicOr(a.err, kErrIndex);
+          slot = 0;
+        }
+        StageMeta m;
+        m.part = part;
+        m.ul = ul;
+        m.valid = a.att_valid[att];
+        m.first = first;
+        sm.meta[st] = m;
+        const uint32_t fb = smem_u32(&sm.full[st]);
+        mbar_arrive_expect_tx(fb, kPageBytes + (first ? qbytes : 0u));
+        const int y = tail ? (int)((a.pool_slots + a.unit_base + ul) * 128)
+                           : (int)(((a.unit_base + ul) * a.cap + slot) * 128);
+        const uint32_t dst = smem_u32(sm.ring + (size_t)st * kStageBytes);
+        tma_load_2d(dst, &tmap, fb, 0, y);
+        tma_load_2d(dst + 8192, &tmap, fb, 64, y);
+        tma_load_2d(dst + 16384, &tmap, fb, 0, y + 64);
+        tma_load_2d(dst + 24576, &tmap, fb, 64, y + 64);
+        if (first) {
+          const int b = ul / a.Hkv, h = ul - b * a.Hkv;
+          bulk_load(dst + kPageBytes, a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, qbytes, fb);
+        }
+        ++i;
+        return true;
+      };
+      // 1) resident pages: tasks of up to ppt pages of one unit
+      int next = atomicAdd(&a.counters[kCtrTaskHits], 1);
+      while (ok) {
+        const int task = next;
+        if (task >= n_hit_tasks) break;
+        next = atomicAdd(&a.counters[kCtrTaskHits], 1);  // prefetch the following task
+        if (*abort_flag) { ok = false; break; }
+        const int ul = task / a.n_chunks, c = task - ul * a.n_chunks;
+        const int nh = a.n_hit[ul];
+        const int j0 = c * a.ppt, j1 = min(nh, j0 + a.ppt);
+        for (int j = j0; j < j1 && ok; ++j) ok = issue(ul, ul * a.ka + j, task, j == j0);
+      }
+      *((volatile int*)sm.hits_done) = 1;  // the late retriever warps may start
+      // 2) retrieved pages, in miss-list order, each once its copy is published
+      while (ok) {
+        const int m = atomicAdd(&a.counters[kCtrTaskMisses], 1);
+        if (m >= n_miss) break;
+        if (*abort_flag) { ok = false; break; }
+        if (!wait_flag(a.ready + m, tag, true)) { ok = false; break; }
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what the generic stores wrote
+        int att = a.miss_att[m];
+        if (att < 0 || att >= U * a.ka) {  // never expected
+          atomicOr(a.err, kErrIndex);
+          att = 0;
+        }
+        const int ul = att / a.ka;
+        ok = issue(ul, att, U * a.n_chunks + att, true);
+      }
+      if (ok) {
+        // sentinel: tells the consumers that no task follows
+        const int st = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) {
+          sm.meta[st].part = -1;
+          mbar_arrive(smem_u32(&sm.full[st]));
+        } else {
+          ok = false;
+        }
+      }
+      if (!ok) {
+        atomicOr(a.err, kErrTimeout);
+        *abort_flag = 1;
+        // drain the copies already issued before leaving (bounded)
+        for (int m = max(0, i - kStages); m < i; ++m)
+          (void)mbar_wait(smem_u32(&sm.full[m % kStages]), (uint32_t)(m / kStages) & 1u);
+      }
+      *((volatile int*)sm.hits_done) = 1;  // also on the abort path: nobody waits for it in vain
+    }
+  } else {
+    // ------------------------------ consumers ------------------------------
+    const int w = warp;               // tokens 16w .. 16w+15 of every page
+    const int t0 = 16 * w;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int g4 = lane >> 2, q4 = lane & 3;
+    const int tokA = t0 + ri + ((mi & 1) << 3);   // K rows feeding the A operand
+    const int tokV = t0 + ri + ((mi >> 1) << 3);  // V rows feeding the transposed A operand
+    float* mw = sm.merge + w * kMergeFloats;
+
+    uint32_t qb[NT][8][2];
+    float o[8][NT][4];
+    float mrow[NT][2], lrow[NT][2];
+    int cur = -1;
+    uint32_t mph = 0;
     int i = 0;
-    bool ok = true;
-    // Stage one page into the ring. part = partial slot of its task.
-    auto issue = [&](int ul, int att, int part, bool first) -> bool {
+
+    for (;;) {
       const int st = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-      if (!mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) return false;
-      int slot = a.att_slot[att];
-      const bool tail = a.tail_n != nullptr && slot == a.cap;  // the unit's tail page
-      if (!tail && (slot < 0 || slot >= a.cap)) {  // never expected: stage slot 0 instead and report
-        atomicOr(a.err, kErrIndex);
-        slot = 0;
+      if (!mbar_wait(smem_u32(&sm.full[st]), ph)) {
+        atomicOr(a.err, kErrTimeout);
+        *abort_flag = 1;
+        break;
       }
-      StageMeta m;
-      m.part = part;
-      m.ul = ul;
-      m.valid = a.att_valid[att];
-      m.first = first;
-      sm.meta[st] = m;
-      const uint32_t fb = smem_u32(&sm.full[st]);
-      mbar_arrive_expect_tx(fb, kPageBytes + (first ? qbytes : 0u));
-      const int y = tail ? (int)((a.pool_slots + a.unit_base + ul) * 128)
-                         : (int)(((a.unit_base + ul) * a.cap + slot) * 128);
-      const uint32_t dst = smem_u32(sm.ring + (size_t)st * kStageBytes);
-      tma_load_2d(dst, &tmap, fb, 0, y);
-      tma_load_2d(dst + 8192, &tmap, fb, 64, y);
-      tma_load_2d(dst + 16384, &tmap, fb, 0, y + 64);
-      tma_load_2d(dst + 24576, &tmap, fb, 64, y + 64);
-      if (first) {
-        const int b = ul / a.Hkv, h = ul - b * a.Hkv;
-        bulk_load(dst + kPageBytes, a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, qbytes, fb);
+      const StageMeta m = sm.meta[st];
+      uint8_t* stage = sm.ring + (size_t)st * kStageBytes;
+      if (m.part != cur || m.part < 0) {
+        if (cur >= 0) {
+          // ---- finalize the previous task: merge the four warps, write partials ----
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float l = lrow[nt][e];
+              l += __shfl_xor_sync(0xffffffffu, l, 4);
+              l += __shfl_xor_sync(0xffffffffu, l, 8);
+              l += __shfl_xor_sync(0xffffffffu, l, 16);
+              const int hh = 8 * nt + 2 * q4 + e;
+#pragma unroll
+              for (int md = 0; md < 8; ++md) {
+                mw[hh * kMergeRow + 16 * md + g4] = o[md][nt][e];
+                mw[hh * kMergeRow + 16 * md + g4 + 8] = o[md][nt][2 + e];
+              }
+              if (g4 == 0) {
+                mw[16 * kMergeRow + hh] = mrow[nt][e];
+                mw[16 * kMergeRow + 16 + hh] = l;
+              }
+            }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.mrg[0]));
+          if (!mbar_wait(smem_u32(&sm.mrg[0]), mph)) {
+            atomicOr(a.err, kErrTimeout);
+            *abort_flag = 1;
+            break;
+          }
+          const int d = w * 32 + lane;  // 0..127
+          for (int g = 0; g < a.G; ++g) {
+            float M = -INFINITY;
+#pragma unroll
+            for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, sm.merge[ww * kMergeFloats + 16 * kMergeRow + g]);
+            float L = 0.f, acc = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+              for (int ww = 0; ww < kCWarps; ++ww) {
+                const float* src = sm.merge + ww * kMergeFloats;
+                const float sc = exp2f(src[16 * kMergeRow + g] - M);
+                L = fmaf(sc, src[16 * kMergeRow + 16 + g], L);
+                acc = fmaf(sc, src[g * kMergeRow + d], acc);
+              }
+            }
+            float* part = a.partials + ((int64_t)cur * a.G + g) * kPartialStride;
+            part[4 + d] = acc;
+            if (d == 0) {
+              part[0] = M;
+              part[1] = L;
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sm.mrg[1]));
+          if (!mbar_wait(smem_u32(&sm.mrg[1]), mph)) {
+            atomicOr(a.err, kErrTimeout);
+            *abort_flag = 1;
+            break;
+          }
+          mph ^= 1u;
+        }
+        if (m.part < 0) break;
+        cur = m.part;
+        // query rows of the unit, brought with the task's first page: B operand fragments
+        const uint8_t* qs = stage + kPageBytes;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int head = 8 * nt + g4;
+          const bool live = head < a.G;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            qb[nt][kk][0] = live ? *reinterpret_cast<const uint32_t*>(qs + head * 256 + (16 * kk + 2 * q4) * 2) : 0u;
+            qb[nt][kk][1] = live ? *reinterpret_cast<const uint32_t*>(qs + head * 256 + (16 * kk + 8 + 2 * q4) * 2)
+                                 : 0u;
+          }
+          mrow[nt][0] = mrow[nt][1] = -INFINITY;
+          lrow[nt][0] = lrow[nt][1] = 0.f;
+#pragma unroll
+          for (int md = 0; md < 8; ++md) o[md][nt][0] = o[md][nt][1] = o[md][nt][2] = o[md][nt][3] = 0.f;
+        }
       }
+
+      // ---------------- one page: tokens t0..t0+15 ----------------
+      const uint32_t kb = smem_u32(stage);
+      const uint32_t vb = kb + 16384;
+      float s[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t af[4];
+        ldsm_x4(kb + swz(tokA, 2 * kk + (mi >> 1)), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
+      }
+      // online softmax per head (column), over this warp's 16 tokens (rows)
+      const bool v0 = (t0 + g4) < m.valid, v1 = (t0 + g4 + 8) < m.valid;
+      uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float p[4];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float x0 = v0 ? s[nt][e] * kScaleLog2 : -INFINITY;
+          const float x1 = v1 ? s[nt][2 + e] * kScaleLog2 : -INFINITY;
+          float mx = fmaxf(x0, x1);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mn = fmaxf(mrow[nt][e], mx);
+          const float al = (mn == -INFINITY) ? 1.f : exp2f(mrow[nt][e] - mn);
+          p[e] = (mn == -INFINITY) ? 0.f : exp2f(x0 - mn);
+          p[2 + e] = (mn == -INFINITY) ? 0.f : exp2f(x1 - mn);
+          lrow[nt][e] = fmaf(lrow[nt][e], al, p[e] + p[2 + e]);
+          mrow[nt][e] = mn;
+#pragma unroll
+          for (int md = 0; md < 8; ++md) {
+            o[md][nt][e] *= al;
+            o[md][nt][2 + e] *= al;
+          }
+        }
+        // P^T fragments (token rows, head columns) -> B operand (head rows, token columns)
+        const uint32_t h0 = pack_bf16(p[0], p[1]), h1 = pack_bf16(p[2], p[3]);
+        const uint32_t l0 = pack_bf16(p[0] - bf16_lo_f(h0), p[1] - bf16_hi_f(h0));
+        const uint32_t l1 = pack_bf16(p[2] - bf16_lo_f(h1), p[3] - bf16_hi_f(h1));
+        bh[nt][0] = movmatrix_t(h0);
+        bh[nt][1] = movmatrix_t(h1);
+        bl[nt][0] = movmatrix_t(l0);
+        bl[nt][1] = movmatrix_t(l1);
+      }
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        uint32_t af[4];
+        ldsm_x4_t(vb + swz(tokV, 2 * md + (mi & 1)), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16(o[md][nt], af, bh[nt][0], bh[nt][1]);
+          mma_bf16(o[md][nt], af, bl[nt][0], bl[nt][1]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
       ++i;
-      return true;
-    };
-    // 1) resident pages: tasks of up to ppt pages of one unit
-    int next = atomicAdd(&a.counters[kCtrTaskHits], 1);
-    while (ok) {
-      const int task = next;
-      if (task >= n_hit_tasks) break;
-      next = atomicAdd(&a.counters[kCtrTaskHits], 1);  // prefetch the following task
-      if (*abort_flag) { ok = false; break; }
-      const int ul = task / a.n_chunks, c = task - ul * a.n_chunks;
-      const int nh = a.n_hit[ul];
-      const int j0 = c * a.ppt, j1 = min(nh, j0 + a.ppt);
-      for (int j = j0; j < j1 && ok; ++j) ok = issue(ul, ul * a.ka + j, task, j == j0);
-    }
-    // 2) retrieved pages, in miss-list order, each once its copy is published
-    while (ok) {
-      const int m = atomicAdd(&a.counters[kCtrTaskMisses], 1);
-      if (m >= n_miss) break;
-      if (*abort_flag) { ok = false; break; }
-      bool ready = ld_acquire(a.ready + m) == tag;
-      if (!ready) {
-        const unsigned long long t0 = globaltimer_ns();
-        for (uint32_t it = 1; it < (1u << 30) && !ready; ++it) {
-          ready = ld_acquire(a.ready + m) == tag;
-          if (!ready && (it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
-        }
-      }
-      if (!ready) { ok = false; break; }
-      asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what the generic stores wrote
-      int att = a.miss_att[m];
-      if (att < 0 || att >= U * a.ka) {  // never expected
-        atomicOr(a.err, kErrIndex);
-        att = 0;
-      }
-      const int ul = att / a.ka;
-      ok = issue(ul, att, U * a.n_chunks + att, true);
-    }
-    if (ok) {
-      // sentinel: tells the consumers that no task follows
-      const int st = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-      if (mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) {
-        sm.meta[st].part = -1;
-        mbar_arrive(smem_u32(&sm.full[st]));
-      } else {
-        ok = false;
-      }
-    }
-    if (!ok) {
-      atomicOr(a.err, kErrTimeout);
-      *abort_flag = 1;
-      // drain the copies already issued before leaving (bounded)
-      for (int m = max(0, i - kStages); m < i; ++m)
-        (void)mbar_wait(smem_u32(&sm.full[m % kStages]), (uint32_t)(m / kStages) & 1u);
-    }
-    return;
-  }
-
-  // ------------------------------ consumers ------------------------------
-  const int w = warp;               // tokens 16w .. 16w+15 of every page
-  const int t0 = 16 * w;
-  const int mi = lane >> 3, ri = lane & 7;
-  const int g4 = lane >> 2, q4 = lane & 3;
-  const int tokA = t0 + ri + ((mi & 1) << 3);   // K rows feeding the A operand
-  const int tokV = t0 + ri + ((mi >> 1) << 3);  // V rows feeding the transposed A operand
-  float* mw = sm.merge + w * kMergeFloats;
-
-  uint32_t qb[NT][8][2];
-  float o[8][NT][4];
-  float mrow[NT][2], lrow[NT][2];
-  int cur = -1;
-  uint32_t mph = 0;
-  int i = 0;
-
-  for (;;) {
-    const int st = i % kStages;
-    const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-    if (!mbar_wait(smem_u32(&sm.full[st]), ph)) {
-      atomicOr(a.err, kErrTimeout);
-      *abort_flag = 1;
-      break;
-    }
-    const StageMeta m = sm.meta[st];
-    uint8_t* stage = sm.ring + (size_t)st * kStageBytes;
-    if (m.part != cur || m.part < 0) {
-      if (cur >= 0) {
-        // ---- finalize the previous task: merge the four warps, write partials ----
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float l = lrow[nt][e];
-            l += __shfl_xor_sync(0xffffffffu, l, 4);
-            l += __shfl_xor_sync(0xffffffffu, l, 8);
-            l += __shfl_xor_sync(0xffffffffu, l, 16);
-            const int hh = 8 * nt + 2 * q4 + e;
-#pragma unroll
-            for (int md = 0; md < 8; ++md) {
-              mw[hh * kMergeRow + 16 * md + g4] = o[md][nt][e];
-              mw[hh * kMergeRow + 16 * md + g4 + 8] = o[md][nt][2 + e];
-            }
-            if (g4 == 0) {
-              mw[16 * kMergeRow + hh] = mrow[nt][e];
-              mw[16 * kMergeRow + 16 + hh] = l;
-            }
-          }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.mrg[0]));
-        if (!mbar_wait(smem_u32(&sm.mrg[0]), mph)) {
-          atomicOr(a.err, kErrTimeout);
-          *abort_flag = 1;
-          break;
-        }
-        const int d = w * 32 + lane;  // 0..127
-        for (int g = 0; g < a.G; ++g) {
-          float M = -INFINITY;
-#pragma unroll
-          for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, sm.merge[ww * kMergeFloats + 16 * kMergeRow + g]);
-          float L = 0.f, acc = 0.f;
-          if (M != -INFINITY) {
-#pragma unroll
-            for (int ww = 0; ww < kCWarps; ++ww) {
-              const float* src = sm.merge + ww * kMergeFloats;
-              const float sc = exp2f(src[16 * kMergeRow + g] - M);
-              L = fmaf(sc, src[16 * kMergeRow + 16 + g], L);
-              acc = fmaf(sc, src[g * kMergeRow + d], acc);
-            }
-          }
-          float* part = a.partials + ((int64_t)cur * a.G + g) * kPartialStride;
-          part[4 + d] = acc;
-          if (d == 0) {
-            part[0] = M;
-            part[1] = L;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sm.mrg[1]));
-        if (!mbar_wait(smem_u32(&sm.mrg[1]), mph)) {
-          atomicOr(a.err, kErrTimeout);
-          *abort_flag = 1;
-          break;
-        }
-        mph ^= 1u;
-      }
-      if (m.part < 0) break;
-      cur = m.part;
-      // query rows of the unit, brought with the task's first page: B operand fragments
-      const uint8_t* qs = stage + kPageBytes;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int head = 8 * nt + g4;
-        const bool live = head < a.G;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          qb[nt][kk][0] = live ? *reinterpret_cast<const uint32_t*>(qs + head * 256 + (16 * kk + 2 * q4) * 2) : 0u;
-          qb[nt][kk][1] = live ? *reinterpret_cast<const uint32_t*>(qs + head * 256 + (16 * kk + 8 + 2 * q4) * 2)
-                               : 0u;
-        }
-        mrow[nt][0] = mrow[nt][1] = -INFINITY;
-        lrow[nt][0] = lrow[nt][1] = 0.f;
-#pragma unroll
-        for (int md = 0; md < 8; ++md) o[md][nt][0] = o[md][nt][1] = o[md][nt][2] = o[md][nt][3] = 0.f;
-      }
     }
 
-    // ---------------- one page: tokens t0..t0+15 ----------------
-    const uint32_t kb = smem_u32(stage);
-    const uint32_t vb = kb + 16384;
-    float s[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t af[4];
-      ldsm_x4(kb + swz(tokA, 2 * kk + (mi >> 1)), af[0], af[1], af[2], af[3]);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma_bf16(s[nt], af, qb[nt][kk][0], qb[nt][kk][1]);
-    }
-    // online softmax per head (column), over this warp's 16 tokens (rows)
-    const bool v0 = (t0 + g4) < m.valid, v1 = (t0 + g4 + 8) < m.valid;
-    uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float p[4];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float x0 = v0 ? s[nt][e] * kScaleLog2 : -INFINITY;
-        const float x1 = v1 ? s[nt][2 + e] * kScaleLog2 : -INFINITY;
-        float mx = fmaxf(x0, x1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mn = fmaxf(mrow[nt][e], mx);
-        const float al = (mn == -INFINITY) ? 1.f : exp2f(mrow[nt][e] - mn);
-        p[e] = (mn == -INFINITY) ? 0.f : exp2f(x0 - mn);
-        p[2 + e] = (mn == -INFINITY) ? 0.f : exp2f(x1 - mn);
-        lrow[nt][e] = fmaf(lrow[nt][e], al, p[e] + p[2 + e]);
-        mrow[nt][e] = mn;
-#pragma unroll
-        for (int md = 0; md < 8; ++md) {
-          o[md][nt][e] *= al;
-          o[md][nt][2 + e] *= al;
-        }
-      }
-      // P^T fragments (token rows, head columns) -> B operand (head rows, token columns)
-      const uint32_t h0 = pack_bf16(p[0], p[1]), h1 = pack_bf16(p[2], p[3]);
-      const uint32_t l0 = pack_bf16(p[0] - bf16_lo_f(h0), p[1] - bf16_hi_f(h0));
-      const uint32_t l1 = pack_bf16(p[2] - bf16_lo_f(h1), p[3] - bf16_hi_f(h1));
-      bh[nt][0] = movmatrix_t(h0);
-      bh[nt][1] = movmatrix_t(h1);
-      bl[nt][0] = movmatrix_t(l0);
-      bl[nt][1] = movmatrix_t(l1);
-    }
-#pragma unroll
-    for (int md = 0; md < 8; ++md) {
-      uint32_t af[4];
-      ldsm_x4_t(vb + swz(tokV, 2 * md + (mi & 1)), af[0], af[1], af[2], af[3]);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        mma_bf16(o[md][nt], af, bh[nt][0], bh[nt][1]);
-        mma_bf16(o[md][nt], af, bl[nt][0], bl[nt][1]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
-    ++i;
   }
 
   // ---------------- all pages of all CTAs done: combine the partials ----------------
-  asm volatile("bar.sync 2, %0;" ::"n"(kCWarps * 32) : "memory");
+  // Every warp of the CTA (retrievers after their last claim, the producer, the
+  // consumers after their last page) meets here before the CTA arrives, so block 0's
+  // counter reset below cannot race with a late claim of this step.
+  __syncthreads();
   if (tid == 0) {
     __threadfence();
     atomicAdd(&a.counters[kCtrArrive], 1);
     const int target = (int)gridDim.x * tag;  // the counter grows by gridDim.x every step
-    bool done = ld_acquire(&a.counters[kCtrArrive]) >= target;
-    const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t it = 1; it < (1u << 30) && !done; ++it) {
-      done = ld_acquire(&a.counters[kCtrArrive]) >= target;
-      if (!done && (it & 255u) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
-    }
-    if (!done) atomicOr(a.err, kErrTimeout);
+    if (!wait_flag(&a.counters[kCtrArrive], target, false)) atomicOr(a.err, kErrTimeout);
     if (blockIdx.x == 0) {  // the step's counters are no longer read by anyone
       a.counters[kCtrMiss] = 0;
       a.counters[kCtrTaskHits] = 0;
@@ -618,9 +643,10 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       a.counters[kCtrStep] += 1;
     }
   }
-  asm volatile("bar.sync 2, %0;" ::"n"(kCWarps * 32) : "memory");
+  __syncthreads();
+  if (warp >= kCWarps) return;
   const int U = a.B * a.Hkv;
-  for (int ul = blockIdx.x; ul < U; ul += gridDim.x) combine_unit(a, ul, w, lane);
+  for (int ul = blockIdx.x; ul < U; ul += gridDim.x) combine_unit(a, ul, warp, lane);
 }
 
 }  // namespace

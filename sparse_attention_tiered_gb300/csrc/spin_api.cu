@@ -89,7 +89,8 @@ struct spin_ctx {
   int B = 0, L = 0, Hq = 0, Hkv = 0, G = 0, k = 0, cap = 0, D = 0, P_max = 0, ppt = 1, n_chunks = 1;
   int sm_count = 0;
   int select_group = 0;  // SPIN_SELECT_GROUP: threads of the top-k/manager group (0 = by unit size)
-  int retr_warps = 2;  // SPIN_RETRIEVE_WARPS (1..8): retriever warps per attend CTA
+  int retr_warps = 2;  // SPIN_RETRIEVE_WARPS (1..8): retriever warps per attend CTA from its start
+  int retr_late = 8;   // SPIN_RETRIEVE_LATE (0..8): retriever warps that join after the CTA's resident pages
   std::vector<int64_t> ctx_len;
   std::vector<int32_t> P_b, ntok_b;  // fixed mode: partitions and tokens of each request
   std::vector<int32_t> pstride_b;    // host-store pages per KV head of each request (its partition capacity)
@@ -333,6 +334,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.ppt = c->ppt;
   a.S = (int32_t)c->S;
   a.retr_warps = c->retr_warps;
+  a.retr_late = c->retr_late;
   a.select_group = c->select_group;
   a.ka = c->ka;
   a.P_b = c->d_P_lb + (int64_t)l * c->B;
@@ -526,7 +528,11 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     if (v >= 1 && v <= 8) c->retr_warps = v;
   }
   if (c->G > 8) c->retr_warps = std::min(c->retr_warps, 4);  // the two-tile kernel has four retriever warps
-  if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = 0;    // nothing publishes a retrieved page
+  if (const char* env = getenv("SPIN_RETRIEVE_LATE")) {
+    const int v = atoi(env);
+    if (v >= 0 && v <= 8) c->retr_late = v;
+  }
+  if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = c->retr_late = 0;  // nothing publishes a page
   if (const char* env = getenv("SPIN_SELECT_GROUP")) c->select_group = atoi(env);  // 0 auto, 32, 512
 
   // attention work split: pages per task

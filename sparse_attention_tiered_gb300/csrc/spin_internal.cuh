@@ -33,7 +33,8 @@ enum : uint32_t {
 struct LayerArgs {
   int32_t layer, B, Hq, Hkv, G, k, cap, D, P_max, n_chunks, ppt, S;
   int32_t ka;                // attention entries per unit: k, plus one for the tail page in tail mode
-  int32_t retr_warps;        // retriever warps active per CTA of the attend kernel
+  int32_t retr_warps;        // retriever warps active per CTA of the attend kernel from its start
+  int32_t retr_late;         // further retriever warps that join once the CTA's resident pages are issued
   int32_t select_group;      // 0 = choose by unit size, else 32 or 512 threads for top-k + manager
   const int32_t* P_b;        // [B] selectable partitions of request b in this layer (tail mode: complete ones)
   const int32_t* ntok_b;     // [B] tokens held by those partitions
