@@ -45,35 +45,42 @@ namespace spin {
 
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kCWarps = 4;
-// Retriever warps per CTA: 8 when the group fits one 8-head tile (140 registers a
-// thread), 4 for two tiles (the register file bounds threads x registers).
+constexpr int kStages = 6;    // ring stages (stage i belongs to consumer group i % groups)
+constexpr int kCWarps = 4;    // consumer warps of one group: 16 tokens of a page each
+constexpr int kMaxGroups = 2;
+// Roles per CTA. One 8-head tile (NT = 1, at most 128 registers a thread): two
+// consumer groups that take alternate ring stages, so two pages are in the math at
+// once, each fed by its own producer warp, and six retriever warps (two saturate the
+// host link alone). Two tiles (168 registers): one group, one producer, four
+// retrievers. Threads x registers stay within 64 K.
 template <int NT>
 struct Roles {
-  static constexpr int kRWarps = NT == 1 ? 8 : 4;
-  static constexpr int kThreads = (1 + kCWarps + kRWarps) * 32;
+  static constexpr int kGroups = NT == 1 ? 2 : 1;
+  static constexpr int kConsumers = kCWarps * kGroups;
+  static constexpr int kRWarps = NT == 1 ? 6 : 4;
+  static constexpr int kThreads = (kGroups + kConsumers + kRWarps) * 32;
 };
 constexpr int kQBytes = kMaxGroup * kD * 2;            // query rows of one unit (<= 16 heads)
 constexpr int kStageBytes = kPageBytes + kQBytes;       // 36 KiB, a multiple of 1024
 constexpr int kMergeRow = kD + 4;                       // padded row of the merge buffer
 constexpr int kMergeFloats = 16 * kMergeRow + 32;       // O[16 heads][128+4], m[16], l[16]
+static_assert(kCWarps * kMergeFloats * 4 <= kStageBytes, "a task's merge must fit in its last page's stage");
 constexpr float kScaleLog2 = 0.12751743074173449f;      // log2(e) / sqrt(128)
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s
 
 struct StageMeta {
-  int part, ul, valid, first;  // partial slot of the task, unit, valid tokens, first page of the task
+  int part, ul, valid, first, last;  // partial slot of the task, unit, valid tokens, first / last page of the task
 };
 
 struct AttnSmem {
-  uint8_t* ring;      // kStages x kStageBytes, 1024-aligned
-  float* merge;       // kCWarps x kMergeFloats
+  uint8_t* ring;      // kStages x kStageBytes, 1024-aligned (a task's last stage also holds its merge)
   uint64_t* full;     // [kStages]
   uint64_t* empty;    // [kStages]
-  uint64_t* mrg;      // [2]: written, read
+  uint64_t* mrg;      // [groups][2]: written, read
   StageMeta* meta;    // [kStages]
   int* abort_flag;
-  int* hits_done;     // set by the producer once this CTA's resident-page tasks are issued
+  int* hits_done;     // set once every producer of this CTA has issued its resident-page tasks
+  int* hits_groups;   // producers past their resident pages
 };
 
 __host__ __device__ inline size_t attn_smem_layout(AttnSmem* s, uint8_t* base) {
@@ -85,22 +92,22 @@ __host__ __device__ inline size_t attn_smem_layout(AttnSmem* s, uint8_t* base) {
     return p;
   };
   uint8_t* ring = take((size_t)kStages * kStageBytes, 1024);
-  uint8_t* merge = take(sizeof(float) * kCWarps * kMergeFloats, 16);
   uint8_t* full = take(sizeof(uint64_t) * kStages, 8);
   uint8_t* empty = take(sizeof(uint64_t) * kStages, 8);
-  uint8_t* mrg = take(sizeof(uint64_t) * 2, 8);
+  uint8_t* mrg = take(sizeof(uint64_t) * 2 * kMaxGroups, 8);
   uint8_t* meta = take(sizeof(StageMeta) * kStages, 16);
   uint8_t* ab = take(sizeof(int), 4);
   uint8_t* hd = take(sizeof(int), 4);
+  uint8_t* hg = take(sizeof(int), 4);
   if (s) {
     s->ring = ring;
-    s->merge = (float*)merge;
     s->full = (uint64_t*)full;
     s->empty = (uint64_t*)empty;
     s->mrg = (uint64_t*)mrg;
     s->meta = (StageMeta*)meta;
     s->abort_flag = (int*)ab;
     s->hits_done = (int*)hd;
+    s->hits_groups = (int*)hg;
   }
   return off;
 }
@@ -241,18 +248,18 @@ __device__ __forceinline__ uint32_t swz(int r, int cd) {
 // ---------------------------------------------------------------------------
 // Combine of one unit: out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c
 // over the unit's partials (its hit tasks and its retrieved pages). Consumer
-// warp w takes heads w, w+4, ...; four columns per lane. One pass: the lanes
+// warp w of nw takes heads w, w+nw, ...; four columns per lane. One pass: the lanes
 // fetch the (m, l) of up to 32 partials at a time in parallel, the max and the
 // sum are warp reductions, and the accumulator loads are independent.
 // ---------------------------------------------------------------------------
-__device__ void combine_unit(const LayerArgs& a, int ul, int w, int lane) {
+__device__ void combine_unit(const LayerArgs& a, int ul, int w, int nw, int lane) {
   const int b = ul / a.Hkv, h = ul - b * a.Hkv;
   const int has_tail = (a.tail_n != nullptr && a.tail_n[b] > 0) ? 1 : 0;
   const int keff = a.keff[ul] + has_tail, nh = a.n_hit[ul];  // attended pages; resident ones (tail included)
   const int nc = (nh + a.ppt - 1) / a.ppt;
   const int U = a.B * a.Hkv;
   const int n = nc + (keff - nh);
-  for (int g = w; g < a.G; g += kCWarps) {
+  for (int g = w; g < a.G; g += nw) {
     float4* out = reinterpret_cast<float4*>(a.out + ((int64_t)b * a.Hq + (int64_t)h * a.G + g) * kD);
     // partial slots: hit tasks ul * n_chunks + c (c < nc), retrieved pages U * n_chunks + ul * ka + j (nh <= j < keff)
     auto part_ptr = [&](int i) -> const float* {
@@ -306,6 +313,7 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   AttnSmem sm;
   attn_smem_layout(&sm, base);
+  constexpr int NG = Roles<NT>::kGroups, NC = Roles<NT>::kConsumers;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_miss = a.counters[kCtrMiss];
   const int tag = a.counters[kCtrStep] + 1;  // ready-flag value of this step (flags are never reset)
@@ -313,24 +321,24 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
-      mbar_init(smem_u32(&sm.empty[s]), kCWarps);
+      mbar_init(smem_u32(&sm.empty[s]), kCWarps);  // the four warps of the stage's group
     }
-    mbar_init(smem_u32(&sm.mrg[0]), kCWarps);
-    mbar_init(smem_u32(&sm.mrg[1]), kCWarps);
+    for (int m = 0; m < 2 * NG; ++m) mbar_init(smem_u32(&sm.mrg[m]), kCWarps);
     *sm.abort_flag = 0;
     *sm.hits_done = 0;
+    *sm.hits_groups = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   volatile int* abort_flag = sm.abort_flag;
 
-  if (warp > kCWarps) {
+  if (warp >= NC + NG) {
     // ------------------------------ retrievers ------------------------------
     // retr_warps warps copy from the start; retr_late more join once this CTA's
     // resident pages are issued (so they do not slow the HBM-bound hits); the rest idle.
-    const int rw = warp - kCWarps - 1;
-    bool active = rw < a.retr_warps;
-    if (!active && rw < a.retr_warps + a.retr_late) {
+    const int rw = warp - NC - NG;
+    bool active = rw < a.retr_warps && !a.retrieve_in_select;
+    if (!active && rw < a.retr_warps + a.retr_late && !a.retrieve_in_select) {
       volatile int* hd = sm.hits_done;
       const unsigned long long t0 = globaltimer_ns();
       for (uint32_t it = 1; it < (1u << 30) && !*hd; ++it) {
@@ -363,35 +371,164 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       __syncwarp();
       if (lane == 0) st_release(a.ready + m, tag);
     }
-  } else if (warp == kCWarps) {
-    // ------------------------------ producer ------------------------------
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-      const uint32_t qbytes = (uint32_t)a.G * kD * 2;
-      const int U = a.B * a.Hkv;
-      int i = 0;
-      bool ok = true;
-      // Stage one page into the ring. part = partial slot of its task.
-      auto issue = [&](int ul, int att, int part, bool first) -> bool {
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) return false;
-        int slot = a.att_slot[att];
-        const bool tail = a.tail_n != nullptr && slot == a.cap;  // the unit's tail page
-        if (!tail && (slot < 0 || slot >= a.cap)) {  // never expected: stage slot 0 instead and report
-          atomicOr(a.err, kErrIndex);
-          slot = 0;
+  } else if (warp >= NC) {
+    // ------------------------------ producers ------------------------------
+    // Producer warp g feeds consumer group g: stage indices i = g, g + NG, ... use ring
+    // stage i % kStages. Its stream: resident-page tasks (up to ppt pages of one unit,
+    // claimed from a shared counter), then retrieved pages (one page each, in miss-list
+    // order, once its ready flag is published), then a sentinel.
+    // The whole warp runs the loop so that nothing the issue path needs is a fresh
+    // global load: tasks are claimed two ahead, the next task's page descriptors load
+    // into the lanes' registers (lane j: page j) while the current task issues, and the
+    // next retrieved page's miss-list entry loads before its flag is awaited. Lane 0
+    // alone waits on the ring barriers and issues the copies.
+    constexpr uint32_t kAll = 0xffffffffu;
+    const int g = warp - NC;
+    const uint32_t qbytes = (uint32_t)a.G * kD * 2;
+    const int U = a.B * a.Hkv;
+    if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+    auto load_task = [&](int T, int& slot, int& valid, int& nhit) {
+      if (T < n_hit_tasks) {
+        const int tu = T / a.n_chunks, j0 = (T - tu * a.n_chunks) * a.ppt;
+        nhit = a.n_hit[tu];
+        const bool in = lane < a.ppt && j0 + lane < a.ka;
+        slot = in ? a.att_slot[tu * a.ka + j0 + lane] : 0;
+        valid = in ? a.att_valid[tu * a.ka + j0 + lane] : 0;
+      }
+    };
+    int cur_task = 0, cur_ul = 0, cur_n = 0, cur_j = 0, cur_y = 0, cur_valid = 0;
+    int nx_task, nx_slot = 0, nx_valid = 0, nx_nhit = 0, c2_raw;
+    {
+      const int t0 = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
+      nx_task = __shfl_sync(kAll, t0, 0);
+      load_task(nx_task, nx_slot, nx_valid, nx_nhit);
+      c2_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
+    }
+    bool in_miss = false;
+    // retrieved pages: the next entry claimed and loading ahead
+    int mq = 0, mq_att = 0, mq_valid = 0, m_raw = 0;
+    int64_t mq_dst = 0;
+    bool m_init = false;
+    auto miss_advance = [&]() {
+      mq = __shfl_sync(kAll, m_raw, 0);
+      if (mq < n_miss) {
+        mq_att = a.miss_att[mq];
+        mq_dst = a.miss_dst[mq];
+        mq_valid = a.miss_valid[mq];
+      }
+      m_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskMisses], 1) : 0;
+    };
+    auto leave_hits = [&]() {  // the last producer past its resident pages lets the late retrievers start
+      if (lane == 0 && atomicAdd(sm.hits_groups, 1) == NG - 1) *((volatile int*)sm.hits_done) = 1;
+    };
+    int last_issue[kStages];  // lane 0: last stage index that staged a page in each ring stage
+#pragma unroll
+    for (int st = 0; st < kStages; ++st) last_issue[st] = -1;
+    bool ok = true, done = false;
+    for (int i = g; ok && !done; i += NG) {
+      if (__shfl_sync(kAll, *abort_flag, 0)) {
+        ok = false;
+        break;
+      }
+      int y = 0, valid = 0, part = 0, ul = 0;
+      bool first = false, last_page = false, have = false;
+      while (!have && !done && ok) {
+        if (!in_miss) {
+          if (cur_j < cur_n) {
+            const int j = cur_j++;
+            y = __shfl_sync(kAll, cur_y, j);
+            valid = __shfl_sync(kAll, cur_valid, j);
+            ul = cur_ul;
+            part = cur_task;
+            first = j == 0;
+            last_page = j == cur_n - 1;
+            have = true;
+          } else {
+            const int T = nx_task;
+            if (T >= n_hit_tasks) {
+              in_miss = true;
+              leave_hits();
+              continue;
+            }
+            const int tu = T / a.n_chunks, j0 = (T - tu * a.n_chunks) * a.ppt;
+            cur_task = T;
+            cur_ul = tu;
+            cur_n = max(0, min(nx_nhit, j0 + a.ppt) - j0);
+            cur_j = 0;
+            int slot = nx_slot;
+            if (a.tail_n != nullptr && slot == a.cap) {  // the unit's tail page
+              cur_y = (int)((a.pool_slots + a.unit_base + tu) * 128);
+            } else {
+              if (slot < 0 || slot >= a.cap) {  // never expected for a page of the task: stage slot 0 and report
+                if (lane < cur_n) atomicOr(a.err, kErrIndex);
+                slot = 0;
+              }
+              cur_y = (int)(((a.unit_base + tu) * a.cap + slot) * 128);
+            }
+            cur_valid = nx_valid;
+            nx_task = __shfl_sync(kAll, c2_raw, 0);  // claimed a task ago: no wait
+            load_task(nx_task, nx_slot, nx_valid, nx_nhit);
+            c2_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
+          }
+        } else {
+          if (!m_init) {
+            m_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskMisses], 1) : 0;
+            miss_advance();
+            m_init = true;
+          }
+          if (mq >= n_miss) {
+            done = true;
+            break;
+          }
+          int okf = 1;
+          if (lane == 0) okf = wait_flag(a.ready + mq, tag, true) ? 1 : 0;
+          if (!__shfl_sync(kAll, okf, 0)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");  // TMA reads the generic stores
+          int att = mq_att;
+          int64_t dp = mq_dst;
+          if (att < 0 || att >= U * a.ka || dp < 0 || dp >= a.pool_slots) {  // never expected
+            if (lane == 0) atomicOr(a.err, kErrIndex);
+            att = 0;
+            dp = 0;
+          }
+          ul = att / a.ka;
+          part = U * a.n_chunks + att;
+          y = (int)(dp * 128);
+          valid = mq_valid;
+          first = last_page = true;
+          have = true;
+          miss_advance();
         }
+      }
+      if (!ok) break;
+      const int st = i % kStages;
+      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      int oke = 1;
+      if (lane == 0) oke = mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u) ? 1 : 0;
+      if (!__shfl_sync(kAll, oke, 0)) {
+        ok = false;
+        break;
+      }
+      if (!have) {  // the group's sentinel: no task follows
+        if (lane == 0) {
+          sm.meta[st].part = -1;
+          mbar_arrive(smem_u32(&sm.full[st]));
+        }
+        break;
+      }
+      if (lane == 0) {
         StageMeta m;
         m.part = part;
         m.ul = ul;
-        m.valid = a.att_valid[att];
+        m.valid = valid;
         m.first = first;
+        m.last = last_page;
         sm.meta[st] = m;
         const uint32_t fb = smem_u32(&sm.full[st]);
         mbar_arrive_expect_tx(fb, kPageBytes + (first ? qbytes : 0u));
-        const int y = tail ? (int)((a.pool_slots + a.unit_base + ul) * 128)
-                           : (int)(((a.unit_base + ul) * a.cap + slot) * 128);
         const uint32_t dst = smem_u32(sm.ring + (size_t)st * kStageBytes);
         tma_load_2d(dst, &tmap, fb, 0, y);
         tma_load_2d(dst + 8192, &tmap, fb, 64, y);
@@ -401,73 +538,35 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
           const int b = ul / a.Hkv, h = ul - b * a.Hkv;
           bulk_load(dst + kPageBytes, a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, qbytes, fb);
         }
-        ++i;
-        return true;
-      };
-      // 1) resident pages: tasks of up to ppt pages of one unit
-      int next = atomicAdd(&a.counters[kCtrTaskHits], 1);
-      while (ok) {
-        const int task = next;
-        if (task >= n_hit_tasks) break;
-        next = atomicAdd(&a.counters[kCtrTaskHits], 1);  // prefetch the following task
-        if (*abort_flag) { ok = false; break; }
-        const int ul = task / a.n_chunks, c = task - ul * a.n_chunks;
-        const int nh = a.n_hit[ul];
-        const int j0 = c * a.ppt, j1 = min(nh, j0 + a.ppt);
-        for (int j = j0; j < j1 && ok; ++j) ok = issue(ul, ul * a.ka + j, task, j == j0);
+        last_issue[st] = i;
       }
-      *((volatile int*)sm.hits_done) = 1;  // the late retriever warps may start
-      // 2) retrieved pages, in miss-list order, each once its copy is published
-      while (ok) {
-        const int m = atomicAdd(&a.counters[kCtrTaskMisses], 1);
-        if (m >= n_miss) break;
-        if (*abort_flag) { ok = false; break; }
-        if (!wait_flag(a.ready + m, tag, true)) { ok = false; break; }
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // the TMA reads what the generic stores wrote
-        int att = a.miss_att[m];
-        if (att < 0 || att >= U * a.ka) {  // never expected
-          atomicOr(a.err, kErrIndex);
-          att = 0;
-        }
-        const int ul = att / a.ka;
-        ok = issue(ul, att, U * a.n_chunks + att, true);
-      }
-      if (ok) {
-        // sentinel: tells the consumers that no task follows
-        const int st = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u)) {
-          sm.meta[st].part = -1;
-          mbar_arrive(smem_u32(&sm.full[st]));
-        } else {
-          ok = false;
-        }
-      }
-      if (!ok) {
-        atomicOr(a.err, kErrTimeout);
-        *abort_flag = 1;
-        // drain the copies already issued before leaving (bounded)
-        for (int m = max(0, i - kStages); m < i; ++m)
-          (void)mbar_wait(smem_u32(&sm.full[m % kStages]), (uint32_t)(m / kStages) & 1u);
-      }
-      *((volatile int*)sm.hits_done) = 1;  // also on the abort path: nobody waits for it in vain
+    }
+    if (!in_miss) leave_hits();
+    if (lane == 0 && !ok) {
+      atomicOr(a.err, kErrTimeout);
+      *abort_flag = 1;
+      *((volatile int*)sm.hits_done) = 1;  // nobody waits for it in vain
+      // drain the copies already issued before leaving (bounded)
+#pragma unroll
+      for (int st = 0; st < kStages; ++st)
+        if (last_issue[st] >= 0) (void)mbar_wait(smem_u32(&sm.full[st]), (uint32_t)(last_issue[st] / kStages) & 1u);
     }
   } else {
     // ------------------------------ consumers ------------------------------
-    const int w = warp;               // tokens 16w .. 16w+15 of every page
+    const int grp = warp / kCWarps;   // consumer group: stage indices grp, grp + NG, ...
+    const int w = warp % kCWarps;     // tokens 16w .. 16w+15 of every page
     const int t0 = 16 * w;
     const int mi = lane >> 3, ri = lane & 7;
     const int g4 = lane >> 2, q4 = lane & 3;
     const int tokA = t0 + ri + ((mi & 1) << 3);   // K rows feeding the A operand
     const int tokV = t0 + ri + ((mi >> 1) << 3);  // V rows feeding the transposed A operand
-    float* mw = sm.merge + w * kMergeFloats;
+    const uint32_t mrg0 = smem_u32(&sm.mrg[2 * grp]), mrg1 = smem_u32(&sm.mrg[2 * grp + 1]);
 
     uint32_t qb[NT][8][2];
     float o[8][NT][4];
     float mrow[NT][2], lrow[NT][2];
-    int cur = -1;
     uint32_t mph = 0;
-    int i = 0;
+    int i = grp;
 
     for (;;) {
       const int st = i % kStages;
@@ -478,69 +577,9 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
         break;
       }
       const StageMeta m = sm.meta[st];
+      if (m.part < 0) break;  // the group's sentinel
       uint8_t* stage = sm.ring + (size_t)st * kStageBytes;
-      if (m.part != cur || m.part < 0) {
-        if (cur >= 0) {
-          // ---- finalize the previous task: merge the four warps, write partials ----
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float l = lrow[nt][e];
-              l += __shfl_xor_sync(0xffffffffu, l, 4);
-              l += __shfl_xor_sync(0xffffffffu, l, 8);
-              l += __shfl_xor_sync(0xffffffffu, l, 16);
-              const int hh = 8 * nt + 2 * q4 + e;
-#pragma unroll
-              for (int md = 0; md < 8; ++md) {
-                mw[hh * kMergeRow + 16 * md + g4] = o[md][nt][e];
-                mw[hh * kMergeRow + 16 * md + g4 + 8] = o[md][nt][2 + e];
-              }
-              if (g4 == 0) {
-                mw[16 * kMergeRow + hh] = mrow[nt][e];
-                mw[16 * kMergeRow + 16 + hh] = l;
-              }
-            }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sm.mrg[0]));
-          if (!mbar_wait(smem_u32(&sm.mrg[0]), mph)) {
-            atomicOr(a.err, kErrTimeout);
-            *abort_flag = 1;
-            break;
-          }
-          const int d = w * 32 + lane;  // 0..127
-          for (int g = 0; g < a.G; ++g) {
-            float M = -INFINITY;
-#pragma unroll
-            for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, sm.merge[ww * kMergeFloats + 16 * kMergeRow + g]);
-            float L = 0.f, acc = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-              for (int ww = 0; ww < kCWarps; ++ww) {
-                const float* src = sm.merge + ww * kMergeFloats;
-                const float sc = exp2f(src[16 * kMergeRow + g] - M);
-                L = fmaf(sc, src[16 * kMergeRow + 16 + g], L);
-                acc = fmaf(sc, src[g * kMergeRow + d], acc);
-              }
-            }
-            float* part = a.partials + ((int64_t)cur * a.G + g) * kPartialStride;
-            part[4 + d] = acc;
-            if (d == 0) {
-              part[0] = M;
-              part[1] = L;
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sm.mrg[1]));
-          if (!mbar_wait(smem_u32(&sm.mrg[1]), mph)) {
-            atomicOr(a.err, kErrTimeout);
-            *abort_flag = 1;
-            break;
-          }
-          mph ^= 1u;
-        }
-        if (m.part < 0) break;
-        cur = m.part;
+      if (m.first) {
         // query rows of the unit, brought with the task's first page: B operand fragments
         const uint8_t* qs = stage + kPageBytes;
 #pragma unroll
@@ -618,9 +657,70 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
           mma_bf16(o[md][nt], af, bl[nt][0], bl[nt][1]);
         }
       }
+      if (m.last) {
+        // ---- the task's last page: merge the group's four warps inside this stage ----
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mrg0);
+        if (!mbar_wait(mrg0, mph)) {  // every warp of the group is done reading the page
+          atomicOr(a.err, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        float* gmerge = reinterpret_cast<float*>(stage);
+        float* mw = gmerge + w * kMergeFloats;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float l = lrow[nt][e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int hh = 8 * nt + 2 * q4 + e;
+#pragma unroll
+            for (int md = 0; md < 8; ++md) {
+              mw[hh * kMergeRow + 16 * md + g4] = o[md][nt][e];
+              mw[hh * kMergeRow + 16 * md + g4 + 8] = o[md][nt][2 + e];
+            }
+            if (g4 == 0) {
+              mw[16 * kMergeRow + hh] = mrow[nt][e];
+              mw[16 * kMergeRow + 16 + hh] = l;
+            }
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mrg1);
+        if (!mbar_wait(mrg1, mph)) {
+          atomicOr(a.err, kErrTimeout);
+          *abort_flag = 1;
+          break;
+        }
+        mph ^= 1u;
+        const int d = w * 32 + lane;  // 0..127
+        for (int g = 0; g < a.G; ++g) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int ww = 0; ww < kCWarps; ++ww) M = fmaxf(M, gmerge[ww * kMergeFloats + 16 * kMergeRow + g]);
+          float L = 0.f, acc = 0.f;
+          if (M != -INFINITY) {
+#pragma unroll
+            for (int ww = 0; ww < kCWarps; ++ww) {
+              const float* src = gmerge + ww * kMergeFloats;
+              const float sc = exp2f(src[16 * kMergeRow + g] - M);
+              L = fmaf(sc, src[16 * kMergeRow + 16 + g], L);
+              acc = fmaf(sc, src[g * kMergeRow + d], acc);
+            }
+          }
+          float* part = a.partials + ((int64_t)m.part * a.G + g) * kPartialStride;
+          part[4 + d] = acc;
+          if (d == 0) {
+            part[0] = M;
+            part[1] = L;
+          }
+        }
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));
-      ++i;
+      if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));  // the group's four warps free the stage
+      i += NG;
     }
 
   }
@@ -644,9 +744,9 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
     }
   }
   __syncthreads();
-  if (warp >= kCWarps) return;
+  if (warp >= NC) return;
   const int U = a.B * a.Hkv;
-  for (int ul = blockIdx.x; ul < U; ul += gridDim.x) combine_unit(a, ul, warp, lane);
+  for (int ul = blockIdx.x; ul < U; ul += gridDim.x) combine_unit(a, ul, warp, NC, lane);
 }
 
 }  // namespace

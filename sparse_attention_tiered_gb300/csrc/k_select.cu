@@ -108,6 +108,9 @@ struct SelSmem {
   int32_t* dirs;      // [D]
   uint32_t* whist;    // [kSelWarps][256]
   uint8_t* mand;      // [cap]
+  int64_t* msrc;      // [k] host page of the unit's r-th miss (copy in this kernel)
+  int64_t* mdst;      // [k] pool page of the unit's r-th miss
+  int32_t* midx;      // [k] miss-list entry of the unit's r-th miss, -1 = none
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -130,6 +133,9 @@ __host__ __device__ inline size_t sel_smem_layout(int P_max, int cap, int k, int
   uint8_t* dirs = take(sizeof(int32_t) * (D > 0 ? D : 1));
   uint8_t* wh = take(sizeof(uint32_t) * kSelWarps * 256);
   uint8_t* mand = take((size_t)cap);
+  uint8_t* msrc = take(sizeof(int64_t) * k);
+  uint8_t* mdst = take(sizeof(int64_t) * k);
+  uint8_t* midx = take(sizeof(int32_t) * k);
   if (s) {
     s->keys = (uint32_t*)keys;
     s->sp = (int32_t*)sp;
@@ -142,6 +148,9 @@ __host__ __device__ inline size_t sel_smem_layout(int P_max, int cap, int k, int
     s->dirs = (int32_t*)dirs;
     s->whist = (uint32_t*)wh;
     s->mand = mand;
+    s->msrc = (int64_t*)msrc;
+    s->mdst = (int64_t*)mdst;
+    s->midx = (int32_t*)midx;
   }
   return off;
 }
@@ -414,6 +423,7 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
     sm.mand[s] = 0;
   }
   for (int d = tid; d < a.D; d += NT) sm.dirs[d] = a.dir[unit * a.D + d];
+  for (int j = tid; j < k; j += NT) sm.midx[j] = -1;
   if (tid == 0) {
     s_cnt_hits = 0;
     s_cnt_res = 0;
@@ -584,9 +594,18 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       atomicOr(a.err, kErrIndex);
       continue;
     }
-    a.miss_src[idx] = host_page_index(a, b, h, p);
-    a.miss_dst[idx] = unit * cap + s;
+    const int64_t src = host_page_index(a, b, h, p), dst = unit * cap + s;
+    a.miss_src[idx] = src;
+    a.miss_dst[idx] = dst;
     a.miss_att[idx] = ul * a.ka + hits + has_tail + rank;  // misses follow the hits and the tail
+    a.miss_valid[idx] = (p == P - 1) ? a.ntok_b[b] - p * kPart : kPart;
+    if (src >= 0 && src < a.host_pages && dst >= 0 && dst < a.pool_slots) {
+      sm.msrc[rank] = src;
+      sm.mdst[rank] = dst;
+      sm.midx[rank] = idx;
+    } else {
+      atomicOr(a.err, kErrIndex);  // never expected: the page is not copied
+    }
   }
   group_sync<NT>();
 
@@ -635,6 +654,37 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
     if (s_evicted) atomicAdd(&a.stats[kStatEvictions], (unsigned long long)s_evicted);
     if (demand > 0) atomicAdd(&a.stats[kStatLruRounds], 1ull);
     if (keff) atomicAdd(&a.stats[kStatSelected], (unsigned long long)keff);
+  }
+
+  // ---------------- Retrieve in this kernel (retrieve_in_select) ----------------
+  // The group copies the unit's missing pages host -> HBM right after managing the
+  // unit (while other units are still being selected), then publishes each page's
+  // ready flag; the attend kernel then finds every page resident.
+  if (a.retrieve_in_select && misses > 0) {
+    group_sync<NT>();
+    constexpr int kPV = kPageElems / 8;  // 16-byte vectors per page (2048)
+    constexpr int kU = 8;                // vectors in flight per thread
+    const int nvec = misses * kPV;
+    const uint4* hs = reinterpret_cast<const uint4*>(a.host_store);
+    uint4* pool = reinterpret_cast<uint4*>(a.pool);
+    for (int blk = 0; blk < nvec; blk += NT * kU) {
+      uint4 r[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = blk + u * NT + tid;
+        if (e < nvec && sm.midx[e / kPV] >= 0) r[u] = __ldcs(hs + sm.msrc[e / kPV] * kPV + (e % kPV));
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = blk + u * NT + tid;
+        if (e < nvec && sm.midx[e / kPV] >= 0) pool[sm.mdst[e / kPV] * kPV + (e % kPV)] = r[u];
+      }
+    }
+    __threadfence();
+    group_sync<NT>();
+    for (int r = tid; r < misses; r += NT)
+      if (sm.midx[r] >= 0)
+        asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(a.ready + sm.midx[r]), "r"(t + 1) : "memory");
   }
 }
 

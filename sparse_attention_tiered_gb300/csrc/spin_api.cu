@@ -60,6 +60,7 @@ struct LayerBuf {
   int64_t* miss_src = nullptr;
   int64_t* miss_dst = nullptr;
   int32_t* miss_att = nullptr;
+  int32_t* miss_valid = nullptr;
   int32_t* ready = nullptr;
   int32_t* att_slot = nullptr;
   int32_t* att_valid = nullptr;
@@ -91,6 +92,7 @@ struct spin_ctx {
   int select_group = 0;  // SPIN_SELECT_GROUP: threads of the top-k/manager group (0 = by unit size)
   int retr_warps = 2;  // SPIN_RETRIEVE_WARPS (1..8): retriever warps per attend CTA from its start
   int retr_late = 8;   // SPIN_RETRIEVE_LATE (0..8): retriever warps that join after the CTA's resident pages
+  int retrieve_in_select = 0;  // SPIN_RETRIEVE_IN_SELECT: misses copied by the select/manage kernel
   std::vector<int64_t> ctx_len;
   std::vector<int32_t> P_b, ntok_b;  // fixed mode: partitions and tokens of each request
   std::vector<int32_t> pstride_b;    // host-store pages per KV head of each request (its partition capacity)
@@ -335,6 +337,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.S = (int32_t)c->S;
   a.retr_warps = c->retr_warps;
   a.retr_late = c->retr_late;
+  a.retrieve_in_select = c->retrieve_in_select;
   a.select_group = c->select_group;
   a.ka = c->ka;
   a.P_b = c->d_P_lb + (int64_t)l * c->B;
@@ -364,6 +367,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.miss_src = lb.miss_src;
   a.miss_dst = lb.miss_dst;
   a.miss_att = lb.miss_att;
+  a.miss_valid = lb.miss_valid;
   a.ready = lb.ready;
   a.att_slot = lb.att_slot;
   a.att_valid = lb.att_valid;
@@ -532,7 +536,8 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     const int v = atoi(env);
     if (v >= 0 && v <= 8) c->retr_late = v;
   }
-  if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = c->retr_late = 0;  // nothing publishes a page
+  if (const char* env = getenv("SPIN_RETRIEVE_IN_SELECT")) c->retrieve_in_select = atoi(env) != 0;
+  if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = c->retr_late = c->retrieve_in_select = 0;
   if (const char* env = getenv("SPIN_SELECT_GROUP")) c->select_group = atoi(env);  // 0 auto, 32, 512
 
   // attention work split: pages per task
@@ -556,6 +561,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     ALLOC(lb.att_valid, Ul * c->ka, "allocating layer scratch");
     ALLOC(lb.n_hit, Ul, "allocating layer scratch");
     ALLOC(lb.miss_att, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.miss_valid, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.ready, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.counters, kNumCtr, "allocating layer scratch");
     ALLOC(lb.partials, Ul * (c->n_chunks + c->ka) * c->G * kPartialStride, "allocating layer scratch");

@@ -35,6 +35,7 @@ struct LayerArgs {
   int32_t ka;                // attention entries per unit: k, plus one for the tail page in tail mode
   int32_t retr_warps;        // retriever warps active per CTA of the attend kernel from its start
   int32_t retr_late;         // further retriever warps that join once the CTA's resident pages are issued
+  int32_t retrieve_in_select;// 1: the select/manage kernel copies each unit's misses; the attend kernel only reads HBM
   int32_t select_group;      // 0 = choose by unit size, else 32 or 512 threads for top-k + manager
   const int32_t* P_b;        // [B] selectable partitions of request b in this layer (tail mode: complete ones)
   const int32_t* ntok_b;     // [B] tokens held by those partitions
@@ -63,6 +64,7 @@ struct LayerArgs {
   int64_t* miss_src;         // [U_l * k] host page index of each miss (miss list, append order)
   int64_t* miss_dst;         // [U_l * k] pool slot index of each miss
   int32_t* miss_att;         // [U_l * k] ul * ka + attention position of each miss
+  int32_t* miss_valid;       // [U_l * k] valid tokens of each miss's page
   int32_t* ready;            // [U_l * k] per miss-list entry: step tag once its page is in HBM
   int32_t* att_slot;         // [U_l][ka] slots in attention order: hits, the tail (slot == cap), then misses
   int32_t* att_valid;        // [U_l][ka] valid tokens of those pages
