@@ -246,61 +246,65 @@ __device__ __forceinline__ uint32_t swz(int r, int cd) {
 }
 
 // ---------------------------------------------------------------------------
-// Combine of one unit: out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c
-// over the unit's partials (its hit tasks and its retrieved pages). Consumer
-// warp w of nw takes heads w, w+nw, ...; four columns per lane. One pass: the lanes
-// fetch the (m, l) of up to 32 partials at a time in parallel, the max and the
-// sum are warp reductions, and the accumulator loads are independent.
+// Combine of one (unit, query head): out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c
+// over the unit's partials (its hit tasks and its retrieved pages), by one warp, four
+// columns per lane. The lanes fetch the (m, l) of up to 32 partials at once; the
+// accumulator rows are loaded eight at a time before they are used, so a head costs
+// a few round trips to L2 whatever the number of partials.
 // ---------------------------------------------------------------------------
-__device__ void combine_unit(const LayerArgs& a, int ul, int w, int nw, int lane) {
+__device__ void combine_head(const LayerArgs& a, int ul, int g, int lane) {
   const int b = ul / a.Hkv, h = ul - b * a.Hkv;
   const int has_tail = (a.tail_n != nullptr && a.tail_n[b] > 0) ? 1 : 0;
   const int keff = a.keff[ul] + has_tail, nh = a.n_hit[ul];  // attended pages; resident ones (tail included)
   const int nc = (nh + a.ppt - 1) / a.ppt;
   const int U = a.B * a.Hkv;
   const int n = nc + (keff - nh);
-  for (int g = w; g < a.G; g += nw) {
-    float4* out = reinterpret_cast<float4*>(a.out + ((int64_t)b * a.Hq + (int64_t)h * a.G + g) * kD);
-    // partial slots: hit tasks ul * n_chunks + c (c < nc), retrieved pages U * n_chunks + ul * ka + j (nh <= j < keff)
-    auto part_ptr = [&](int i) -> const float* {
-      const int64_t slot =
-          i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.ka + nh + (i - nc);
-      return a.partials + (slot * a.G + g) * kPartialStride;
-    };
-    float M = -INFINITY;
-    for (int i0 = 0; i0 < n; i0 += 32)
-      if (i0 + lane < n) M = fmaxf(M, __ldcg(part_ptr(i0 + lane)));
+  float4* out = reinterpret_cast<float4*>(a.out + ((int64_t)b * a.Hq + (int64_t)h * a.G + g) * kD);
+  // partial slots: hit tasks ul * n_chunks + c (c < nc), retrieved pages U * n_chunks + ul * ka + j (nh <= j < keff)
+  auto part_ptr = [&](int i) -> const float* {
+    const int64_t slot =
+        i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.ka + nh + (i - nc);
+    return a.partials + (slot * a.G + g) * kPartialStride;
+  };
+  float M = -INFINITY;
+  for (int i0 = 0; i0 < n; i0 += 32)
+    if (i0 + lane < n) M = fmaxf(M, __ldcg(part_ptr(i0 + lane)));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-    if (M != -INFINITY) {
-      for (int i0 = 0; i0 < n; i0 += 32) {
-        float sc_l = 0.f, l_l = 0.f;
-        if (i0 + lane < n) {
-          const float* pp = part_ptr(i0 + lane);
-          sc_l = exp2f(__ldcg(pp) - M);
-          l_l = __ldcg(pp + 1);
-        }
-        float ls = sc_l * l_l;
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int i0 = 0; i0 < n; i0 += 32) {
+      float sc_l = 0.f, l_l = 0.f;
+      if (i0 + lane < n) {
+        const float* pp = part_ptr(i0 + lane);
+        sc_l = exp2f(__ldcg(pp) - M);
+        l_l = __ldcg(pp + 1);
+      }
+      float ls = sc_l * l_l;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-        L += ls;
-        const int cnt = min(32, n - i0);
-#pragma unroll 4
-        for (int i = 0; i < cnt; ++i) {
-          const float sc = __shfl_sync(0xffffffffu, sc_l, i);
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(part_ptr(i0 + i) + 4) + lane);
-          acc.x = fmaf(sc, v.x, acc.x);
-          acc.y = fmaf(sc, v.y, acc.y);
-          acc.z = fmaf(sc, v.z, acc.z);
-          acc.w = fmaf(sc, v.w, acc.w);
+      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      L += ls;
+      const int cnt = min(32, n - i0);
+      for (int i1 = 0; i1 < cnt; i1 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = (i1 + u < cnt) ? __ldcg(reinterpret_cast<const float4*>(part_ptr(i0 + i1 + u) + 4) + lane)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float sc = __shfl_sync(0xffffffffu, sc_l, (i1 + u) & 31);  // 0 past cnt: its v is 0 too
+          acc.x = fmaf(sc, v[u].x, acc.x);
+          acc.y = fmaf(sc, v[u].y, acc.y);
+          acc.z = fmaf(sc, v[u].z, acc.z);
+          acc.w = fmaf(sc, v[u].w, acc.w);
         }
       }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    out[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  out[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -745,8 +749,9 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
   }
   __syncthreads();
   if (warp >= NC) return;
-  const int U = a.B * a.Hkv;
-  for (int ul = blockIdx.x; ul < U; ul += gridDim.x) combine_unit(a, ul, warp, NC, lane);
+  // (unit, head) pairs spread over every consumer warp of the grid
+  const int pairs = a.B * a.Hkv * a.G;
+  for (int p = blockIdx.x * NC + warp; p < pairs; p += gridDim.x * NC) combine_head(a, p / a.G, p % a.G, lane);
 }
 
 }  // namespace
