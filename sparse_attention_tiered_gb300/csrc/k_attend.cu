@@ -9,12 +9,16 @@
 // One cooperative persistent kernel per layer step does both, one CTA per SM:
 //   * retriever warps walk the step's miss list (host page -> HBM slot, 16-byte
 //     zero-copy loads over the host link), and publish each copied page with a
-//     release store of the step tag into its ready flag;
-//   * a producer warp (one elected lane) streams pages through TMA into a 4-stage
-//     shared-memory ring guarded by mbarriers: first the resident pages (hits) in
-//     tasks of up to `ppt` pages of one unit, then the retrieved pages in miss-list
-//     order, each after an acquire of its ready flag;
-//   * four consumer warps run the attention math on every staged page.
+//     release store of the step tag into its ready flag; two start at once, the
+//     others join when the CTA's resident pages have all been issued;
+//   * two consumer groups of four warps take alternate stages of a 6-stage
+//     shared-memory ring guarded by mbarriers, so two pages are in the math at once;
+//   * each group has a producer warp that stages its pages through TMA: first
+//     resident pages (hits) in tasks of up to `ppt` pages of one unit, then
+//     retrieved pages in miss-list order, each after an acquire of its ready flag.
+//     Nothing on the issue path waits for a fresh global load: tasks are claimed
+//     two ahead, the next task's page descriptors sit in the lanes' registers, and a
+//     retrieved page's miss-list entry is loaded before its flag is awaited.
 // So the attention over the hits (HBM bound) hides under the retrieval (host-link
 // bound) and each retrieved page is attended as soon as it lands (and from L2).
 //
@@ -30,10 +34,11 @@
 //   online softmax per head in fp32 (base-2 exponent, scale log2(e)/sqrt(128))
 //   O^T[128][8 heads] += V^T P             P transposed in registers (movmatrix) and
 //                                          split into bf16 hi + lo parts, two mma each
-// At the end of a task the four warps merge (m, l, O) in shared memory and write
-// one partial (m, l, acc[128]) per query head. When every CTA has finished its
-// pages (an arrival counter; all CTAs are co-resident under the cooperative
-// launch), the consumer warps combine the partials of each unit into the output:
+// At the end of a task the group's four warps merge (m, l, O) in the stage of the
+// task's last page and write one partial (m, l, acc[128]) per query head. When
+// every CTA has finished its pages (an arrival counter; all CTAs are co-resident
+// under the cooperative launch), every consumer warp of the grid combines
+// (unit, query head) pairs of partials into the output:
 //   out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
 //
 // Every wait (mbarrier, ready flag, arrival counter) is bounded in time; a wait
