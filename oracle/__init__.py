@@ -93,6 +93,8 @@ def _bind(L):
     L.oracle_unit_create_tail.argtypes = [i32, i32, i32]
     L.oracle_unit_create_tail.restype = vp
     L.oracle_unit_grow.argtypes = [vp]
+    L.oracle_unit_set_budget.argtypes = [vp, i32]
+    L.oracle_unit_set_budget.restype = i32
     L.oracle_unit_grow.restype = i32
     L.oracle_attend_tail.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, vp]
     return L
@@ -192,6 +194,10 @@ class Unit:
 
     def resolve(self, p: int) -> int:
         return self.lib.oracle_resolve(self.h, p)
+
+    def set_budget(self, pages: int):
+        """Buffer elasticity: the unit may keep at most `pages` resident from the next step on."""
+        assert self.lib.oracle_unit_set_budget(self.h, pages) == 0, "budget outside [1, cap]"
 
     def live_segments(self) -> int:
         return self.lib.oracle_live_segments(self.h)
@@ -321,6 +327,9 @@ class TailUnit:
 
     def live_segments(self) -> int:
         return self.lib.oracle_live_segments(self.h)
+
+    def set_budget(self, pages: int):
+        assert self.lib.oracle_unit_set_budget(self.h, pages) == 0, "budget outside [1, cap]"
 
     def manage(self, sel: np.ndarray, t: int):
         sel = np.ascontiguousarray(sel, np.int32)

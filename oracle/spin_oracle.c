@@ -146,6 +146,7 @@ typedef struct oracle_unit {
   int32_t P_cap;       /* partitions the unit may grow to (tail mode), else P */
   int32_t ntok;        /* valid tokens (last partition may be short) */
   int32_t cap;         /* resident capacity in pages (mandatory + buffer) */
+  int32_t budget;      /* pages the unit may keep resident now, k <= budget <= cap (buffer elasticity) */
   int32_t D;           /* directory entries = ceil(P / 64) */
   int32_t S;           /* segments in this unit's pool */
   int32_t* dir;        /* [D] segment id or -1 */
@@ -161,6 +162,7 @@ oracle_unit* oracle_unit_create(int32_t ntok, int32_t cap) {
   u->ntok = ntok;
   u->P = (ntok + OPART - 1) / OPART;
   u->cap = cap;
+  u->budget = cap;
   u->P_cap = u->P;
   u->D = (u->P + OSEG - 1) / OSEG;
   u->S = u->D < cap ? u->D : cap;
@@ -192,6 +194,19 @@ oracle_unit* oracle_unit_create_tail(int32_t P_complete, int32_t P_capacity, int
   u->P = P_complete;
   u->ntok = P_complete * OPART;
   return u;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Buffer elasticity ([XT] §2: the buffer part of a request's pages is resized */
+/* by the scheduler with load; [GS] §2B). reading: the budget bounds the       */
+/* resident pages; the manager counts free pages against it, so after a shrink */
+/* the next step's demand includes the excess and the bucketed LRU reclaims    */
+/* down to the budget. The budget never drops below the mandatory pages (k).   */
+/* ------------------------------------------------------------------------- */
+int32_t oracle_unit_set_budget(oracle_unit* u, int32_t pages) {
+  if (pages < 1 || pages > u->cap) return -1;
+  u->budget = pages;
+  return 0;
 }
 
 int32_t oracle_unit_grow(oracle_unit* u) {
@@ -270,7 +285,8 @@ typedef struct oracle_manage_out {
 /*     one histogram pass, then whole buckets are reclaimed from the oldest     */
 /*     upward until the reclaimed count covers the demand;                      */
 /*  4. each miss gets a free page and its bytes are copied from the host page. */
-/* readings: capacity = mandatory + buffer pages; bucket of a page =           */
+/* readings: capacity = mandatory + buffer pages, free pages counted against  */
+/* the unit's current budget (buffer elasticity); bucket of a page =            */
 /* 63 - min(63, t - last_use) (0 = oldest); misses in ascending partition      */
 /* order take free slots in ascending slot order.                              */
 /* sel_slot[j], sel_hit[j] describe sel[j]; victims[] gets the evicted         */
@@ -295,7 +311,7 @@ void oracle_manage(oracle_unit* u, const int32_t* sel, int32_t keff, int32_t t, 
   }
   out->misses = keff - out->hits;
   for (int32_t s = 0; s < u->cap; ++s) out->resident_before += u->slot_part[s] >= 0;
-  out->free_before = u->cap - out->resident_before;
+  out->free_before = u->budget - out->resident_before; /* negative after a shrink */
   out->demand = out->misses - out->free_before;
 
   /* 3: bucketed LRU */

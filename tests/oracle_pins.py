@@ -178,13 +178,17 @@ def _bucket(t, last):
     return 63 - min(63, t - last)
 
 
-def _run_invariants(lib, ntok, cap, k, steps, seed, locality):
+def _run_invariants(lib, ntok, cap, k, steps, seed, locality, budgets=None):
     rng = np.random.default_rng(seed)
     kb, vb = rand_kv(rng, ntok)
     u = O.Unit(ntok, cap=cap, k_bits=kb, v_bits=vb, lib=lib)
     P = u.P
+    budget = cap
     prev = np.sort(rng.choice(P, size=min(k, P), replace=False))
     for t in range(steps):
+        if budgets and t in budgets:
+            budget = budgets[t]
+            u.set_budget(budget)
         # a selection that keeps part of the previous one (temporal locality)
         keep = prev[rng.random(prev.size) < locality]
         fresh = rng.choice(P, size=min(k, P), replace=False)
@@ -197,7 +201,7 @@ def _run_invariants(lib, ntok, cap, k, steps, seed, locality):
         # hits are exactly the selected partitions resident before the step
         assert [bool(int(p) in resident0) for p in sel] == list(sel_hit)
         assert mo.hits == int(sel_hit.sum()) and mo.misses == len(sel) - mo.hits
-        free0 = cap - len(resident0)
+        free0 = budget - len(resident0)
         demand = mo.misses - free0
         assert mo.demand == demand
         mand = set(int(p) for p in sel)
@@ -228,9 +232,9 @@ def _run_invariants(lib, ntok, cap, k, steps, seed, locality):
         free_after_evict = sorted(s for s in range(cap) if sp0[s] < 0 or int(sp0[s]) in set(map(int, victims)))
         miss_slots = [int(s) for s, h in zip(sel_slot, sel_hit) if not h]
         assert miss_slots == free_after_evict[:len(miss_slots)]
-        # resident <= cap; page table round trip; live segments = occupied 64-ranges
+        # resident <= budget <= cap; page table round trip; live segments = occupied 64-ranges
         res = [int(p) for p in sp1 if p >= 0]
-        assert len(res) <= cap and len(set(res)) == len(res)
+        assert len(res) <= budget <= cap and len(set(res)) == len(res)
         for p in range(P):
             s = rs1[p]
             if s >= 0:
@@ -256,6 +260,39 @@ def check_lru_invariants(lib):
     _run_invariants(lib, ntok=300 * 64, cap=4, k=4, steps=80, seed=7, locality=0.5)     # no buffering
     _run_invariants(lib, ntok=40 * 64, cap=40, k=8, steps=90, seed=8, locality=0.8)      # cap = P
     _run_invariants(lib, ntok=5 * 64, cap=10, k=8, steps=20, seed=9, locality=0.3)       # k > P
+    # buffer elasticity: the budget shrinks to the mandatory pages, grows, shrinks again
+    _run_invariants(lib, ntok=300 * 64, cap=20, k=4, steps=120, seed=11, locality=0.7,
+                    budgets={30: 4, 50: 20, 80: 9, 100: 5})
+
+
+def check_budget_hand_trace(lib):
+    """Buffer elasticity, hand traced: cap 6, k 2.
+
+    t=0..2 select {0,1}, {2,3}, {4,5}: six misses fill slots 0..5 (last use 0,0,1,1,2,2).
+    budget -> 3.
+    t=3 sel {5,10}: hit 5 (slot 5, stamped 3), miss 10. resident 6 > budget 3: free -3,
+                    demand 1 + 3 = 4. Non-mandatory buckets: 0,1 age 3 -> 60; 2,3 age 2
+                    -> 61; 4 age 1 -> 62. Cumulative 2, 4: cutoff 61 reclaims 0,1,2,3
+                    (slots 0..3); 10 takes slot 0. Resident {10,4,5} = 3 pages.
+    budget -> 6.
+    t=4 sel {6,7}: two misses, resident 3, free 3, demand -1: no eviction; slots 1, 2.
+    """
+    ntok = 20 * 64
+    rng = np.random.default_rng(13)
+    kb, vb = rand_kv(rng, ntok)
+    u = O.Unit(ntok, cap=6, k_bits=kb, v_bits=vb, lib=lib)
+    for t, sel in enumerate(([0, 1], [2, 3], [4, 5])):
+        ss, hit, vic, mo = u.manage(np.array(sel, np.int32), t)
+        assert mo.evicted == 0
+    u.set_budget(3)
+    ss, hit, vic, mo = u.manage(np.array([5, 10], np.int32), 3)
+    assert list(hit) == [True, False] and mo.free_before == -3 and mo.demand == 4 and mo.cutoff == 61
+    assert sorted(vic.tolist()) == [0, 1, 2, 3] and list(ss) == [5, 0]
+    sp, lu, rs = u.export()
+    assert list(sp) == [10, -1, -1, -1, 4, 5] and lu[0] == 3 and lu[5] == 3
+    u.set_budget(6)
+    ss, hit, vic, mo = u.manage(np.array([6, 7], np.int32), 4)
+    assert mo.demand == -1 and mo.evicted == 0 and list(ss) == [1, 2]
 
 
 def check_lru_hand_trace(lib):
@@ -340,4 +377,5 @@ def check_append_tail(lib):
 
 
 ALL_CHECKS = [check_dense_attention, check_attention_closed_forms, check_scores_probe, check_topk_bruteforce,
-              check_index, check_lru_invariants, check_lru_hand_trace, check_step_consistency, check_append_tail]
+              check_index, check_lru_invariants, check_lru_hand_trace, check_budget_hand_trace,
+              check_step_consistency, check_append_tail]

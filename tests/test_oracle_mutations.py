@@ -45,6 +45,8 @@ MUTANTS = {
     "miss_copies_wrong_page": ("host_pages + (int64_t)p * OPAGE_ELEMS,", "host_pages + (int64_t)(p / 2) * OPAGE_ELEMS,"),
     "append_tail_not_attended": ("        valid = tail_n;\n        K = tail_kv;", "        valid = 0;\n        K = tail_kv;"),
     "append_no_growth": ("  u->P += 1;\n  u->ntok = u->P * OPART;", "  u->ntok = u->P * OPART;"),
+    "budget_ignored": ("out->free_before = u->budget - out->resident_before;",
+                       "out->free_before = u->cap - out->resident_before;"),
     "offload_drops_tail_token": ("for (int64_t t = 0; t < ntok; ++t) {\n    int64_t p = t / OPART",
                                  "for (int64_t t = 0; t < ntok - 1; ++t) {\n    int64_t p = t / OPART"),
 }
