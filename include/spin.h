@@ -182,6 +182,17 @@ int spin_index_offload(spin_ctx* ctx, int32_t b, int32_t layer, const uint16_t* 
  * that step's spin_decode_step, which then attends it. */
 int spin_append_kv(spin_ctx* ctx, int32_t layer, const uint16_t* k_new, const uint16_t* v_new, spin_stream_t stream);
 
+/* Buffer elasticity ([XT] §2: the buffer part of a request's pages is resized by
+ * the scheduler with load; [GS] §2B). Sets the resident budget of request b to
+ * `pages` per unit (every layer and KV head of the request), topk <= pages <=
+ * buf_mult * topk; spin_create starts every request at buf_mult * topk. The
+ * manager counts free pages against the budget, so after a shrink the next step's
+ * demand includes the excess and the bucketed LRU reclaims down to the budget;
+ * after a growth the extra pages fill on later misses. Takes effect for the decode
+ * steps enqueued on `stream` after it (asynchronous; order it on the stream of the
+ * steps). Returns SPIN_ERR_INVALID for b or pages out of range. */
+int spin_set_buffer(spin_ctx* ctx, int32_t b, int32_t pages, spin_stream_t stream);
+
 /* One decode step of one layer for the whole batch ([XT] §2 and Fig 5 steps 1-4,
  * §3; [GS] §2B-C). q: device bf16 [batch][q_heads][128]; out: device fp32
  * [batch][q_heads][128] = softmax(q K_sel^T / sqrt(128)) V_sel over the tokens of

@@ -36,7 +36,7 @@ PAGE_BYTES = 32768
 SPIN_NOALLOC_MAX_SCORES_DEFAULT = 1 << 20  # SPIN_NOALLOC_MAX_SCORES in include/spin.h
 
 # Every symbol include/spin.h declares.
-EXPORTS = ("spin_create", "spin_index_offload", "spin_append_kv", "spin_decode_step", "spin_decode_step_host", "spin_stats",
+EXPORTS = ("spin_create", "spin_index_offload", "spin_append_kv", "spin_set_buffer", "spin_decode_step", "spin_decode_step_host", "spin_stats",
            "spin_debug_export", "spin_debug_read_page", "spin_debug_summaries", "spin_destroy", "spin_last_error",
            "spin_select_noalloc")
 
@@ -115,6 +115,8 @@ def load(build_if_missing: bool = True):
             L.spin_index_offload.restype = ctypes.c_int
             L.spin_append_kv.argtypes = [vp, i32, vp, vp, vp]
             L.spin_append_kv.restype = ctypes.c_int
+            L.spin_set_buffer.argtypes = [vp, i32, i32, vp]
+            L.spin_set_buffer.restype = ctypes.c_int
             L.spin_decode_step.argtypes = [vp, i32, vp, vp, vp]
             L.spin_decode_step.restype = ctypes.c_int
             L.spin_decode_step_host.argtypes = [vp, i32, vp, vp, vp]
@@ -160,6 +162,10 @@ def spin_index_offload(ctx: int, b: int, layer: int, k_ptr: int, v_ptr: int, n_t
 
 def spin_append_kv(ctx: int, layer: int, k_ptr: int, v_ptr: int, stream: int = 0):
     _check(load().spin_append_kv(ctx, layer, k_ptr, v_ptr, stream), ctx)
+
+
+def spin_set_buffer(ctx: int, b: int, pages: int, stream: int = 0):
+    _check(load().spin_set_buffer(ctx, b, pages, stream), ctx)
 
 
 def spin_decode_step(ctx: int, layer: int, q_ptr: int, out_ptr: int, stream: int = 0):

@@ -90,6 +90,11 @@ class SpinContext:
                 self.tail_lb[layer][b] = 0
                 self.P_lb[layer][b] += 1
 
+    # ---- buffer elasticity ----
+    def set_buffer(self, b: int, pages: int, stream: int = 0):
+        """Resident budget of request b: topk <= pages <= buf_mult * topk pages per unit."""
+        B.spin_set_buffer(self.h, b, pages, stream)
+
     # ---- decode ----
     def decode_step(self, layer: int, q_dev, out_dev, stream: int = 0):
         """q_dev: CUDA bf16/int16 [B][Hq][128]; out_dev: CUDA fp32 [B][Hq][128]."""

@@ -301,7 +301,16 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
     }
     __syncthreads();
   } else {
-    for (int p = tid; p < P; p += kSelThreads) sm.keys[p] = float_key(a.scores[(int64_t)ul * a.P_max + p]);
+    // eight independent loads per thread before the stores: one round trip per 4096 keys
+    const float* sc = a.scores + (int64_t)ul * a.P_max;
+    for (int p0 = tid; p0 < P; p0 += 8 * kSelThreads) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = (p0 + u * kSelThreads < P) ? sc[p0 + u * kSelThreads] : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (p0 + u * kSelThreads < P) sm.keys[p0 + u * kSelThreads] = float_key(v[u]);
+    }
   }
 
   __syncthreads();  // keys complete for every thread
@@ -465,7 +474,9 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   // tail mode: the request's tail page is attended after the hits, before the misses
   const int has_tail = (a.tail_n != nullptr && a.tail_n[b] > 0) ? 1 : 0;
   const int resident = s_cnt_res;
-  const int demand = misses - (cap - resident);
+  // free pages are counted against the request's budget (buffer elasticity): after a
+  // shrink the demand includes the excess and the LRU reclaims down to the budget
+  const int demand = misses - (a.budget_b[b] - resident);
 
   // ---------------- 3. bucketed LRU ----------------
   if (demand > 0) {
@@ -758,6 +769,13 @@ cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st) {
   else if (w) select_manage_kernel<32, false><<<grid, kSelThreads, smem, st>>>(a);
   else if (f) select_manage_kernel<kSelThreads, true><<<grid, kSelThreads, smem, st>>>(a);
   else select_manage_kernel<kSelThreads, false><<<grid, kSelThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+__global__ void set_int_kernel(int32_t* p, int32_t v) { *p = v; }
+
+cudaError_t launch_set_int(int32_t* p, int32_t v, cudaStream_t st) {
+  set_int_kernel<<<1, 1, 0, st>>>(p, v);
   return cudaGetLastError();
 }
 

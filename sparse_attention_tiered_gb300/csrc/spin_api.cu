@@ -113,6 +113,7 @@ struct spin_ctx {
   float* d_summ = nullptr;
   int32_t *d_P_lb = nullptr, *d_ntok_lb = nullptr, *d_tail_lb = nullptr;  // [L][B]
   int32_t* d_pstride_b = nullptr;
+  int32_t* d_budget_b = nullptr;  // [B] resident budget per unit of each request
   int64_t* d_poff_b = nullptr;
   int32_t *d_dir = nullptr, *d_seg = nullptr, *d_seg_live = nullptr;
   int32_t* h_seg = nullptr;  // tier split: the segment entries in pinned host memory (d_seg maps it)
@@ -344,6 +345,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.ntok_b = c->d_ntok_lb + (int64_t)l * c->B;
   a.tail_n = c->tail_mode ? c->d_tail_lb + (int64_t)l * c->B : nullptr;
   a.pstride_b = c->d_pstride_b;
+  a.budget_b = c->d_budget_b;
   a.poff_b = c->d_poff_b;
   a.layer_page_base = (int64_t)l * c->pages_per_layer;
   a.unit_base = (int64_t)l * c->B * c->Hkv;
@@ -467,6 +469,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   ALLOC(c->d_ntok_lb, (int64_t)c->L * c->B, "allocating request tables");
   ALLOC(c->d_tail_lb, (int64_t)c->L * c->B, "allocating request tables");
   ALLOC(c->d_pstride_b, c->B, "allocating request tables");
+  ALLOC(c->d_budget_b, c->B, "allocating request tables");
   ALLOC(c->d_poff_b, c->B, "allocating request tables");
   ALLOC(c->d_dir, c->units * c->D, "allocating the directory");
   if (c->flags & SPIN_FLAG_TIER_SPLIT) {
@@ -509,6 +512,11 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   }
   SPIN_CUDA(nullptr, cudaMemcpy(c->d_pstride_b, c->pstride_b.data(), 4 * c->B, cudaMemcpyHostToDevice),
             "uploading tables");
+  {
+    const std::vector<int32_t> budget(c->B, c->cap);
+    SPIN_CUDA(nullptr, cudaMemcpy(c->d_budget_b, budget.data(), 4 * c->B, cudaMemcpyHostToDevice),
+              "uploading tables");
+  }
   SPIN_CUDA(nullptr, cudaMemcpy(c->d_poff_b, c->poff_b.data(), 8 * c->B, cudaMemcpyHostToDevice), "uploading tables");
   if (tail_pages)
     SPIN_CUDA(nullptr, cudaMemset(c->d_pool + slots * kPageElems, 0, (size_t)tail_pages * kPageBytes),
@@ -540,9 +548,11 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = c->retr_late = c->retrieve_in_select = 0;
   if (const char* env = getenv("SPIN_SELECT_GROUP")) c->select_group = atoi(env);  // 0 auto, 32, 512
 
-  // attention work split: pages per task
+  // attention work split: pages per task, about one task per consumer group when pages
+  // are few (each task costs a merge and a partial to combine), at most 8
   const int64_t pages_layer = (int64_t)c->B * c->Hkv * c->k;
-  c->ppt = (int)std::max<int64_t>(1, std::min<int64_t>(8, pages_layer / (4 * std::max(1, c->sm_count))));
+  const int64_t groups = (int64_t)std::max(1, c->sm_count) * (c->G <= 8 ? 2 : 1);
+  c->ppt = (int)std::max<int64_t>(1, std::min<int64_t>(8, (pages_layer + groups - 1) / groups));
   c->n_chunks = (c->ka + c->ppt - 1) / c->ppt;
 
   const int64_t Ul = (int64_t)c->B * c->Hkv;
@@ -772,6 +782,18 @@ int spin_append_kv(spin_ctx* c, int32_t layer, const uint16_t* k_new, const uint
     }
   }
   c->appended += c->B;
+  return SPIN_OK;
+}
+
+int spin_set_buffer(spin_ctx* c, int32_t b, int32_t pages, spin_stream_t stream) {
+  if (!c) return fail(nullptr, SPIN_ERR_INVALID, "ctx is NULL");
+  if (b < 0 || b >= c->B) return fail(c, SPIN_ERR_INVALID, "request %d outside [0, %d)", b, c->B);
+  if (pages < c->k || pages > c->cap)
+    return fail(c, SPIN_ERR_INVALID, "buffer of %d pages outside [topk, buf_mult * topk] = [%d, %d]", pages, c->k,
+                c->cap);
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  SPIN_CUDA(c, launch_set_int(c->d_budget_b + b, pages, static_cast<cudaStream_t>(stream)), "setting the budget");
   return SPIN_OK;
 }
 

@@ -41,6 +41,7 @@ struct LayerArgs {
   const int32_t* ntok_b;     // [B] tokens held by those partitions
   const int32_t* tail_n;     // [B] tokens in the request's tail page (tail mode), else nullptr
   const int32_t* pstride_b;  // [B] host-store pages per KV head of request b (its partition capacity)
+  const int32_t* budget_b;   // [B] resident budget per unit of request b (k <= budget <= cap)
   const int64_t* poff_b;     // [B] sum of pstride over earlier requests
   int64_t layer_page_base;   // first page of this layer in the host store / summaries
   int64_t unit_base;         // first global unit of this layer = layer * B * Hkv
@@ -105,6 +106,8 @@ cudaError_t launch_score(const LayerArgs& a, cudaStream_t st);
 // KV append of one token per request of the layer (tail mode).
 cudaError_t launch_append(const LayerArgs& a, const uint16_t* k_new, const uint16_t* v_new, int32_t* P_b,
                           int32_t* ntok_b, int32_t* tail_n, cudaStream_t st);
+// Writes one int on the device, ordered on the stream (request tables).
+cudaError_t launch_set_int(int32_t* p, int32_t v, cudaStream_t st);
 // Sets the request's layer state (partitions, their tokens, tail tokens) on the device.
 cudaError_t launch_set_request(int32_t* P_b, int32_t* ntok_b, int32_t* tail_n, int32_t P, int32_t ntok,
                                int32_t tail, cudaStream_t st);

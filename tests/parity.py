@@ -118,12 +118,14 @@ class Lockstep:
 
     def __init__(self, w: W.Workload, units: Optional[List[Tuple[int, int, int]]] = None, device: int = 0,
                  flags: int = 0, seg_pool_segments: int = 0, offload_from_device: bool = False,
-                 gen_threads: int = 0, append: int = 0):
+                 gen_threads: int = 0, append: int = 0, budgets=None):
         import torch
         from sparse_attention_tiered_gb300 import SpinContext
         self.torch = torch
         self.w = w
         self.append = append
+        self.budgets = budgets or {}  # step -> [(request, pages)]: buffer elasticity events
+        self.budget_b = [w.cap] * w.B
         self.dev = torch.device(f"cuda:{device}")
         self.units = units if units is not None else [(l, b, h) for l in range(w.L) for b in range(w.B)
                                                       for h in range(w.Hkv)]
@@ -175,6 +177,12 @@ class Lockstep:
         w = self.w
         qb = self.qs.bf16()
         qd = torch.from_numpy(qb.view(np.int16)).to(self.dev)
+        for (b, pages) in self.budgets.get(self.t, []):
+            self.ctx.set_buffer(b, pages)
+            self.budget_b[b] = pages
+            for (l, bb, h), u in self.oracle.items():
+                if bb == b:
+                    u.set_budget(pages)
         if self.append:
             t = self.t
             for l in range(w.L):
@@ -206,6 +214,9 @@ class Lockstep:
             for b in range(w.B):
                 for h in range(w.Hkv):
                     check_invariants(ex, b * w.Hkv + h, self.ctx.P_lb[l][b], t, f"step {t} unit {(l, b, h)}")
+                    resident = int((ex["slot_part"][b * w.Hkv + h] >= 0).sum())
+                    assert resident <= self.budget_b[b], (
+                        f"step {t} unit {(l, b, h)}: {resident} pages resident over the budget {self.budget_b[b]}")
         for (l, b, h), u in self.oracle.items():
             ex = exports[l]
             ul = b * w.Hkv + h

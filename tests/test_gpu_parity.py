@@ -271,6 +271,33 @@ def test_append_errors():
 
 
 # ---------------------------------------------------------------------------
+# Buffer elasticity: per-request budgets change between steps.
+# ---------------------------------------------------------------------------
+def test_buffer_elasticity_lockstep():
+    """Budgets shrink to the mandatory pages, grow back and shrink again on different
+    requests mid-run; page state stays bit-exact with the oracle and no unit keeps more
+    pages resident than its request's budget."""
+    w = W.Workload("elastic", B=3, L=2, Hq=10, Hkv=2, ctx_len=[3000, 4113, 9000], topk=8, buf_mult=4,
+                   drift_a=0.8, drift_c=0.2, steps=30, seed=53)
+    events = {8: [(0, 8), (2, 16)], 16: [(0, 32)], 22: [(1, 8), (2, 9)]}
+    ls = Lockstep(w, budgets=events)
+    try:
+        for _ in range(w.steps):
+            ls.step()
+        st = ls.ctx.stats()
+        assert st["device_error"] == 0 and st["evictions"] > 0
+        assert ls.report.max_out_err <= OUT_TOL
+        from sparse_attention_tiered_gb300 import SpinError
+        from sparse_attention_tiered_gb300._binding import SPIN_ERR_INVALID
+        for b, pages in ((0, w.topk - 1), (0, w.cap + 1), (w.B, w.topk)):
+            with pytest.raises(SpinError) as e:
+                ls.ctx.set_buffer(b, pages)
+            assert e.value.code == SPIN_ERR_INVALID
+    finally:
+        ls.close()
+
+
+# ---------------------------------------------------------------------------
 # Full-size workloads: sampled units, the launch configuration the benchmark times.
 # ---------------------------------------------------------------------------
 FULL = [
