@@ -95,6 +95,13 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(LayerArgs a) {
 // ---------------------------------------------------------------------------
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
+// Units with more partitions than this take the wide-unit paths of the top-k (512
+// threads only): the radix passes after the first run on the keys of the threshold
+// bin, and the compaction ranks a short list of the keys >= the threshold.
+constexpr int kWideP = 4096;
+constexpr int kCandMax = 8192;   // keys of the first pass's threshold bin kept for the later passes
+__host__ __device__ inline int cand_capacity(int P_max) { return P_max > kWideP ? (P_max < kCandMax ? P_max : kCandMax) : 0; }
+constexpr int kListMax = 1024;   // keys >= the threshold ranked in the list compaction
 
 struct SelSmem {
   uint32_t* keys;     // [P_max]
@@ -111,6 +118,7 @@ struct SelSmem {
   int64_t* msrc;      // [k] host page of the unit's r-th miss (copy in this kernel)
   int64_t* mdst;      // [k] pool page of the unit's r-th miss
   int32_t* midx;      // [k] miss-list entry of the unit's r-th miss, -1 = none
+  uint32_t* cand;     // [cand_capacity(P_max)] (wide units) keys of the first radix pass's threshold bin
 };
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -136,6 +144,7 @@ __host__ __device__ inline size_t sel_smem_layout(int P_max, int cap, int k, int
   uint8_t* msrc = take(sizeof(int64_t) * k);
   uint8_t* mdst = take(sizeof(int64_t) * k);
   uint8_t* midx = take(sizeof(int32_t) * k);
+  uint8_t* cand = take(sizeof(uint32_t) * (size_t)cand_capacity(P_max));
   if (s) {
     s->keys = (uint32_t*)keys;
     s->sp = (int32_t*)sp;
@@ -151,6 +160,7 @@ __host__ __device__ inline size_t sel_smem_layout(int P_max, int cap, int k, int
     s->msrc = (int64_t*)msrc;
     s->mdst = (int64_t*)mdst;
     s->midx = (int32_t*)midx;
+    s->cand = (uint32_t*)cand;
   }
   return off;
 }
@@ -239,6 +249,7 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   __shared__ int s_bin, s_above, s_cnt_hits, s_cnt_res, s_cutoff, s_evicted;
   __shared__ int s_wgt[kSelWarps], s_weq[kSelWarps], s_wpos[kSelWarps], s_wtake[kSelWarps];
   __shared__ int s_scan[kSelWarps];
+  __shared__ int s_ncand, s_nlist, s_ntaken;
   SelSmem sm;
   sel_smem_layout(a.P_max, a.cap, a.k, a.D, &sm, smem_raw);
 
@@ -319,13 +330,17 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
   // ---------------- top-k: radix select on order-preserving keys ----------------
   uint32_t prefix = 0, mask = 0;
   int krem = keff;
+  const bool wide = NT == kSelThreads && P > kWideP;
+  int ncand = -1;  // >= 0: the later passes scan sm.cand[0, ncand) instead of every key
   if (keff > 0) {
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       for (int i = tid; i < kW * 256; i += NT) sm.whist[i] = 0;
       group_sync<NT>();
-      for (int p = tid; p < P; p += NT) {
-        const uint32_t key = sm.keys[p];
+      const uint32_t* src = ncand >= 0 ? sm.cand : sm.keys;
+      const int nsrc = ncand >= 0 ? ncand : P;
+      for (int p = tid; p < nsrc; p += NT) {
+        const uint32_t key = src[p];
         if ((key & mask) == prefix) atomicAdd(&sm.whist[warp * 256 + ((key >> shift) & 255u)], 1u);
       }
       group_sync<NT>();
@@ -369,13 +384,78 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       prefix |= (uint32_t)s_bin << shift;
       mask |= 0xFFu << shift;
       krem -= s_above;
+      if (pass == 0 && wide && (int)sm.whist[s_bin] <= cand_capacity(a.P_max)) {
+        // keep the keys of the threshold bin (row 0 of the histogram holds its merged count)
+        group_sync<NT>();
+        if (tid == 0) s_ncand = 0;
+        group_sync<NT>();
+        for (int p = tid; p < P; p += NT) {
+          const uint32_t key = sm.keys[p];
+          if ((key & mask) == prefix) sm.cand[atomicAdd(&s_ncand, 1)] = key;
+        }
+        group_sync<NT>();
+        ncand = s_ncand;
+      }
       group_sync<NT>();
     }
   }
   const uint32_t T = prefix;  // the k-th largest key; krem = equal keys still to take
 
   // ---------------- compaction in ascending partition order ----------------
-  {
+  // Wide units: the keys >= T go to a short unordered list (partition, key) in the
+  // histogram scratch; each list entry is taken when its key is > T or it is one of the
+  // krem equal keys with the lowest partitions, and lands at the rank of its partition
+  // among the taken entries. A list that would overflow falls back to the warp scans.
+  bool compacted = false;
+  if (wide && keff > 0) {
+    int32_t* lp = reinterpret_cast<int32_t*>(sm.whist);                // [kListMax] partition
+    uint32_t* lk = sm.whist + kListMax;                                  // [kListMax] key
+    int32_t* tk = reinterpret_cast<int32_t*>(sm.whist) + 2 * kListMax;  // [kListMax] taken flag
+    static_assert(3 * kListMax <= kSelWarps * 256, "the list must fit in the histogram scratch");
+    if (tid == 0) {
+      s_nlist = 0;
+      s_ntaken = 0;
+    }
+    group_sync<NT>();
+    for (int p = tid; p < P; p += NT) {
+      const uint32_t key = sm.keys[p];
+      if (key >= T) {
+        const int i = atomicAdd(&s_nlist, 1);
+        if (i < kListMax) {
+          lp[i] = p;
+          lk[i] = key;
+        }
+      }
+    }
+    group_sync<NT>();
+    const int n = s_nlist;
+    if (n <= kListMax) {
+      for (int i = tid; i < n; i += NT) {
+        int taken = lk[i] > T;
+        if (!taken) {  // equal key: taken when fewer than krem equal keys sit at lower partitions
+          int eqb = 0;
+          for (int j = 0; j < n; ++j) eqb += (lk[j] == T && lp[j] < lp[i]);
+          taken = eqb < krem;
+        }
+        tk[i] = taken;
+        if (taken) atomicAdd(&s_ntaken, 1);
+      }
+      group_sync<NT>();
+      if (s_ntaken != keff) {  // never expected: leave the unit untouched and report
+        if (tid == 0) atomicOr(a.err, kErrSelCount);
+        return;
+      }
+      for (int i = tid; i < n; i += NT) {
+        if (!tk[i]) continue;
+        int pos = 0;
+        for (int j = 0; j < n; ++j) pos += (tk[j] && lp[j] < lp[i]);
+        if (pos < keff) sm.sel[pos] = lp[i];
+      }
+      compacted = true;
+    }
+    group_sync<NT>();
+  }
+  if (!compacted) {
     const int chunk = ((P + NT - 1) / NT) * 32;
     const int wb = warp * chunk, we = min(P, wb + chunk);
     int gt = 0, eq = 0;

@@ -372,3 +372,53 @@ def test_hugepage_host_store_same_results():
     assert rep_b.max_out_err <= OUT_TOL
     for key in ("hits", "misses", "evictions", "live_segments", "host_store_bytes"):
         assert st_a[key] == st_b[key], key
+
+
+def _wide_ties_run(P, npat, scale_spread, topk, steps, seed):
+    """One unit with P partitions copied from `npat` patterns (exact score ties between
+    copies), scaled over `scale_spread` binades; GPU vs oracle every step."""
+    from sparse_attention_tiered_gb300 import SpinContext
+    rng = np.random.default_rng(seed)
+    G, cap = 2, 2 * topk
+    pat_k = rng.standard_normal((npat, 64, 128)).astype(np.float32)
+    pat_v = rng.standard_normal((npat, 64, 128)).astype(np.float32)
+    scales = 2.0 ** (np.arange(npat) % max(scale_spread, 1))
+    pat_k *= scales[:, None, None]
+    to_bits = lambda x: (np.ascontiguousarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kp, vp = to_bits(pat_k), to_bits(pat_v)
+    idx = np.arange(P) % npat
+    k = np.ascontiguousarray(kp[idx].reshape(1, P * 64, 128))
+    v = np.ascontiguousarray(vp[idx].reshape(1, P * 64, 128))
+    ctx = SpinContext(1, 1, G, 1, [P * 64], topk, 2)
+    try:
+        ctx.index_offload_host(0, 0, k, v)
+        torch.cuda.synchronize()
+        u = O.Unit(P * 64, cap, k[0], v[0])
+        out = torch.empty((1, G, 128), dtype=torch.float32, device="cuda")
+        for t in range(steps):
+            qf = rng.standard_normal((G, 128)).astype(np.float32)
+            qb = to_bits(qf)
+            ctx.decode_step(0, torch.from_numpy(qb.view(np.int16)[None]).cuda(), out)
+            torch.cuda.synchronize()
+            r = u.step(qb, topk, t)
+            ex = ctx.export(0)
+            keff = int(ex["keff"][0])
+            assert np.array_equal(ex["sel"][0][:keff], r["sel"]), f"step {t}: selection differs"
+            assert np.array_equal(ex["sel_slot"][0][:keff], r["sel_slot"]), f"step {t}: slots differ"
+            err = float(np.abs(out.cpu().numpy()[0] - r["out"]).max())
+            assert err <= OUT_TOL, f"step {t}: output error {err}"
+        assert ctx.stats()["device_error"] == 0
+    finally:
+        ctx.close()
+
+
+def test_wide_unit_exact_ties_candidate_and_list_paths():
+    """P > 4096: 100 exact copies of each of 50 patterns spread over 12 binades; the k-th
+    largest score sits in a tie group, resolved to the lowest partitions."""
+    _wide_ties_run(P=5000, npat=50, scale_spread=12, topk=64, steps=4, seed=61)
+
+
+def test_wide_unit_all_equal_scores_fallbacks():
+    """P > 4096, every partition identical: more tied keys than either list holds, so the
+    full-scan radix passes and the warp-scan compaction run; partitions 0..k-1 win."""
+    _wide_ties_run(P=5000, npat=1, scale_spread=1, topk=64, steps=2, seed=67)
