@@ -198,7 +198,13 @@ int spin_set_buffer(spin_ctx* ctx, int32_t b, int32_t pages, spin_stream_t strea
  * [batch][q_heads][128] = softmax(q K_sel^T / sqrt(128)) V_sel over the tokens of
  * the k selected partitions of the query head's KV head, plus, in tail mode, the
  * request's tail tokens (zeros for an empty request). Asynchronous on `stream`; the layer's step counter t advances by one
- * per call. Requires every request of `layer` to have been offloaded. */
+ * per call. Requires every request of `layer` to have been offloaded.
+ * The first step after any spin_index_offload call (of any layer) first enqueues one read
+ * pass over the whole host store: a 4-byte load every host page (at most every 32 KiB).
+ * The GPU translates each host page's address on its first read, and those translations
+ * resolve slowly; the pass pays for them once, so the steps' retrieval does not.
+ * Environment variable SPIN_STORE_WARM, read by spin_create, sets the number of passes:
+ * 0 to 8, default 1; 0 turns the pass off. */
 int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream);
 
 /* The same step with host buffers: q_host [batch][q_heads][128] bf16 and

@@ -93,6 +93,9 @@ struct spin_ctx {
   int retr_warps = 2;  // SPIN_RETRIEVE_WARPS (1..8): retriever warps per attend CTA from its start
   int retr_late = 8;   // SPIN_RETRIEVE_LATE (0..8): retriever warps that join after the CTA's resident pages
   int retrieve_in_select = 0;  // SPIN_RETRIEVE_IN_SELECT: misses copied by the select/manage kernel
+  int store_warm = 1;          // SPIN_STORE_WARM: read passes over the host store after it is written (0..8)
+  bool store_cold = false;     // the store was written since its last read pass
+  int64_t warm_stride = 32768; // bytes between the read pass's loads: the host page size, at most 32 KiB
   std::vector<int64_t> ctx_len;
   std::vector<int32_t> P_b, ntok_b;  // fixed mode: partitions and tokens of each request
   std::vector<int32_t> pstride_b;    // host-store pages per KV head of each request (its partition capacity)
@@ -121,6 +124,7 @@ struct spin_ctx {
   int32_t *d_slot_part = nullptr, *d_last_use = nullptr;
   unsigned long long* d_stats = nullptr;
   uint32_t* d_err = nullptr;
+  uint32_t* d_warm_sink = nullptr;  // the read pass's sink word (written only if a sum hits its key)
   uint16_t *d_stage_k = nullptr, *d_stage_v = nullptr;
   int64_t stage_tokens = 0;
   std::vector<LayerBuf> layers;
@@ -497,6 +501,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   ALLOC(c->d_last_use, slots, "allocating the page state");
   ALLOC(c->d_stats, 8, "allocating counters");
   ALLOC(c->d_err, 1, "allocating counters");
+  ALLOC(c->d_warm_sink, 1, "allocating counters");
   c->bytes_meta = (c->units * c->D + (c->h_seg ? 0 : c->S * kSeg) + c->S + nwords + 2 * slots) * 4;
   c->bytes_flat = (c->units * (int64_t)c->P_max + 2 * slots) * 4;
 
@@ -545,6 +550,11 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     if (v >= 0 && v <= 8) c->retr_late = v;
   }
   if (const char* env = getenv("SPIN_RETRIEVE_IN_SELECT")) c->retrieve_in_select = atoi(env) != 0;
+  if (const char* env = getenv("SPIN_STORE_WARM")) c->store_warm = std::max(0, std::min(8, atoi(env)));
+  {
+    const long pg = sysconf(_SC_PAGESIZE);
+    c->warm_stride = pg >= 4096 ? std::min<int64_t>(pg, kPageBytes) : 4096;
+  }
   if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = c->retr_late = c->retrieve_in_select = 0;
   if (const char* env = getenv("SPIN_SELECT_GROUP")) c->select_group = atoi(env);  // 0 auto, 32, 512
 
@@ -617,6 +627,12 @@ int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStre
   auto mark = [&](int i) {
     if (timed) cudaEventRecord(tc.ev[i], st);
   };
+  for (int i = 0; c->store_cold && i < c->store_warm; ++i) {
+    // after the store is (re)written, before the first retrieval can touch it
+    SPIN_CUDA(c, launch_warm_store(c->d_store, c->bytes_store, c->warm_stride, c->d_warm_sink, c->sm_count, st),
+              "launching the host-store read pass");
+  }
+  c->store_cold = false;
   mark(0);
   SPIN_CUDA(c, launch_score(a, st), "launching score");
   mark(1);
@@ -750,6 +766,7 @@ int spin_index_offload(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k,
     }
   }
   c->offloaded[(size_t)layer * c->B + b] = 1;
+  if (n_part_tok > 0) c->store_cold = true;
   return SPIN_OK;
 }
 
