@@ -120,6 +120,12 @@ __global__ void set_request_kernel(int32_t* P_b, int32_t* ntok_b, int32_t* tail_
   if (tail_n) *tail_n = tail;
 }
 
+// Plain 16-byte copy, grid-stride; used to stage a query batch from mapped host memory.
+__global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = __ldcs(src + i);
+}
+
 // Read pass over the pinned host store: one 4-byte load every `stride` bytes.
 // The first GPU read of a host page pays for translating its address, and those
 // translations resolve at a limited rate (on GB300 machines, 45-100 GB/s of random
@@ -168,6 +174,15 @@ cudaError_t launch_warm_store(const void* store, int64_t bytes, int64_t stride, 
   const int64_t n_reads = bytes / stride;  // every read ends inside the store
   warm_store_kernel<<<(sm_count > 0 ? sm_count : 1) * 4, 256, 0, st>>>(static_cast<const uint8_t*>(store), n_reads,
                                                                         stride, sink, 0x9E3779B9u);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy16(const void* src, void* dst, int64_t bytes, int sm_count, cudaStream_t st) {
+  const int64_t n = bytes / 16;  // callers pass multiples of 16 bytes, 16-byte aligned
+  if (n <= 0) return cudaSuccess;
+  const int64_t want = (n + 255) / 256, most = (int64_t)(sm_count > 0 ? sm_count : 1) * 2;
+  const int grid = (int)(want < most ? want : most);
+  copy16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n);
   return cudaGetLastError();
 }
 

@@ -127,11 +127,15 @@ def test_resident_pages_byte_exact():
 
 
 def test_host_buffer_entry_point_matches_device():
+    """spin_decode_step_host gives the device entry point's bytes whether its buffers are
+    mapped pinned memory (used in place by the kernels), pageable memory, or pinned memory
+    at an offset that is not 16-byte aligned (both copied through HBM)."""
     w = W.Workload("hostep", B=2, L=2, Hq=10, Hkv=2, ctx_len=[2048, 1500], topk=6, buf_mult=2,
                    drift_a=0.9, drift_c=0.1, steps=5, seed=23)
     from sparse_attention_tiered_gb300 import SpinContext
-    results = []
-    for use_host in (False, True):
+    n = w.B * w.Hq * 128
+    results = {}
+    for mode in ("device", "pinned", "pageable", "pinned_unaligned"):
         with SpinContext.for_workload(w) as ctx:
             for l in range(w.L):
                 for b in range(w.B):
@@ -140,25 +144,34 @@ def test_host_buffer_entry_point_matches_device():
                     torch.cuda.synchronize()
             qs = w.queries()
             outs = []
-            q_pin = torch.empty((w.B, w.Hq, 128), dtype=torch.int16).pin_memory()
-            o_pin = torch.empty((w.B, w.Hq, 128), dtype=torch.float32).pin_memory()
+            if mode == "pinned":
+                q_buf = torch.empty(n, dtype=torch.int16).pin_memory()
+                o_buf = torch.empty(n, dtype=torch.float32).pin_memory()
+            elif mode == "pinned_unaligned":  # 2- and 4-byte offsets into pinned allocations
+                q_buf = torch.empty(n + 8, dtype=torch.int16).pin_memory()[1:1 + n]
+                o_buf = torch.empty(n + 4, dtype=torch.float32).pin_memory()[1:1 + n]
+            else:
+                q_buf = torch.from_numpy(np.empty(n, np.int16))
+                o_buf = torch.from_numpy(np.empty(n, np.float32))
             od = torch.empty((w.B, w.Hq, 128), dtype=torch.float32, device="cuda")
             for t in range(w.steps):
                 qb = qs.bf16()
                 for l in range(w.L):
-                    if use_host:
-                        q_pin.copy_(torch.from_numpy(qb[l].view(np.int16)))
-                        ctx.decode_step_host(l, q_pin.data_ptr(), o_pin.data_ptr())
-                        torch.cuda.synchronize()
-                        outs.append(o_pin.numpy().copy())
-                    else:
+                    if mode == "device":
                         qd = torch.from_numpy(qb[l].view(np.int16)).cuda()
                         ctx.decode_step(l, qd, od)
                         torch.cuda.synchronize()
-                        outs.append(od.cpu().numpy())
+                        outs.append(od.cpu().numpy().reshape(-1))
+                    else:
+                        q_buf.copy_(torch.from_numpy(qb[l].view(np.int16).reshape(-1)))
+                        o_buf.fill_(float("nan"))
+                        ctx.decode_step_host(l, q_buf.data_ptr(), o_buf.data_ptr())
+                        torch.cuda.synchronize()
+                        outs.append(o_buf.numpy().copy())
                 qs.advance()
-            results.append(np.stack(outs))
-    assert np.array_equal(results[0], results[1])
+            results[mode] = np.stack(outs)
+    for mode in ("pinned", "pageable", "pinned_unaligned"):
+        assert np.array_equal(results["device"], results[mode]), mode
 
 
 def test_segment_pool_exhaustion_reports_capacity():
