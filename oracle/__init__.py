@@ -97,6 +97,10 @@ def _bind(L):
     L.oracle_unit_set_budget.restype = i32
     L.oracle_unit_grow.restype = i32
     L.oracle_attend_tail.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, vp]
+    L.oracle_index_parts.argtypes = [vp, vp, vp, i32, vp]
+    L.oracle_offload_parts.argtypes = [vp, vp, vp, vp, i32, vp]
+    L.oracle_unit_create_parts.argtypes = [vp, i32, i32]
+    L.oracle_unit_create_parts.restype = vp
     return L
 
 
@@ -144,6 +148,36 @@ def offload(k_bits: np.ndarray, v_bits: np.ndarray, lib=None) -> np.ndarray:
     return pages
 
 
+def _parts_args(order: np.ndarray, starts: np.ndarray):
+    order = np.ascontiguousarray(order, np.int32)
+    starts = np.ascontiguousarray(starts, np.int32)
+    return order, starts, starts.shape[0] - 1
+
+
+def index_parts(k_bits: np.ndarray, order: np.ndarray, starts: np.ndarray, lib=None) -> np.ndarray:
+    """Mean keys, double [P][128], of variable partitions: partition p holds the tokens
+    order[starts[p]:starts[p+1]] of K [ntok][128] (bf16 bits)."""
+    lib = lib or load()
+    k_bits = np.ascontiguousarray(k_bits, np.uint16)
+    order, starts, P = _parts_args(order, starts)
+    s = np.empty((max(P, 1), D), np.float64)
+    lib.oracle_index_parts(_p(k_bits), _p(order), _p(starts), P, _p(s))
+    return s[:P]
+
+
+def offload_parts(k_bits: np.ndarray, v_bits: np.ndarray, order: np.ndarray, starts: np.ndarray,
+                  lib=None) -> np.ndarray:
+    """Host pages [P][2][64][128] of variable partitions: page p holds its partition's
+    tokens in order from row 0, zero padded."""
+    lib = lib or load()
+    k_bits = np.ascontiguousarray(k_bits, np.uint16)
+    v_bits = np.ascontiguousarray(v_bits, np.uint16)
+    order, starts, P = _parts_args(order, starts)
+    pages = np.empty((max(P, 1), 2, PART, D), np.uint16)
+    lib.oracle_offload_parts(_p(k_bits), _p(v_bits), _p(order), _p(starts), P, _p(pages))
+    return pages[:P]
+
+
 def scores(summ: np.ndarray, q_bits: np.ndarray, lib=None) -> np.ndarray:
     lib = lib or load()
     summ = np.ascontiguousarray(summ, np.float64)
@@ -177,8 +211,36 @@ class Unit:
         self.h = self.lib.oracle_unit_create(ntok, cap)
         self.summ = None
         self.host_pages = None
+        self.part_n = None
         if k_bits is not None:
             self.load_kv(k_bits, v_bits)
+
+    @classmethod
+    def from_parts(cls, k_bits: np.ndarray, v_bits: np.ndarray, order: np.ndarray, starts: np.ndarray, cap: int,
+                   lib=None) -> "Unit":
+        """Unit of variable partitions (Index and Offload over the given grouping)."""
+        u = cls.__new__(cls)
+        u.lib = lib or load()
+        starts = np.ascontiguousarray(starts, np.int32)
+        u.part_n = np.ascontiguousarray(np.diff(starts), np.int32)
+        u.P = int(u.part_n.shape[0])
+        u.ntok = int(starts[-1])
+        u.cap = cap
+        u.h = u.lib.oracle_unit_create_parts(_p(u.part_n) if u.P else None, u.P, cap)
+        u.summ = index_parts(k_bits, order, starts, u.lib)
+        u.host_pages = offload_parts(k_bits, v_bits, order, starts, u.lib)
+        return u
+
+    def clone_empty(self, cap: int) -> "Unit":
+        """A unit with the same partitions, summaries and host pages, and nothing resident."""
+        c = Unit.__new__(Unit)
+        c.lib, c.cap, c.ntok, c.P, c.part_n = self.lib, cap, self.ntok, self.P, self.part_n
+        if self.part_n is not None:
+            c.h = self.lib.oracle_unit_create_parts(_p(self.part_n) if self.P else None, self.P, cap)
+        else:
+            c.h = self.lib.oracle_unit_create(self.ntok, cap)
+        c.summ, c.host_pages = self.summ, self.host_pages
+        return c
 
     def load_kv(self, k_bits: np.ndarray, v_bits: np.ndarray):
         """Index + Offload of this unit's keys and values."""

@@ -82,6 +82,38 @@ void oracle_offload(const uint16_t* k, const uint16_t* v, int64_t ntok, uint16_t
 }
 
 /* ------------------------------------------------------------------------- */
+/* Variable partitions ([XT] §1: a partition is a group of tokens that is the  */
+/* unit of selection and retrieval, either a fixed-size block or a cluster     */
+/* found dynamically; [GS] §2A: blocks, clusters and tokens are all mapped      */
+/* onto one page-based KV substrate). The grouping is the algorithm's Index;   */
+/* here it arrives as a token order and partition boundaries: partition p holds */
+/* tokens order[starts[p]] .. order[starts[p+1] - 1], 1 to 64 of them.          */
+/* reading: each partition occupies one page, its tokens in that order from row */
+/* 0, zero padded; its summary is the mean key of its tokens.                   */
+/* ------------------------------------------------------------------------- */
+void oracle_index_parts(const uint16_t* k, const int32_t* order, const int32_t* starts, int32_t P, double* summ) {
+  for (int32_t p = 0; p < P; ++p) {
+    const int32_t j0 = starts[p], j1 = starts[p + 1];
+    for (int i = 0; i < OD; ++i) {
+      double s = 0.0;
+      for (int32_t j = j0; j < j1; ++j) s += bf(k[(int64_t)order[j] * OD + i]);
+      summ[(int64_t)p * OD + i] = s / (double)(j1 - j0);
+    }
+  }
+}
+
+void oracle_offload_parts(const uint16_t* k, const uint16_t* v, const int32_t* order, const int32_t* starts,
+                          int32_t P, uint16_t* pages) {
+  memset(pages, 0, sizeof(uint16_t) * (size_t)((int64_t)P * OPAGE_ELEMS));
+  for (int32_t p = 0; p < P; ++p)
+    for (int32_t j = starts[p]; j < starts[p + 1]; ++j) {
+      const int64_t t = order[j], r = j - starts[p];
+      memcpy(pages + (int64_t)p * OPAGE_ELEMS + r * OD, k + t * OD, OD * sizeof(uint16_t));
+      memcpy(pages + (int64_t)p * OPAGE_ELEMS + OPART * OD + r * OD, v + t * OD, OD * sizeof(uint16_t));
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Select ([XT] §1 / Fig 3: Select picks the critical partitions for the       */
 /* query; [GS] §2A). reading: score_p = sum over the G query heads of the GQA  */
 /* group of q_g . summary_p; take the k highest scores, equal scores going to  */
@@ -145,6 +177,7 @@ typedef struct oracle_unit {
   int32_t P;           /* partitions of the unit (in tail mode: the complete ones) */
   int32_t P_cap;       /* partitions the unit may grow to (tail mode), else P */
   int32_t ntok;        /* valid tokens (last partition may be short) */
+  int32_t* part_n;     /* [P] tokens of each partition (variable partitions), else NULL */
   int32_t cap;         /* resident capacity in pages (mandatory + buffer) */
   int32_t budget;      /* pages the unit may keep resident now, k <= budget <= cap (buffer elasticity) */
   int32_t D;           /* directory entries = ceil(P / 64) */
@@ -180,6 +213,25 @@ oracle_unit* oracle_unit_create(int32_t ntok, int32_t cap) {
     u->last_use[i] = 0;
   }
   return u;
+}
+
+/* Unit of variable partitions: partition p holds part_n[p] tokens (1..64). */
+oracle_unit* oracle_unit_create_parts(const int32_t* part_n, int32_t P, int32_t cap) {
+  oracle_unit* u = oracle_unit_create(P * OPART, cap);
+  u->part_n = (int32_t*)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+  int32_t n = 0;
+  for (int32_t p = 0; p < P; ++p) {
+    u->part_n[p] = part_n[p];
+    n += part_n[p];
+  }
+  u->ntok = n;
+  return u;
+}
+
+/* Tokens held by partition p's page. */
+static int32_t unit_valid(const oracle_unit* u, int32_t p) {
+  if (u->part_n) return u->part_n[p];
+  return (p == u->P - 1) ? u->ntok - p * OPART : OPART;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -224,6 +276,7 @@ void oracle_unit_destroy(oracle_unit* u) {
   free(u->slot_part);
   free(u->last_use);
   free(u->slots);
+  free(u->part_n);
   free(u);
 }
 
@@ -377,7 +430,7 @@ void oracle_attend_tail(const oracle_unit* u, const int32_t* sel, const int32_t*
   int64_t n = tail_n;
   for (int32_t j = 0; j < keff; ++j) {
     int32_t p = sel[j];
-    n += (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+    n += unit_valid(u, p);
   }
   double* x = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
   const double scale = 1.0 / sqrt((double)OD);
@@ -393,7 +446,7 @@ void oracle_attend_tail(const oracle_unit* u, const int32_t* sel, const int32_t*
       int32_t valid;
       if (j < keff) {
         int32_t p = sel[j];
-        valid = (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+        valid = unit_valid(u, p);
         K = u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS;
       } else {
         valid = tail_n;
@@ -414,7 +467,7 @@ void oracle_attend_tail(const oracle_unit* u, const int32_t* sel, const int32_t*
       int32_t valid;
       if (j < keff) {
         int32_t p = sel[j];
-        valid = (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+        valid = unit_valid(u, p);
         V = u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS + OPART * OD;
       } else {
         valid = tail_n;
@@ -437,7 +490,7 @@ void oracle_attend(const oracle_unit* u, const int32_t* sel, const int32_t* sel_
   int64_t n = 0;
   for (int32_t j = 0; j < keff; ++j) {
     int32_t p = sel[j];
-    int32_t valid = (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+    int32_t valid = unit_valid(u, p);
     n += valid;
   }
   double* x = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
@@ -450,7 +503,7 @@ void oracle_attend(const oracle_unit* u, const int32_t* sel, const int32_t* sel_
     double m = -INFINITY;
     for (int32_t j = 0; j < keff; ++j) {
       int32_t p = sel[j];
-      int32_t valid = (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+      int32_t valid = unit_valid(u, p);
       const uint16_t* K = u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS;
       for (int32_t r = 0; r < valid; ++r) {
         double s = 0.0;
@@ -464,7 +517,7 @@ void oracle_attend(const oracle_unit* u, const int32_t* sel, const int32_t* sel_
     c = 0;
     for (int32_t j = 0; j < keff; ++j) {
       int32_t p = sel[j];
-      int32_t valid = (p == u->P - 1) ? u->ntok - p * OPART : OPART;
+      int32_t valid = unit_valid(u, p);
       const uint16_t* V = u->slots + (int64_t)sel_slot[j] * OPAGE_ELEMS + OPART * OD;
       for (int32_t r = 0; r < valid; ++r) {
         double w = exp(x[c] - m);

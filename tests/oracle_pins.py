@@ -17,6 +17,11 @@ What pins what:
   manage      bucketed-LRU invariants, page-table round trip, slot-order rule,
               a hand-traced scenario
   retrieve    byte equality of resident pages with the host pages
+  variable    partitions given as a token order and boundaries: numpy means of
+  partitions  the gathered rows, single-token and constant groups, page rows in
+              order with zero padding, dense identity over all tokens whatever
+              the grouping, and a partial selection equal to dense attention
+              over the union of the chosen groups' tokens
 """
 from __future__ import annotations
 
@@ -376,6 +381,73 @@ def check_append_tail(lib):
         assert ra2["mo"].hits == min(max(a.P, 1), a.P) == len(ra2["sel"]) and ra2["mo"].misses == 0
 
 
+def _sdpa(q_bits, k_rows, v_rows):
+    import torch
+    import torch.nn.functional as F
+    G, n = q_bits.shape[0], k_rows.shape[0]
+    qt = torch.from_numpy(bf(q_bits)).view(1, G, 1, D)
+    kt = torch.from_numpy(bf(k_rows)).view(1, 1, n, D).expand(1, G, n, D)
+    vt = torch.from_numpy(bf(v_rows)).view(1, 1, n, D).expand(1, G, n, D)
+    return F.scaled_dot_product_attention(qt, kt, vt).view(G, D).numpy()
+
+
+def check_variable_partitions(lib):
+    """Variable partitions: Index, Offload and Attention over a given grouping."""
+    rng = np.random.default_rng(13)
+    cases = [(300, [64, 1, 30, 64, 41, 50, 50]), (64, [1] * 64), (128, [64, 64]), (1000, None), (77, [77 - 64, 64])]
+    for n, sizes in cases:
+        if sizes is None:
+            order, starts = W.random_parts(rng, n, 40)
+        else:
+            order = rng.permutation(n).astype(np.int32)
+            starts = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        P = len(starts) - 1
+        k, v = rand_kv(rng, n, scale=1.4)
+        # index: the mean of each group's gathered rows (numpy), exact for 1-token groups
+        summ = O.index_parts(k, order, starts, lib)
+        kf = bf(k)
+        for p in range(P):
+            rows = order[starts[p]:starts[p + 1]]
+            ref = kf[rows].mean(axis=0)
+            assert np.abs(summ[p] - ref).max() <= 1e-12, f"group {p} mean differs"
+            if len(rows) == 1:
+                assert np.array_equal(summ[p], kf[rows[0]]), "a 1-token group's summary is its key"
+        # offload: page p holds the group's tokens in order from row 0, then zeros
+        pages = O.offload_parts(k, v, order, starts, lib)
+        for p in range(P):
+            rows = order[starts[p]:starts[p + 1]]
+            m = len(rows)
+            assert np.array_equal(pages[p, 0, :m], k[rows]) and np.array_equal(pages[p, 1, :m], v[rows])
+            assert not pages[p, :, m:].any(), "page padding must be zero"
+        G = 1 + n % 5
+        q = f32_to_bf16_bits(rng.standard_normal((G, D)).astype(np.float32))
+        # every group selected: dense attention over all tokens, whatever the grouping
+        u = O.Unit.from_parts(k, v, order, starts, cap=P, lib=lib)
+        r = u.step(q, k=P, t=0)
+        assert list(r["sel"]) == list(range(P))
+        err = np.abs(r["out"] - _sdpa(q, k, v)).max()
+        assert err <= 1e-12, f"dense identity over variable partitions broken (n={n}): {err}"
+        # a partial selection: the k best groups by q . mean summed over heads (numpy
+        # ranking, equal scores to the lower index), then dense attention over their tokens
+        kk = max(1, P // 3)
+        u2 = O.Unit.from_parts(k, v, order, starts, cap=kk, lib=lib)
+        r2 = u2.step(q, k=kk, t=0)
+        sc = (bf(q).sum(axis=0)[None, :] * np.stack([kf[order[starts[p]:starts[p + 1]]].mean(axis=0)
+                                                    for p in range(P)])).sum(axis=1)
+        want = np.sort(sorted(range(P), key=lambda p: (-sc[p], p))[:kk])
+        assert list(r2["sel"]) == list(want), "selection over group summaries differs from the ranking"
+        rows = np.concatenate([order[starts[p]:starts[p + 1]] for p in want])
+        err2 = np.abs(r2["out"] - _sdpa(q, k[rows], v[rows])).max()
+        assert err2 <= 1e-12, f"partial selection must attend exactly the chosen groups' tokens: {err2}"
+    # constant groups: every token of a group carries the group's key
+    order, starts = W.random_parts(rng, 500, 20)
+    consts = f32_to_bf16_bits(rng.standard_normal((20, D)).astype(np.float32))
+    k = np.empty((500, D), np.uint16)
+    for p in range(20):
+        k[order[starts[p]:starts[p + 1]]] = consts[p]
+    assert np.array_equal(O.index_parts(k, order, starts, lib), bf(consts)), "constant group mean"
+
+
 ALL_CHECKS = [check_dense_attention, check_attention_closed_forms, check_scores_probe, check_topk_bruteforce,
               check_index, check_lru_invariants, check_lru_hand_trace, check_budget_hand_trace,
-              check_step_consistency, check_append_tail]
+              check_step_consistency, check_append_tail, check_variable_partitions]

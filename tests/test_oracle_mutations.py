@@ -49,6 +49,13 @@ MUTANTS = {
                        "out->free_before = u->cap - out->resident_before;"),
     "offload_drops_tail_token": ("for (int64_t t = 0; t < ntok; ++t) {\n    int64_t p = t / OPART",
                                  "for (int64_t t = 0; t < ntok - 1; ++t) {\n    int64_t p = t / OPART"),
+    "parts_valid_drops_last_token": ("  if (u->part_n) return u->part_n[p];",
+                                     "  if (u->part_n) return u->part_n[p] - (u->part_n[p] > 1);"),
+    "parts_index_ignores_order": ("s += bf(k[(int64_t)order[j] * OD + i]);", "s += bf(k[(int64_t)j * OD + i]);"),
+    "parts_index_divides_by_64": ("summ[(int64_t)p * OD + i] = s / (double)(j1 - j0);",
+                                  "summ[(int64_t)p * OD + i] = s / (double)OPART;"),
+    "parts_offload_rows_reversed": ("const int64_t t = order[j], r = j - starts[p];",
+                                    "const int64_t t = order[j], r = starts[p + 1] - 1 - j;"),
 }
 
 

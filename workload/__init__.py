@@ -115,6 +115,7 @@ class Workload:
     hot_frac: float = 0.0
     d: int = D
     part: int = PART
+    mean_part: int = 0          # > 0: variable partitions averaging about this many tokens
 
     # ---- derived shapes ----
     @property
@@ -144,6 +145,31 @@ class Workload:
 
     def summary_bytes_per_step(self) -> int:
         return sum(self.partitions(b) for b in range(self.B)) * self.L * self.Hkv * self.d * 4
+
+    # ---- variable partitions (a stand-in for a clustering Index) ----
+    def var_partitions(self, b: int) -> int:
+        """Partitions per KV head of request b when mean_part > 0 (the same for every head
+        and layer of the request): ceil(ctx / mean_part), kept within [ceil(ctx / 64), ctx]."""
+        n = self.ctx_len[b]
+        if n == 0:
+            return 0
+        want = -(-n // max(self.mean_part, 1))
+        return int(min(n, max(-(-n // self.part), want)))
+
+    @property
+    def max_partitions(self) -> int:
+        return max((self.var_partitions(b) for b in range(self.B)), default=0)
+
+    def unit_parts(self, layer: int, b: int, h: int):
+        """Grouping of one unit's tokens: (order int32 [ctx], starts int32 [P + 1]).
+        Partition p holds tokens order[starts[p]:starts[p + 1]]."""
+        rng = np.random.default_rng([self.seed, 0x7061, layer, b, h])
+        return random_parts(rng, self.ctx_len[b], self.var_partitions(b))
+
+    def request_parts(self, layer: int, b: int):
+        """unit_parts of every KV head of request b: order [Hkv][ctx], starts [Hkv][P + 1]."""
+        parts = [self.unit_parts(layer, b, h) for h in range(self.Hkv)]
+        return (np.stack([o for o, _ in parts]).astype(np.int32), np.stack([s for _, s in parts]).astype(np.int32))
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -212,6 +238,29 @@ class QueryStream:
         out = np.empty(self.state.shape, np.uint16)
         lib().wl_to_bf16(_ptr(self.state), self.state.size, _ptr(out))
         return out
+
+
+def random_parts(rng, n: int, P: int, window: int = 256, max_size: int = PART):
+    """n tokens in P groups of 1..max_size: the tokens are shuffled within windows of
+    `window` consecutive tokens (clusters gather nearby tokens, not only adjacent ones) and
+    the order is cut into sizes drawn with exponential weights, so small and full groups
+    both occur."""
+    if n == 0:
+        return np.zeros(0, np.int32), np.zeros(1, np.int32)
+    assert 0 < P <= n <= max_size * P, (n, P)
+    sizes = np.ones(P, np.int64)
+    left = n - P
+    w = rng.exponential(size=P)
+    add = np.minimum(max_size - 1, np.floor(left * w / w.sum()).astype(np.int64))
+    sizes += add
+    left -= int(add.sum())
+    while left > 0:  # the remainder, one token each to groups with room, in random order
+        room = rng.permutation(np.flatnonzero(sizes < max_size))[:left]
+        sizes[room] += 1
+        left -= len(room)
+    order = np.concatenate([t0 + rng.permutation(min(window, n - t0)) for t0 in range(0, n, window)])
+    starts = np.concatenate([[0], np.cumsum(sizes)])
+    return order.astype(np.int32), starts.astype(np.int32)
 
 
 def normals(seed: int, tag: int, n: int) -> np.ndarray:
