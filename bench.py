@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default="qwen3_14b_32k", choices=sorted(W.ALL))
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling runs)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs)")
+    ap.add_argument("--mean-part", type=int, default=0,
+                    help="variable partitions of 1-64 tokens averaging about this many (a seeded grouping)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
@@ -103,14 +105,21 @@ def make_workload(args, rank=0):
         w = w.with_(L=args.layers)
     if args.batch:
         w = w.with_(B=args.batch, ctx_len=w.ctx_len[:args.batch])
+    if args.mean_part:
+        w = w.with_(mean_part=args.mean_part)
     return w
 
 
 def workload_desc(w):
     ctx = w.ctx_len
     ctx_s = str(ctx[0]) if len(set(ctx)) == 1 else f"{min(ctx)}-{max(ctx)} (mean {int(np.mean(ctx))})"
+    parts = "64-token partitions"
+    if w.mean_part:
+        n_p = sum(w.var_partitions(b) for b in range(w.B))
+        parts = (f"variable partitions of 1-64 tokens (mean {sum(ctx) / max(n_p, 1):.1f}, "
+                 f"seeded grouping within 256-token windows)")
     return (f"{w.name}: batch {w.B}, {w.L} layers, {w.Hq} q / {w.Hkv} kv heads, head_dim 128, context {ctx_s} tokens, "
-            f"64-token partitions, top-{w.topk}, buffer {w.buf_mult}x, drift {w.drift_a}/{w.drift_c}, seed {w.seed}")
+            f"{parts}, top-{w.topk}, buffer {w.buf_mult}x, drift {w.drift_a}/{w.drift_c}, seed {w.seed}")
 
 
 def measured_peaks():
@@ -219,8 +228,13 @@ def run_oracle_sample(w, steps_budget, cpu_seconds):
     units, qgroup = [], []
     for l in range(w.L):
         k, v = w.request_kv(l, 0)
+        order, starts = w.request_parts(l, 0) if w.mean_part else (None, None)
         for h in range(w.Hkv):
-            units.append(O.Unit(w.ctx_len[0], w.cap, np.ascontiguousarray(k[h]), np.ascontiguousarray(v[h])))
+            if w.mean_part:
+                units.append(O.Unit.from_parts(np.ascontiguousarray(k[h]), np.ascontiguousarray(v[h]), order[h],
+                                               starts[h], w.cap))
+            else:
+                units.append(O.Unit(w.ctx_len[0], w.cap, np.ascontiguousarray(k[h]), np.ascontiguousarray(v[h])))
             qgroup.append((l, h))
         del k, v
     qs = w.queries()
@@ -300,7 +314,10 @@ def bench_spin(args):
                 keep = [torch.empty((w.Hkv, n, 128), dtype=torch.int16).pin_memory() for _ in range(2)]
                 kbuf, vbuf = (t_.numpy().view(np.uint16) for t_ in keep)
             w.request_kv(l, b, kbuf, vbuf)
-            ctx.index_offload_host(b, l, kbuf, vbuf)
+            if w.mean_part:
+                ctx.index_offload_parts(b, l, kbuf, vbuf, *w.request_parts(l, b))
+            else:
+                ctx.index_offload_host(b, l, kbuf, vbuf)
             torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
 

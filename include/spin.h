@@ -105,6 +105,12 @@ typedef struct spin_config {
                                 partitions are selectable; the newest ctx % 64 tokens form the request's tail,
                                 which every decode step attends in full, and a tail that reaches 64 tokens is
                                 summarised, offloaded and becomes the next partition. */
+  int32_t max_partitions;    /* 0: fixed partitions of 64 consecutive tokens (the last may be short).
+                                > 0: variable partitions ([XT] §1; [GS] §2A): each request may hold up to this
+                                many partitions per KV head, each of 1 to 64 tokens in a page of its own, as
+                                spin_index_offload_parts groups them; spin_index_offload is then refused.
+                                Needs append_tokens == 0, max_partitions <= 2^20 and
+                                ceil(ctx_len[b] / 64) <= max_partitions for every request. */
 } spin_config;
 
 /* Counters since spin_create. */
@@ -167,6 +173,27 @@ int spin_create(const spin_config* cfg, spin_ctx** out);
  * pinned host store. Asynchronous on `stream`. */
 int spin_index_offload(spin_ctx* ctx, int32_t b, int32_t layer, const uint16_t* k, const uint16_t* v,
                        int64_t n_tokens, int32_t src_is_host, spin_stream_t stream);
+
+/* Index + Offload of variable partitions ([XT] §1: a partition is the unit of selection and
+ * retrieval, either a fixed-size block or a cluster found dynamically; [GS] §2A: blocks,
+ * clusters and tokens all map onto one page substrate). The grouping is the algorithm's Index
+ * and comes from the caller, as host arrays:
+ *   order  int32 [kv_heads][n_tokens]: for each head, a permutation of 0 .. n_tokens-1;
+ *   starts int32 [kv_heads][n_parts + 1]: starts[h][0] = 0, starts[h][n_parts] = n_tokens and
+ *          1 <= starts[h][p+1] - starts[h][p] <= 64.
+ * Partition p of head h holds the tokens order[h][starts[h][p]] .. order[h][starts[h][p+1] - 1];
+ * they are written in that order from row 0 of the partition's page (zero padded), the page
+ * records its token count, and the summary is their fp32 mean key. Selection, the page
+ * manager, retrieval and attention then work on these partitions as on fixed ones; attention
+ * reads each page's own token count. k, v: bf16 [kv_heads][n_tokens][128], host or device
+ * as in spin_index_offload; n_tokens == ctx_len[b]; 1 <= n_parts <= max_partitions, or 0
+ * when n_tokens == 0; every head of the request has n_parts partitions. Needs a context
+ * created with max_partitions > 0 (else SPIN_ERR_STATE). A grouping that breaks these rules
+ * returns SPIN_ERR_INVALID with nothing enqueued. Synchronous: returns once the work
+ * enqueued on `stream` has finished, so the host arrays may be reused at once. */
+int spin_index_offload_parts(spin_ctx* ctx, int32_t b, int32_t layer, const uint16_t* k, const uint16_t* v,
+                             int64_t n_tokens, const int32_t* order, const int32_t* starts, int32_t n_parts,
+                             int32_t src_is_host, spin_stream_t stream);
 
 /* KV append ([XT] §1, Figure 3: Index and Offload also run for the tokens decode
  * produces; the pages leave the mechanics open). Appends ONE token to every request

@@ -36,7 +36,7 @@ PAGE_BYTES = 32768
 SPIN_NOALLOC_MAX_SCORES_DEFAULT = 1 << 20  # SPIN_NOALLOC_MAX_SCORES in include/spin.h
 
 # Every symbol include/spin.h declares.
-EXPORTS = ("spin_create", "spin_index_offload", "spin_append_kv", "spin_set_buffer", "spin_decode_step", "spin_decode_step_host", "spin_stats",
+EXPORTS = ("spin_create", "spin_index_offload", "spin_index_offload_parts", "spin_append_kv", "spin_set_buffer", "spin_decode_step", "spin_decode_step_host", "spin_stats",
            "spin_debug_export", "spin_debug_read_page", "spin_debug_summaries", "spin_destroy", "spin_last_error",
            "spin_select_noalloc")
 
@@ -63,6 +63,7 @@ class spin_config(ctypes.Structure):
         ("device", ctypes.c_int32),
         ("flags", ctypes.c_uint32),
         ("append_tokens", ctypes.c_int32),
+        ("max_partitions", ctypes.c_int32),
     ]
 
 
@@ -113,6 +114,8 @@ def load(build_if_missing: bool = True):
             L.spin_create.restype = ctypes.c_int
             L.spin_index_offload.argtypes = [vp, i32, i32, vp, vp, i64, i32, vp]
             L.spin_index_offload.restype = ctypes.c_int
+            L.spin_index_offload_parts.argtypes = [vp, i32, i32, vp, vp, i64, vp, vp, i32, i32, vp]
+            L.spin_index_offload_parts.restype = ctypes.c_int
             L.spin_append_kv.argtypes = [vp, i32, vp, vp, vp]
             L.spin_append_kv.restype = ctypes.c_int
             L.spin_set_buffer.argtypes = [vp, i32, i32, vp]
@@ -158,6 +161,12 @@ def spin_create(cfg: spin_config) -> int:
 def spin_index_offload(ctx: int, b: int, layer: int, k_ptr: int, v_ptr: int, n_tokens: int, src_is_host: bool,
                        stream: int = 0):
     _check(load().spin_index_offload(ctx, b, layer, k_ptr, v_ptr, n_tokens, 1 if src_is_host else 0, stream), ctx)
+
+
+def spin_index_offload_parts(ctx: int, b: int, layer: int, k_ptr: int, v_ptr: int, n_tokens: int, order_ptr: int,
+                             starts_ptr: int, n_parts: int, src_is_host: bool, stream: int = 0):
+    _check(load().spin_index_offload_parts(ctx, b, layer, k_ptr, v_ptr, n_tokens, order_ptr, starts_ptr, n_parts,
+                                           1 if src_is_host else 0, stream), ctx)
 
 
 def spin_append_kv(ctx: int, layer: int, k_ptr: int, v_ptr: int, stream: int = 0):

@@ -22,7 +22,7 @@ class SpinContext:
 
     def __init__(self, batch: int, layers: int, q_heads: int, kv_heads: int, ctx_len: Sequence[int], topk: int,
                  buf_mult: int, device: int = 0, seg_pool_segments: int = 0, flags: int = 0,
-                 append_tokens: int = 0):
+                 append_tokens: int = 0, max_partitions: int = 0):
         self.B, self.L, self.Hq, self.Hkv = batch, layers, q_heads, kv_heads
         self.G = q_heads // kv_heads
         self.ctx_len = [int(x) for x in ctx_len]
@@ -30,8 +30,14 @@ class SpinContext:
         self.cap = topk * buf_mult
         self.append_tokens = int(append_tokens)
         self.tail_mode = self.append_tokens > 0
+        self.max_partitions = int(max_partitions)
+        self.part_mode = self.max_partitions > 0
         PT = B.PART_TOKENS
-        if self.tail_mode:
+        if self.part_mode:
+            # variable partitions: none until each (layer, request) is offloaded
+            self.P = [0] * batch
+            self.P_cap = [self.max_partitions] * batch
+        elif self.tail_mode:
             # complete partitions per (layer, request); the rest of the context is the tail
             self.P = [n // PT for n in self.ctx_len]
             self.P_cap = [(n + self.append_tokens + PT - 1) // PT for n in self.ctx_len]
@@ -41,14 +47,20 @@ class SpinContext:
         self.P_lb = [list(self.P) for _ in range(layers)]
         self.tail_lb = [[(n % PT) if self.tail_mode else 0 for n in self.ctx_len] for _ in range(layers)]
         self.P_max = max(self.P_cap) if self.P_cap else 0
+        if self.part_mode:
+            self.P_lb = [[0] * batch for _ in range(layers)]
         self.device = device
         self._ctx_arr = (ctypes.c_int64 * batch)(*self.ctx_len)
         cfg = B.spin_config(batch, layers, q_heads, kv_heads, B.HEAD_DIM, B.PART_TOKENS, topk, buf_mult,
-                            self._ctx_arr, 0, seg_pool_segments, device, flags, self.append_tokens)
+                            self._ctx_arr, 0, seg_pool_segments, device, flags, self.append_tokens,
+                            self.max_partitions)
         self.h = B.spin_create(cfg)
 
     @classmethod
     def for_workload(cls, w, device: int = 0, **kw) -> "SpinContext":
+        """A context for a workload; variable partitions when the workload has mean_part > 0."""
+        if getattr(w, "mean_part", 0) and "max_partitions" not in kw:
+            kw["max_partitions"] = w.max_partitions
         return cls(w.B, w.L, w.Hq, w.Hkv, w.ctx_len, w.topk, w.buf_mult, device=device, **kw)
 
     def close(self):
@@ -79,6 +91,25 @@ class SpinContext:
         """k_dev, v_dev: contiguous CUDA tensors [Hkv][ctx_len[b]][128] of bf16 or int16 bits."""
         n = self.ctx_len[b]
         B.spin_index_offload(self.h, b, layer, k_dev.data_ptr(), v_dev.data_ptr(), n, False, stream)
+
+    def index_offload_parts(self, b: int, layer: int, k, v, order: np.ndarray, starts: np.ndarray,
+                            stream: int = 0):
+        """Variable partitions. k, v: uint16 host arrays or CUDA tensors [Hkv][ctx_len[b]][128];
+        order int32 [Hkv][ctx_len[b]] and starts int32 [Hkv][P + 1] host arrays (the grouping:
+        partition p of head h holds tokens order[h][starts[h][p]:starts[h][p + 1]]).
+        Returns once done."""
+        n = self.ctx_len[b]
+        order = np.ascontiguousarray(order, np.int32)
+        starts = np.ascontiguousarray(starts, np.int32)
+        assert order.shape == (self.Hkv, n) and starts.ndim == 2 and starts.shape[0] == self.Hkv
+        n_parts = starts.shape[1] - 1
+        host = isinstance(k, np.ndarray)
+        kp = _ptr(k) if host else k.data_ptr()
+        vp = _ptr(v) if host else v.data_ptr()
+        if host:
+            assert k.shape == (self.Hkv, n, B.HEAD_DIM) and v.shape == k.shape
+        B.spin_index_offload_parts(self.h, b, layer, kp, vp, n, _ptr(order), _ptr(starts), n_parts, host, stream)
+        self.P_lb[layer][b] = n_parts
 
     # ---- KV append (tail mode) ----
     def append_kv(self, layer: int, k_dev, v_dev, stream: int = 0):

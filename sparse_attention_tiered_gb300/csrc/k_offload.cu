@@ -120,6 +120,51 @@ __global__ void set_request_kernel(int32_t* P_b, int32_t* ntok_b, int32_t* tail_
   if (tail_n) *tail_n = tail;
 }
 
+// Variable partitions: one CTA per (partition, kv head). Partition p of head h holds the
+// tokens order[h][starts[h][p]] .. order[h][starts[h][p+1] - 1] (1 to 64 of them, checked
+// on the host); they go into the partition's page from row 0 in that order, zero padded,
+// and its summary is their fp32 mean key, summed in row order as summarize_offload_kernel
+// sums a block. k, v: [kv_heads][n_tokens][128].
+__global__ void __launch_bounds__(kOffloadThreads)
+gather_offload_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int64_t n_tokens,
+                      const int32_t* __restrict__ order, const int32_t* __restrict__ starts, int32_t n_parts,
+                      float* __restrict__ summ_unit0, uint16_t* __restrict__ host_unit0, int64_t unit_pages,
+                      uint8_t* __restrict__ valid_unit0) {
+  __shared__ __align__(16) uint16_t ks[kPart * kD];
+  __shared__ int32_t rows[kPart];
+  const int p = blockIdx.x, h = blockIdx.y;
+  const int32_t* st = starts + (int64_t)h * (n_parts + 1);
+  const int j0 = st[p];
+  const int cnt = st[p + 1] - j0;
+  if (threadIdx.x < kPart) rows[threadIdx.x] = threadIdx.x < cnt ? order[(int64_t)h * n_tokens + j0 + threadIdx.x] : 0;
+  __syncthreads();
+  const uint16_t* kh = k + (int64_t)h * n_tokens * kD;
+  const uint16_t* vh = v + (int64_t)h * n_tokens * kD;
+  uint4* page = reinterpret_cast<uint4*>(host_unit0 + ((int64_t)h * unit_pages + p) * kPageElems);
+  constexpr int kRowVec = kD / 8;                      // 16-byte vectors per row
+  constexpr int kVecPerHalf = kPart * kRowVec;
+  for (int i = threadIdx.x; i < kVecPerHalf; i += kOffloadThreads) {
+    const int r = i / kRowVec, c = i % kRowVec;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < cnt) val = reinterpret_cast<const uint4*>(kh + (int64_t)rows[r] * kD)[c];
+    reinterpret_cast<uint4*>(ks)[i] = val;
+    page[i] = val;
+  }
+  for (int i = threadIdx.x; i < kVecPerHalf; i += kOffloadThreads) {
+    const int r = i / kRowVec, c = i % kRowVec;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < cnt) val = reinterpret_cast<const uint4*>(vh + (int64_t)rows[r] * kD)[c];
+    page[kVecPerHalf + i] = val;
+  }
+  __syncthreads();
+  if (threadIdx.x < kD) {
+    float s = 0.f;
+    for (int r = 0; r < cnt; ++r) s += bf16_bits_to_float(ks[r * kD + threadIdx.x]);
+    summ_unit0[((int64_t)h * unit_pages + p) * kD + threadIdx.x] = s / (float)cnt;
+  }
+  if (threadIdx.x == 0) valid_unit0[(int64_t)h * unit_pages + p] = (uint8_t)cnt;
+}
+
 // Plain 16-byte copy, grid-stride; used to stage a query batch from mapped host memory.
 __global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
@@ -174,6 +219,16 @@ cudaError_t launch_warm_store(const void* store, int64_t bytes, int64_t stride, 
   const int64_t n_reads = bytes / stride;  // every read ends inside the store
   warm_store_kernel<<<(sm_count > 0 ? sm_count : 1) * 4, 256, 0, st>>>(static_cast<const uint8_t*>(store), n_reads,
                                                                         stride, sink, 0x9E3779B9u);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_offload(const uint16_t* k, const uint16_t* v, int64_t n_tokens, int32_t kv_heads,
+                                  const int32_t* order, const int32_t* starts, int32_t n_parts, float* summ_unit0,
+                                  uint16_t* host_unit0, int64_t unit_pages, uint8_t* valid_unit0, cudaStream_t st) {
+  if (n_tokens <= 0 || n_parts <= 0) return cudaSuccess;
+  dim3 grid((unsigned)n_parts, (unsigned)kv_heads);
+  gather_offload_kernel<<<grid, kOffloadThreads, 0, st>>>(k, v, n_tokens, order, starts, n_parts, summ_unit0,
+                                                           host_unit0, unit_pages, valid_unit0);
   return cudaGetLastError();
 }
 

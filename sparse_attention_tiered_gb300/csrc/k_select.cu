@@ -689,7 +689,9 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
     a.miss_src[idx] = src;
     a.miss_dst[idx] = dst;
     a.miss_att[idx] = ul * a.ka + hits + has_tail + rank;  // misses follow the hits and the tail
-    a.miss_valid[idx] = (p == P - 1) ? a.ntok_b[b] - p * kPart : kPart;
+    a.miss_valid[idx] = (a.part_valid && src >= 0 && src < a.host_pages)
+                            ? (int)a.part_valid[src]
+                            : ((p == P - 1) ? a.ntok_b[b] - p * kPart : kPart);
     if (src >= 0 && src < a.host_pages && dst >= 0 && dst < a.pool_slots) {
       sm.msrc[rank] = src;
       sm.mdst[rank] = dst;
@@ -721,7 +723,10 @@ __global__ void __launch_bounds__(kSelThreads) select_manage_kernel(LayerArgs a)
       const bool hit = sm.hit[j] > 0;
       const int pos = hit ? j - sm.mrank[j] : hits + has_tail + sm.mrank[j];
       a.att_slot[(int64_t)ul * a.ka + pos] = sm.sslot[j];
-      a.att_valid[(int64_t)ul * a.ka + pos] = (p == P - 1) ? ntok - p * kPart : kPart;
+      const int64_t hp = host_page_index(a, b, h, p);
+      a.att_valid[(int64_t)ul * a.ka + pos] = (a.part_valid && hp >= 0 && hp < a.host_pages)
+                                                  ? (int)a.part_valid[hp]
+                                                  : ((p == P - 1) ? ntok - p * kPart : kPart);
     }
     if (has_tail && tid == 0) {
       a.att_slot[(int64_t)ul * a.ka + hits] = cap;

@@ -103,6 +103,14 @@ struct spin_ctx {
   // tail mode (append_tokens > 0): per-(layer, request) complete partitions and tail tokens,
   // mirrored on the host (every append adds exactly one token, so the host knows them)
   bool tail_mode = false;
+  // variable partitions (max_partitions > 0): every request has room for max_partitions per KV
+  // head; part_valid holds each page's token count; the grouping is staged in HBM
+  bool part_mode = false;
+  int32_t max_partitions = 0;
+  uint8_t* d_part_valid = nullptr;
+  int32_t* d_gorder = nullptr;   // [Hkv][max ctx_len]
+  int32_t* d_gstarts = nullptr;  // [Hkv][max_partitions + 1]
+  uint16_t *d_gk = nullptr, *d_gv = nullptr;  // host-source staging, [Hkv][max ctx_len][128]
   int64_t append_tokens = 0, appended = 0;
   int ka = 0;  // attention entries per unit
   std::vector<int32_t> P_lb, tail_lb;
@@ -318,6 +326,16 @@ int validate(const spin_config* cfg) {
       return fail(nullptr, SPIN_ERR_INVALID, "ctx_len[%d] + append_tokens = %lld outside [0, %d]", b,
                   (long long)(cfg->ctx_len[b] + cfg->append_tokens), 32768 * kPart);
   }
+  if (cfg->max_partitions < 0 || cfg->max_partitions > (1 << 20))
+    return fail(nullptr, SPIN_ERR_INVALID, "max_partitions must be in [0, 2^20]");
+  if (cfg->max_partitions > 0) {
+    if (cfg->append_tokens > 0)
+      return fail(nullptr, SPIN_ERR_INVALID, "variable partitions (max_partitions > 0) need append_tokens == 0");
+    for (int b = 0; b < cfg->batch; ++b)
+      if ((cfg->ctx_len[b] + kPart - 1) / kPart > cfg->max_partitions)
+        return fail(nullptr, SPIN_ERR_INVALID, "ctx_len[%d] = %lld needs more than max_partitions = %d partitions", b,
+                    (long long)cfg->ctx_len[b], cfg->max_partitions);
+  }
   if (cfg->seg_pool_segments < 0) return fail(nullptr, SPIN_ERR_INVALID, "seg_pool_segments must be >= 0");
   const int64_t units = (int64_t)cfg->batch * cfg->layers * cfg->kv_heads;
   if (units * ((int64_t)cfg->buf_mult * cfg->topk + 1) >= (int64_t)1 << 24)
@@ -348,6 +366,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.P_b = c->d_P_lb + (int64_t)l * c->B;
   a.ntok_b = c->d_ntok_lb + (int64_t)l * c->B;
   a.tail_n = c->tail_mode ? c->d_tail_lb + (int64_t)l * c->B : nullptr;
+  a.part_valid = c->d_part_valid;
   a.pstride_b = c->d_pstride_b;
   a.budget_b = c->d_budget_b;
   a.poff_b = c->d_poff_b;
@@ -398,6 +417,8 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   c->ctx_len.assign(cfg->ctx_len, cfg->ctx_len + c->B);
   c->append_tokens = cfg->append_tokens;
   c->tail_mode = cfg->append_tokens > 0;
+  c->part_mode = cfg->max_partitions > 0;
+  c->max_partitions = cfg->max_partitions;
   c->ka = c->k + (c->tail_mode ? 1 : 0);
   c->P_b.resize(c->B);
   c->ntok_b.resize(c->B);
@@ -410,7 +431,9 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     c->ntok_b[b] = (int32_t)c->ctx_len[b];
     c->P_b[b] = (int32_t)((c->ctx_len[b] + kPart - 1) / kPart);
     // tail mode: room for every partition the request can reach
-    c->pstride_b[b] = c->tail_mode ? (int32_t)((c->ctx_len[b] + c->append_tokens + kPart - 1) / kPart) : c->P_b[b];
+    c->pstride_b[b] = c->tail_mode   ? (int32_t)((c->ctx_len[b] + c->append_tokens + kPart - 1) / kPart)
+                      : c->part_mode ? c->max_partitions
+                                     : c->P_b[b];
     c->poff_b[b] = poff;
     poff += c->pstride_b[b];
     c->P_max = std::max(c->P_max, c->pstride_b[b]);
@@ -419,7 +442,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   }
   c->P_lb.assign((size_t)c->L * c->B, 0);
   c->tail_lb.assign((size_t)c->L * c->B, 0);
-  for (int l = 0; l < c->L && !c->tail_mode; ++l)
+  for (int l = 0; l < c->L && !c->tail_mode && !c->part_mode; ++l)
     for (int b = 0; b < c->B; ++b) c->P_lb[(size_t)l * c->B + b] = c->P_b[b];
   c->D = std::max(1, (c->P_max + kSeg - 1) / kSeg);
   c->pages_per_layer = poff * c->Hkv;
@@ -469,6 +492,11 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   if ((e = dalloc(c, &(ptr), (size_t)(n))) != cudaSuccess) return cuda_fail(nullptr, e, what)
   ALLOC(c->d_pool, (slots + tail_pages) * kPageElems, "allocating the HBM page pool");
   ALLOC(c->d_summ, total_pages * kD, "allocating the summaries");
+  if (c->part_mode) {
+    ALLOC(c->d_part_valid, total_pages, "allocating the partition sizes");
+    SPIN_CUDA(nullptr, cudaMemset(c->d_part_valid, 0, (size_t)std::max<int64_t>(total_pages, 1)),
+              "initialising the partition sizes");
+  }
   ALLOC(c->d_P_lb, (int64_t)c->L * c->B, "allocating request tables");
   ALLOC(c->d_ntok_lb, (int64_t)c->L * c->B, "allocating request tables");
   ALLOC(c->d_tail_lb, (int64_t)c->L * c->B, "allocating request tables");
@@ -506,9 +534,10 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   c->bytes_flat = (c->units * (int64_t)c->P_max + 2 * slots) * 4;
 
   {
-    // fixed mode: every layer holds the request's partitions; tail mode: nothing until offload
+    // fixed mode: every layer holds the request's partitions; tail mode and variable
+    // partitions: nothing until offload
     std::vector<int32_t> ntok_lb((size_t)c->L * c->B, 0);
-    for (int l = 0; l < c->L && !c->tail_mode; ++l)
+    for (int l = 0; l < c->L && !c->tail_mode && !c->part_mode; ++l)
       for (int b = 0; b < c->B; ++b) ntok_lb[(size_t)l * c->B + b] = c->ntok_b[b];
     const size_t n = (size_t)c->L * c->B * 4;
     SPIN_CUDA(nullptr, cudaMemcpy(c->d_P_lb, c->P_lb.data(), n, cudaMemcpyHostToDevice), "uploading tables");
@@ -708,6 +737,8 @@ int spin_index_offload(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k,
   if (!c) return fail(nullptr, SPIN_ERR_INVALID, "ctx is NULL");
   if (b < 0 || b >= c->B || layer < 0 || layer >= c->L)
     return fail(c, SPIN_ERR_INVALID, "request %d / layer %d out of range", b, layer);
+  if (c->part_mode)
+    return fail(c, SPIN_ERR_STATE, "a context with max_partitions > 0 takes spin_index_offload_parts");
   if (n_tokens != c->ctx_len[b])
     return fail(c, SPIN_ERR_INVALID, "n_tokens %lld differs from ctx_len[%d] = %lld", (long long)n_tokens, b,
                 (long long)c->ctx_len[b]);
@@ -781,6 +812,97 @@ int spin_index_offload(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k,
   }
   c->offloaded[(size_t)layer * c->B + b] = 1;
   if (n_part_tok > 0) c->store_cold = true;
+  return SPIN_OK;
+}
+
+int spin_index_offload_parts(spin_ctx* c, int32_t b, int32_t layer, const uint16_t* k, const uint16_t* v,
+                             int64_t n_tokens, const int32_t* order, const int32_t* starts, int32_t n_parts,
+                             int32_t src_is_host, spin_stream_t stream) {
+  if (!c) return fail(nullptr, SPIN_ERR_INVALID, "ctx is NULL");
+  if (!c->part_mode)
+    return fail(c, SPIN_ERR_STATE, "spin_index_offload_parts needs a context created with max_partitions > 0");
+  if (b < 0 || b >= c->B || layer < 0 || layer >= c->L)
+    return fail(c, SPIN_ERR_INVALID, "request %d / layer %d out of range", b, layer);
+  if (n_tokens != c->ctx_len[b])
+    return fail(c, SPIN_ERR_INVALID, "n_tokens %lld differs from ctx_len[%d] = %lld", (long long)n_tokens, b,
+                (long long)c->ctx_len[b]);
+  if (n_tokens == 0 ? n_parts != 0 : (n_parts < 1 || n_parts > c->max_partitions))
+    return fail(c, SPIN_ERR_INVALID, "n_parts = %d outside [1, max_partitions = %d] (0 for an empty request)",
+                n_parts, c->max_partitions);
+  if (n_tokens > 0 && (!k || !v || !order || !starts)) return fail(c, SPIN_ERR_INVALID, "k, v, order or starts is NULL");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+    return fail(c, SPIN_ERR_INVALID, "k and v must be 16-byte aligned");
+  // the grouping: per head, partitions of 1..64 tokens that cover a permutation of the tokens
+  if (n_tokens > 0) {
+    std::vector<uint8_t> seen((size_t)n_tokens);
+    for (int h = 0; h < c->Hkv; ++h) {
+      const int32_t* st = starts + (int64_t)h * (n_parts + 1);
+      const int32_t* od = order + (int64_t)h * n_tokens;
+      if (st[0] != 0 || st[n_parts] != n_tokens)
+        return fail(c, SPIN_ERR_INVALID, "head %d: starts must run from 0 to n_tokens", h);
+      for (int p = 0; p < n_parts; ++p) {
+        const int64_t m = (int64_t)st[p + 1] - st[p];
+        if (m < 1 || m > kPart)
+          return fail(c, SPIN_ERR_INVALID, "head %d partition %d holds %lld tokens (1..%d allowed)", h, p, (long long)m,
+                      kPart);
+      }
+      std::fill(seen.begin(), seen.end(), 0);
+      for (int64_t j = 0; j < n_tokens; ++j) {
+        const int32_t t = od[j];
+        if (t < 0 || t >= n_tokens || seen[t])
+          return fail(c, SPIN_ERR_INVALID, "head %d: order is not a permutation of the request's tokens", h);
+        seen[t] = 1;
+      }
+    }
+  }
+  DeviceGuard g(c->device);
+  if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t P = c->pstride_b[b];  // = max_partitions: host-store pages per KV head of the request
+  const int64_t page0 = (int64_t)layer * c->pages_per_layer + (int64_t)c->Hkv * c->poff_b[b];
+  if (n_tokens > 0) {
+    int64_t max_ctx = 0;
+    for (int64_t n : c->ctx_len) max_ctx = std::max(max_ctx, n);
+    cudaError_t e;
+    if (!c->d_gorder) {
+      if ((e = dalloc(c, &c->d_gorder, (size_t)c->Hkv * max_ctx)) != cudaSuccess)
+        return cuda_fail(c, e, "allocating the grouping buffer");
+      if ((e = dalloc(c, &c->d_gstarts, (size_t)c->Hkv * (c->max_partitions + 1))) != cudaSuccess)
+        return cuda_fail(c, e, "allocating the grouping buffer");
+    }
+    SPIN_CUDA(c, cudaMemcpyAsync(c->d_gorder, order, (size_t)c->Hkv * n_tokens * 4, cudaMemcpyHostToDevice, st),
+              "copying the token order");
+    SPIN_CUDA(c,
+              cudaMemcpyAsync(c->d_gstarts, starts, (size_t)c->Hkv * (n_parts + 1) * 4, cudaMemcpyHostToDevice, st),
+              "copying the partition starts");
+    const uint16_t *ks = k, *vs = v;
+    if (src_is_host) {
+      if (!c->d_gk) {
+        if ((e = dalloc(c, &c->d_gk, (size_t)c->Hkv * max_ctx * kD)) != cudaSuccess)
+          return cuda_fail(c, e, "allocating the offload staging buffer");
+        if ((e = dalloc(c, &c->d_gv, (size_t)c->Hkv * max_ctx * kD)) != cudaSuccess)
+          return cuda_fail(c, e, "allocating the offload staging buffer");
+      }
+      const size_t bytes = (size_t)c->Hkv * n_tokens * kD * 2;
+      SPIN_CUDA(c, cudaMemcpyAsync(c->d_gk, k, bytes, cudaMemcpyHostToDevice, st), "copying K to the staging buffer");
+      SPIN_CUDA(c, cudaMemcpyAsync(c->d_gv, v, bytes, cudaMemcpyHostToDevice, st), "copying V to the staging buffer");
+      ks = c->d_gk;
+      vs = c->d_gv;
+    }
+    SPIN_CUDA(c,
+              launch_gather_offload(ks, vs, n_tokens, c->Hkv, c->d_gorder, c->d_gstarts, n_parts,
+                                    c->d_summ + page0 * kD, c->d_store + page0 * kPageElems, P,
+                                    c->d_part_valid + page0, st),
+              "launching gather/offload");
+  }
+  const size_t lb = (size_t)layer * c->B + b;
+  SPIN_CUDA(c,
+            launch_set_request(c->d_P_lb + lb, c->d_ntok_lb + lb, nullptr, n_parts, (int32_t)n_tokens, 0, st),
+            "setting the request state");
+  SPIN_CUDA(c, cudaStreamSynchronize(st), "finishing the offload");
+  c->P_lb[lb] = n_parts;
+  c->offloaded[lb] = 1;
+  if (n_tokens > 0) c->store_cold = true;
   return SPIN_OK;
 }
 

@@ -40,6 +40,7 @@ struct LayerArgs {
   const int32_t* P_b;        // [B] selectable partitions of request b in this layer (tail mode: complete ones)
   const int32_t* ntok_b;     // [B] tokens held by those partitions
   const int32_t* tail_n;     // [B] tokens in the request's tail page (tail mode), else nullptr
+  const uint8_t* part_valid; // [host pages] tokens of each partition's page (variable partitions), else nullptr
   const int32_t* pstride_b;  // [B] host-store pages per KV head of request b (its partition capacity)
   const int32_t* budget_b;   // [B] resident budget per unit of request b (k <= budget <= cap)
   const int64_t* poff_b;     // [B] sum of pstride over earlier requests
@@ -102,6 +103,9 @@ enum : int {
 cudaError_t launch_summarize_offload(const uint16_t* k, const uint16_t* v, int64_t head_stride, int32_t kv_heads,
                                      int64_t tok0, int64_t ntok_chunk, int64_t ntok_total, float* summ_unit0,
                                      uint16_t* host_unit0, int64_t unit_pages, cudaStream_t st);
+cudaError_t launch_gather_offload(const uint16_t* k, const uint16_t* v, int64_t n_tokens, int32_t kv_heads,
+                                  const int32_t* order, const int32_t* starts, int32_t n_parts, float* summ_unit0,
+                                  uint16_t* host_unit0, int64_t unit_pages, uint8_t* valid_unit0, cudaStream_t st);
 cudaError_t launch_warm_store(const void* store, int64_t bytes, int64_t stride, uint32_t* sink, int sm_count,
                               cudaStream_t st);
 cudaError_t launch_copy16(const void* src, void* dst, int64_t bytes, int sm_count, cudaStream_t st);

@@ -27,6 +27,11 @@ token (drawn by the generator beyond the initial context) on both sides, then
 decodes. The oracle's TailUnit supplies the expected partitions and tail; the
 compared units' tail pages must equal the oracle's tail byte for byte and the
 summaries of partitions made from full tails must match the oracle's means.
+
+Variable partitions (workloads with ``mean_part > 0``): both sides take the
+generator's grouping (token order and partition boundaries); the GPU's summaries
+must match the oracle's group means and, on the first step, every resident page
+must equal the oracle's page of its partition byte for byte.
 """
 from __future__ import annotations
 
@@ -140,24 +145,36 @@ class Lockstep:
         want = {}
         for (l, b, h) in self.units:
             want.setdefault((l, b), []).append(h)
+        self.parts = bool(getattr(w, "mean_part", 0))
         for l in range(w.L):
             for b in range(w.B):
                 n = w.ctx_len[b]
                 k, v = wf.request_kv(l, b, threads=gen_threads)
+                if self.parts:
+                    order, starts = w.request_parts(l, b)
                 if append:
                     self.new_kv[(l, b)] = (np.ascontiguousarray(k[:, n:]), np.ascontiguousarray(v[:, n:]))
                     k, v = np.ascontiguousarray(k[:, :n]), np.ascontiguousarray(v[:, :n])
                 if offload_from_device:
                     kd = torch.from_numpy(k.view(np.int16)).to(self.dev)
                     vd = torch.from_numpy(v.view(np.int16)).to(self.dev)
-                    self.ctx.index_offload_device(b, l, kd, vd)
+                    if self.parts:
+                        self.ctx.index_offload_parts(b, l, kd, vd, order, starts)
+                    else:
+                        self.ctx.index_offload_device(b, l, kd, vd)
                     torch.cuda.synchronize()
                     del kd, vd
+                elif self.parts:
+                    self.ctx.index_offload_parts(b, l, k, v, order, starts)
                 else:
                     self.ctx.index_offload_host(b, l, k, v)
                     torch.cuda.synchronize()  # the host arrays are reused/freed next
                 for h in want.get((l, b), []):
-                    if append:
+                    if self.parts:
+                        self.oracle[(l, b, h)] = O.Unit.from_parts(np.ascontiguousarray(k[h]),
+                                                                   np.ascontiguousarray(v[h]), order[h], starts[h],
+                                                                   w.cap)
+                    elif append:
                         self.oracle[(l, b, h)] = O.TailUnit(np.ascontiguousarray(k[h]), np.ascontiguousarray(v[h]),
                                                             w.cap, append)
                     else:
@@ -233,6 +250,19 @@ class Lockstep:
                     gs = self.ctx.summaries(l, b, h).astype(np.float64)
                     serr = float(np.abs(gs - u.summ).max())
                     assert serr <= 1e-5, f"{where}: summaries differ by {serr}"
+            if self.parts:
+                # variable partitions: the GPU's Index over the same grouping, and (first step)
+                # every resident page byte for byte against the oracle's page of that partition
+                assert u.P == self.ctx.P_lb[l][b], f"{where}: partition count differs"
+                if u.P:
+                    gs = self.ctx.summaries(l, b, h).astype(np.float64)
+                    serr = float(np.abs(gs - u.summ).max())
+                    assert serr <= 1e-5, f"{where}: summaries differ by {serr}"
+                if t == 0:
+                    for s_, p_ in enumerate(ex["slot_part"][ul]):
+                        if p_ >= 0:
+                            pg = self.ctx.read_page(l, b, h, s_)
+                            assert np.array_equal(pg, u.host_pages[p_]), f"{where}: page of partition {p_} differs"
             if u.P == 0 and not (self.append and u.tail_n):
                 assert np.all(g_out == 0), f"{where}: empty request must give zeros"
                 continue
@@ -273,11 +303,7 @@ class Lockstep:
                         match = cand
                         break
                 assert match is not None, f"{where}: GPU set is not one of the valid tie-band sets"
-                if self.append:
-                    fresh = u.clone_empty(self.fresh_cap)
-                else:
-                    fresh = O.Unit(u.ntok, self.fresh_cap)
-                    fresh.summ, fresh.host_pages = u.summ, u.host_pages
+                fresh = u.clone_empty(self.fresh_cap)
                 ss, _, _, _ = fresh.manage(match, 0)
                 o_out = fresh.attend(match, ss, q)
             err = float(np.abs(g_out - o_out).max())

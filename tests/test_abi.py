@@ -45,7 +45,9 @@ def _cfg(**kw):
 @pytest.mark.parametrize("bad", [dict(head_dim=64), dict(part_tokens=32), dict(q_heads=7), dict(topk=0),
                                  dict(topk=1000), dict(buf_mult=0), dict(batch=0), dict(seg_entries=16),
                                  dict(q_heads=2 * 17, kv_heads=2), dict(seg_pool_segments=-1),
-                                 dict(append_tokens=-1), dict(append_tokens=1 << 30)])
+                                 dict(append_tokens=-1), dict(append_tokens=1 << 30), dict(max_partitions=-1),
+                                 dict(max_partitions=(1 << 20) + 1), dict(max_partitions=100, append_tokens=10),
+                                 dict(max_partitions=63)])
 def test_invalid_configs_are_rejected(bad):
     with pytest.raises(B.SpinError) as e:
         B.spin_create(_cfg(**bad))
@@ -72,6 +74,7 @@ def test_null_arguments():
     assert lib.spin_create(None, None) == B.SPIN_ERR_INVALID
     assert lib.spin_decode_step(None, 0, None, None, None) == B.SPIN_ERR_INVALID
     assert lib.spin_stats(None, None) == B.SPIN_ERR_INVALID
+    assert lib.spin_index_offload_parts(None, 0, 0, None, None, 0, None, None, 0, 0, None) == B.SPIN_ERR_INVALID
     lib.spin_destroy(None)
 
 

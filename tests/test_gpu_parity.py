@@ -284,6 +284,83 @@ def test_append_errors():
 
 
 # ---------------------------------------------------------------------------
+# Variable partitions: groups of 1..64 tokens, each in a page of its own.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("mean_part", [20, 48])
+def test_variable_partitions_lockstep_narrow(mean_part):
+    """The generator's grouping (tokens shuffled within 256-token windows, groups of 1..64):
+    ragged contexts, a request with fewer groups than top-k (every group selected, so the
+    output is dense attention over all its tokens), an empty request, GQA 5, 2x buffer.
+    Summaries, the first step's resident pages, selections, page state and outputs follow
+    the oracle over the same grouping."""
+    w = W.Workload("parts", B=4, L=2, Hq=10, Hkv=2, ctx_len=[3000, 777, 100, 0], topk=8, buf_mult=2,
+                   drift_a=0.8, drift_c=0.2, steps=12, seed=51, mean_part=mean_part)
+    ls = Lockstep(w)
+    try:
+        assert ls.ctx.P_lb[1] == [w.var_partitions(b) for b in range(w.B)]
+        for _ in range(w.steps):
+            ls.step()
+        st = ls.ctx.stats()
+        assert st["device_error"] == 0 and st["evictions"] > 0
+        assert ls.report.max_out_err <= OUT_TOL and ls.report.exact_units > 0
+    finally:
+        ls.close()
+
+
+def test_variable_partitions_lockstep_wide():
+    """64 units per layer (the fused score path), GQA 8, K/V offloaded from device memory."""
+    w = W.Workload("parts_wide", B=32, L=1, Hq=16, Hkv=2, ctx_len=[1500 + 37 * b for b in range(32)], topk=6,
+                   buf_mult=3, drift_a=0.8, drift_c=0.2, steps=10, seed=53, mean_part=30)
+    rep, st = _run(w, units=sample_units(w, 16, seed=5), offload_from_device=True)
+    assert st["evictions"] > 0 and rep.max_out_err <= OUT_TOL
+
+
+def test_variable_partitions_errors():
+    """Each offload entry point refuses the other mode; groupings that break the rules are
+    refused before anything is enqueued, and the context stays usable."""
+    from sparse_attention_tiered_gb300 import SpinContext, SpinError
+    from sparse_attention_tiered_gb300._binding import SPIN_ERR_INVALID, SPIN_ERR_STATE
+    w = W.Workload("parts_err", B=1, L=1, Hq=4, Hkv=2, ctx_len=[300], topk=3, buf_mult=2,
+                   drift_a=0.9, drift_c=0.1, steps=1, seed=0, mean_part=30)
+    k, v = w.request_kv(0, 0)
+    order, starts = w.request_parts(0, 0)
+    with SpinContext(w.B, w.L, w.Hq, w.Hkv, w.ctx_len, w.topk, w.buf_mult) as ctx:  # fixed partitions
+        with pytest.raises(SpinError) as e:
+            ctx.index_offload_parts(0, 0, k, v, order, starts)
+        assert e.value.code == SPIN_ERR_STATE
+    with SpinContext.for_workload(w) as ctx:
+        assert ctx.max_partitions == w.max_partitions == 10
+        with pytest.raises(SpinError) as e:
+            ctx.index_offload_host(0, 0, k, v)
+        assert e.value.code == SPIN_ERR_STATE
+        bad = []
+        s1 = starts.copy(); s1[0, 1] = 0                          # an empty partition
+        bad.append((order, s1))
+        s2 = np.array([[0, 65, 300], [0, 150, 300]], np.int32)    # a partition of 65 tokens
+        bad.append((order, s2))
+        s3 = starts.copy(); s3[1, -1] = 299                       # does not end at n_tokens
+        bad.append((order, s3))
+        o4 = order.copy(); o4[0, 5] = o4[0, 6]                     # a token twice
+        bad.append((o4, starts))
+        o5 = order.copy(); o5[1, 0] = 300                          # a token out of range
+        bad.append((o5, starts))
+        s6 = np.tile(np.arange(0, 301, 25, dtype=np.int32), (2, 1))  # 12 partitions > max_partitions
+        bad.append((order, s6))
+        for o_, s_ in bad:
+            with pytest.raises(SpinError) as e:
+                ctx.index_offload_parts(0, 0, k, v, o_, s_)
+            assert e.value.code == SPIN_ERR_INVALID
+        q = torch.from_numpy(w.queries().bf16()[0].view(np.int16)).cuda()
+        out = torch.empty((1, 4, 128), dtype=torch.float32, device="cuda")
+        with pytest.raises(SpinError) as e:  # nothing was offloaded
+            ctx.decode_step(0, q, out)
+        assert e.value.code == SPIN_ERR_STATE
+        ctx.index_offload_parts(0, 0, k, v, order, starts)
+        ctx.decode_step(0, q, out)
+        assert ctx.stats()["device_error"] == 0 and torch.isfinite(out).all()
+
+
+# ---------------------------------------------------------------------------
 # Buffer elasticity: per-request budgets change between steps.
 # ---------------------------------------------------------------------------
 def test_buffer_elasticity_lockstep():
