@@ -105,7 +105,7 @@ def make_workload(args, rank=0):
         w = w.with_(L=args.layers)
     if args.batch:
         w = w.with_(B=args.batch, ctx_len=w.ctx_len[:args.batch])
-    if args.mean_part:
+    if getattr(args, "mean_part", 0):
         w = w.with_(mean_part=args.mean_part)
     return w
 

@@ -235,12 +235,10 @@ int spin_set_buffer(spin_ctx* ctx, int32_t b, int32_t pages, spin_stream_t strea
 int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream);
 
 /* The same step with host buffers: q_host [batch][q_heads][128] bf16 and
- * out_host [batch][q_heads][128] fp32. A buffer that is page-locked and mapped for the
- * device (cudaHostAlloc, cudaHostRegister, torch pin_memory) and 16-byte aligned is used
- * in place: a copy kernel stages q into HBM, and the attention kernel writes out_host
- * directly over the host link. Any other buffer goes through cudaMemcpyAsync, via HBM.
- * Everything is enqueued on `stream`; out_host is valid once the stream has reached the
- * end of the step, and neither buffer may be reused before then. */
+ * out_host [batch][q_heads][128] fp32 (pinned for asynchronous copies). The
+ * host->device copy of q, the step and the device->host copy of out are all
+ * enqueued on `stream`; out_host is valid once the stream has reached that point,
+ * and neither buffer may be reused before then. */
 int spin_decode_step_host(spin_ctx* ctx, int32_t layer, const uint16_t* q_host, float* out_host,
                           spin_stream_t stream);
 

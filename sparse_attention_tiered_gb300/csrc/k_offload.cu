@@ -165,12 +165,6 @@ gather_offload_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict
   if (threadIdx.x == 0) valid_unit0[(int64_t)h * unit_pages + p] = (uint8_t)cnt;
 }
 
-// Plain 16-byte copy, grid-stride; used to stage a query batch from mapped host memory.
-__global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = __ldcs(src + i);
-}
-
 // Read pass over the pinned host store: one 4-byte load every `stride` bytes.
 // The first GPU read of a host page pays for translating its address, and those
 // translations resolve at a limited rate (on GB300 machines, 45-100 GB/s of random
@@ -229,15 +223,6 @@ cudaError_t launch_gather_offload(const uint16_t* k, const uint16_t* v, int64_t 
   dim3 grid((unsigned)n_parts, (unsigned)kv_heads);
   gather_offload_kernel<<<grid, kOffloadThreads, 0, st>>>(k, v, n_tokens, order, starts, n_parts, summ_unit0,
                                                            host_unit0, unit_pages, valid_unit0);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_copy16(const void* src, void* dst, int64_t bytes, int sm_count, cudaStream_t st) {
-  const int64_t n = bytes / 16;  // callers pass multiples of 16 bytes, 16-byte aligned
-  if (n <= 0) return cudaSuccess;
-  const int64_t want = (n + 255) / 256, most = (int64_t)(sm_count > 0 ? sm_count : 1) * 2;
-  const int grid = (int)(want < most ? want : most);
-  copy16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n);
   return cudaGetLastError();
 }
 

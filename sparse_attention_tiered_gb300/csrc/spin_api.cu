@@ -677,20 +677,6 @@ int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStre
   return SPIN_OK;
 }
 
-// Device address of a page-locked, device-mapped host buffer (16-byte aligned), else
-// nullptr: such buffers are read and written in place by the kernels.
-template <class T>
-T* mapped_host_ptr(T* p) {
-  if (reinterpret_cast<uintptr_t>(p) & 15) return nullptr;
-  cudaPointerAttributes at{};
-  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
-  return static_cast<T*>(at.devicePointer);
-}
-
 int check_layer(spin_ctx* c, int layer) {
   if (layer < 0 || layer >= c->L) return fail(c, SPIN_ERR_INVALID, "layer %d outside [0, %d)", layer, c->L);
   for (int b = 0; b < c->B; ++b)
@@ -977,16 +963,13 @@ int spin_decode_step_host(spin_ctx* c, int32_t layer, const uint16_t* q_host, fl
     if ((e = dalloc(c, &lb.out_stage, nq)) != cudaSuccess) return cuda_fail(c, e, "allocating the output buffer");
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const uint16_t* q_map = mapped_host_ptr(q_host);
-  float* out_map = mapped_host_ptr(out_host);
-  if (q_map)
-    SPIN_CUDA(c, launch_copy16(q_map, lb.q_stage, (int64_t)nq * 2, c->sm_count, st), "staging q from host memory");
-  else
-    SPIN_CUDA(c, cudaMemcpyAsync(lb.q_stage, q_host, nq * 2, cudaMemcpyHostToDevice, st), "copying q to the device");
-  rc = enqueue_step(c, layer, lb.q_stage, out_map ? out_map : lb.out_stage, st);
+  // Copy-engine transfers on both sides. Using mapped pinned buffers in place (a kernel
+  // staging q, the combine writing out over the host link) measured about 70 us slower
+  // per layer call on GB300.
+  SPIN_CUDA(c, cudaMemcpyAsync(lb.q_stage, q_host, nq * 2, cudaMemcpyHostToDevice, st), "copying q to the device");
+  rc = enqueue_step(c, layer, lb.q_stage, lb.out_stage, st);
   if (rc) return rc;
-  if (!out_map)
-    SPIN_CUDA(c, cudaMemcpyAsync(out_host, lb.out_stage, nq * 4, cudaMemcpyDeviceToHost, st), "copying out to the host");
+  SPIN_CUDA(c, cudaMemcpyAsync(out_host, lb.out_stage, nq * 4, cudaMemcpyDeviceToHost, st), "copying out to the host");
   return SPIN_OK;
 }
 

@@ -108,7 +108,6 @@ cudaError_t launch_gather_offload(const uint16_t* k, const uint16_t* v, int64_t 
                                   uint16_t* host_unit0, int64_t unit_pages, uint8_t* valid_unit0, cudaStream_t st);
 cudaError_t launch_warm_store(const void* store, int64_t bytes, int64_t stride, uint32_t* sink, int sm_count,
                               cudaStream_t st);
-cudaError_t launch_copy16(const void* src, void* dst, int64_t bytes, int sm_count, cudaStream_t st);
 cudaError_t launch_score(const LayerArgs& a, cudaStream_t st);
 // KV append of one token per request of the layer (tail mode).
 cudaError_t launch_append(const LayerArgs& a, const uint16_t* k_new, const uint16_t* v_new, int32_t* P_b,
