@@ -226,7 +226,8 @@ int spin_set_buffer(spin_ctx* ctx, int32_t b, int32_t pages, spin_stream_t strea
  * the k selected partitions of the query head's KV head, plus, in tail mode, the
  * request's tail tokens (zeros for an empty request). Asynchronous on `stream`; the layer's step counter t advances by one
  * per call. Requires every request of `layer` to have been offloaded.
- * The first step after any spin_index_offload call (of any layer) first enqueues one read
+ * The first step after any spin_index_offload or spin_index_offload_parts call (of any
+ * layer) first enqueues one read
  * pass over the whole host store: a 4-byte load every host page (at most every 32 KiB).
  * The GPU translates each host page's address on its first read, and those translations
  * resolve slowly; the pass pays for them once, so the steps' retrieval does not.
