@@ -48,6 +48,12 @@ def parse():
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs)")
     ap.add_argument("--mean-part", type=int, default=0,
                     help="variable partitions of 1-64 tokens averaging about this many (a seeded grouping)")
+    ap.add_argument("--append", action="store_true",
+                    help="KV append: one new token per request per layer before every decode step (tail mode)")
+    ap.add_argument("--budget", type=int, default=0,
+                    help="resident budget in pages per unit for every request (buffer elasticity), topk..cap")
+    ap.add_argument("--tier-split", action="store_true",
+                    help="second-level segment entries in pinned host memory")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
@@ -285,7 +291,8 @@ def bench_reference(args):
 def bench_spin(args):
     import torch
     from sparse_attention_tiered_gb300 import SpinContext
-    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_HOST_HUGEPAGES, SPIN_FLAG_STAGE_TIMING
+    from sparse_attention_tiered_gb300._binding import (SPIN_FLAG_HOST_HUGEPAGES, SPIN_FLAG_STAGE_TIMING,
+                                                        SPIN_FLAG_TIER_SPLIT)
 
     R = Ranks()
     world, rank, local = R.world, R.rank, R.local
@@ -299,11 +306,18 @@ def bench_spin(args):
 
     w = make_workload(args, rank)
     K, Wm = args.steps, max(3, args.warmup)
+    n_steps_total = Wm + K + (0 if args.no_e2e else K)
+    if args.append and w.mean_part:
+        raise SystemExit("--append and --mean-part cannot be combined (tail mode has fixed partitions)")
+    if args.budget and not (w.topk <= args.budget <= w.cap):
+        raise SystemExit(f"--budget must be in [{w.topk}, {w.cap}]")
 
     # ---- set-up (untimed): Index + Offload of every request and layer ----
     t_setup = time.perf_counter()
     flags = SPIN_FLAG_STAGE_TIMING | (SPIN_FLAG_HOST_HUGEPAGES if args.host_alloc == "hugepages" else 0)
-    ctx = SpinContext.for_workload(w, device=local, flags=flags)
+    flags |= SPIN_FLAG_TIER_SPLIT if args.tier_split else 0
+    ctx = SpinContext.for_workload(w, device=local, flags=flags,
+                                   **({"append_tokens": n_steps_total} if args.append else {}))
     kbuf = vbuf = None
     keep = []
     for l in range(w.L):
@@ -319,10 +333,22 @@ def bench_spin(args):
             else:
                 ctx.index_offload_host(b, l, kbuf, vbuf)
             torch.cuda.synchronize()
+    if args.budget:
+        for b in range(w.B):
+            ctx.set_buffer(b, args.budget)
+        torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
 
+    # ---- appended tokens (tail mode): seeded bf16 N(0,1) K and V, [step][layer][k|v][B][Hkv][128] ----
+    kv_host = kv_dev = kv_stage = None
+    if args.append:
+        gen = torch.Generator().manual_seed(1000 + rank)
+        kv_host = torch.randn((n_steps_total, w.L, 2, w.B, w.Hkv, 128), generator=gen).to(torch.bfloat16)
+        kv_host = kv_host.view(torch.int16).pin_memory()
+        kv_dev = kv_host[:Wm + K].to(dev)
+        kv_stage = torch.empty((2, w.B, w.Hkv, 128), dtype=torch.int16, device=dev)
+
     # ---- queries for every step, resident in HBM (and pinned on the host for e2e) ----
-    n_steps_total = Wm + K + (0 if args.no_e2e else K)
     qs = w.queries()
     q_host = torch.empty((n_steps_total, w.L, w.B, w.Hq, 128), dtype=torch.int16).pin_memory()
     for t in range(n_steps_total):
@@ -334,6 +360,8 @@ def bench_spin(args):
 
     def step(t):
         for l in range(w.L):
+            if args.append:
+                ctx.append_kv(l, kv_dev[t, l, 0], kv_dev[t, l, 1], stream)
             ctx.decode_step(l, q_dev[t, l], out[l], stream)
 
     hbm_gbs, peak_src = measured_peaks()
@@ -373,7 +401,7 @@ def bench_spin(args):
     traffic = attention_traffic(sel_bytes_per_launch)
     combined_ideal_s = d["selected_bytes"] / (hbm_gbs * 1e9) + d["retrieved_bytes"] / (host_gbs * 1e9)
     summ_ideal_s = K * w.summary_bytes_per_step() / (hbm_gbs * 1e9)
-    gpu_launches = K * w.L * (2 if (w.B * w.Hkv >= 64 and w.p_max <= 4096) else 3)
+    gpu_launches = K * w.L * ((2 if (w.B * w.Hkv >= 64 and w.p_max <= 4096) else 3) + (1 if args.append else 0))
 
     # ---- end to end through the host-buffer entry point ----
     e2e = None
@@ -384,12 +412,16 @@ def bench_spin(args):
         a0.record()
         for t in range(Wm + K, Wm + 2 * K):
             for l in range(w.L):
+                if args.append:  # the new token's K and V come from host memory too
+                    kv_stage.copy_(kv_host[t, l], non_blocking=True)
+                    ctx.append_kv(l, kv_stage[0], kv_stage[1], stream)
                 ctx.decode_step_host(l, q_host[t, l].data_ptr(), o_host[l].data_ptr(), stream)
         a1.record()
         barrier()
         ms_e2e = R.max(a0.elapsed_time(a1))
         e2e = {"value": job_tokens_per_s(w.B * K, world, ms_e2e), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(q_host[0].numel() * 2), "d2h_bytes_per_step": int(o_host.numel() * 4)}
+               "h2d_bytes_per_step": int(q_host[0].numel() * 2 + (kv_host[0].numel() * 2 if args.append else 0)),
+               "d2h_bytes_per_step": int(o_host.numel() * 4)}
     st2 = ctx.stats()
     ctx.close()
 
@@ -408,7 +440,11 @@ def bench_spin(args):
                        "parallelism": f"dp{world} (independent requests per GPU)", "timed_decode_steps": K,
                        "first_timed_step": Wm,
                        "host_store": ("cudaHostAlloc" if args.host_alloc == "cuda"
-                                      else "huge-page mmap + cudaHostRegister")},
+                                      else "huge-page mmap + cudaHostRegister"),
+                       **({"append": "one token per request per layer before each decode step (tail mode)"}
+                          if args.append else {}),
+                       **({"budget_pages_per_unit": args.budget} if args.budget else {}),
+                       **({"metadata": "segment entries in pinned host memory"} if args.tier_split else {})},
             "roofline": {"bound": "host_link" if host_bound else "hbm", "kernel": "attend_retrieve_kernel",
                          "achieved": host_achieved if host_bound else hbm_achieved,
                          "peak": host_gbs if host_bound else hbm_gbs, "unit": "GB/s",
