@@ -346,6 +346,17 @@ def check_step_consistency(lib):
         assert np.array_equal(r["sel"], sel) and np.array_equal(r["sel_slot"], ss)
         assert np.array_equal(r["out"], out)
         qs.advance()
+    # the threaded many-unit driver (CPU timing) gives each unit its own one-call step
+    units = [O.Unit(kb.shape[0], cap=w.cap, k_bits=kb, v_bits=vb, lib=lib) for _ in range(3)]
+    ref = O.Unit(kb.shape[0], cap=w.cap, k_bits=kb, v_bits=vb, lib=lib)
+    qs = w.queries()
+    for t in range(3):
+        q = qs.bf16()[0, 0, 1:2]
+        _, keep = O.step_units_parallel(units, [q] * 3, w.topk, t, threads=2, lib=lib)
+        r = ref.step(q, w.topk, t)
+        for (_, sel, _, _, out) in keep:
+            assert np.array_equal(sel[:len(r["sel"])], r["sel"]) and np.array_equal(out, r["out"])
+        qs.advance()
 
 
 def check_append_tail(lib):
