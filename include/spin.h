@@ -15,10 +15,12 @@
  * gist.science/pt "Unifying Sparse Attention with Hierarchical Memory…" (below [GS]),
  * section 2 A-C.
  *
- * Fixed geometry: head_dim 128, partition = page = 64 tokens of one KV head,
- * second-level segment = 64 directory-adjacent partitions, 64 LRU buckets.
- * A page is stored as K[64][128] then V[64][128], bf16 (uint16 bits),
- * token-major, zero padded past the last valid token: 32768 bytes.
+ * Fixed geometry: head_dim 128; a page holds one partition of one KV head: 64
+ * consecutive tokens, or, in a context with max_partitions > 0, a group of 1 to 64
+ * tokens that the caller's Index chose; second-level segment = 64
+ * directory-adjacent partitions; 64 LRU buckets. A page is stored as K[64][128]
+ * then V[64][128], bf16 (uint16 bits), token-major, zero padded past the last
+ * valid token: 32768 bytes.
  *
  * Units. A unit is one (request b, layer l, KV head h). Query head hq belongs to
  * KV head hq / G with G = q_heads / kv_heads (grouped-query attention).
@@ -28,7 +30,8 @@
  * spin_create to spin_destroy: the HBM page pool, the two-level tables, the
  * partition summaries, the pinned host page store, per-layer scratch, its
  * internal streams and events. KV sources passed to spin_index_offload are
- * copied and may be freed when that call's stream work has completed.
+ * copied and may be freed when that call's stream work has completed; those
+ * passed to spin_index_offload_parts may be freed when the call returns.
  *
  * Errors. Every int-returning call returns a spin_status. No call throws, traps
  * or aborts. Kernels report device-side conditions (pool exhausted, a bounded
@@ -144,7 +147,8 @@ typedef struct spin_stats_t {
 /* Host-side view filled by spin_debug_export; any pointer may be NULL. Shapes use
  * U = batch * kv_heads units of the layer (unit ul = b * kv_heads + h), k = topk,
  * cap = buf_mult * topk, Pmax = the largest partition count of any request (in tail
- * mode: the largest count a request can reach, ceil((ctx_len + append_tokens) / 64)). */
+ * mode: the largest count a request can reach, ceil((ctx_len + append_tokens) / 64);
+ * with variable partitions: max_partitions). */
 typedef struct spin_state_view {
   int32_t* keff;       /* [U] partitions selected in the last step = min(k, P_b) */
   int32_t* sel;        /* [U][k] selected partitions of the last step, ascending, -1 padded */
@@ -159,10 +163,12 @@ typedef struct spin_state_view {
 } spin_state_view;
 
 /* Create a context: validates cfg, allocates the pinned host page store
- * (sum_b ceil(ctx_len[b]/64) * L * Hkv pages), the HBM page pool (B*L*Hkv*cap
- * pages), the summaries, the two-level tables (directory [units][ceil(Pmax/64)],
- * shared segment pool) and per-layer scratch, on cfg->device. Every page starts
- * on the host and the GPU holds nothing. *out is set only on SPIN_OK. */
+ * (sum_b S_b * L * Hkv pages, S_b = ceil(ctx_len[b]/64); ceil((ctx_len[b] +
+ * append_tokens)/64) in tail mode; max_partitions with variable partitions), the
+ * HBM page pool (B*L*Hkv*cap pages, plus one tail page per unit in tail mode), the
+ * summaries, the two-level tables (directory [units][ceil(Pmax/64)], shared
+ * segment pool) and per-layer scratch, on cfg->device. Every page starts on the
+ * host and the GPU holds nothing. *out is set only on SPIN_OK. */
 int spin_create(const spin_config* cfg, spin_ctx** out);
 
 /* Index + Offload ([XT] §1, Fig 3; [GS] §2A) of request b in `layer`:
@@ -224,15 +230,16 @@ int spin_set_buffer(spin_ctx* ctx, int32_t b, int32_t pages, spin_stream_t strea
  * §3; [GS] §2B-C). q: device bf16 [batch][q_heads][128]; out: device fp32
  * [batch][q_heads][128] = softmax(q K_sel^T / sqrt(128)) V_sel over the tokens of
  * the k selected partitions of the query head's KV head, plus, in tail mode, the
- * request's tail tokens (zeros for an empty request). Asynchronous on `stream`; the layer's step counter t advances by one
- * per call. Requires every request of `layer` to have been offloaded.
- * The first step after any spin_index_offload or spin_index_offload_parts call (of any
- * layer) first enqueues one read
- * pass over the whole host store: a 4-byte load every host page (at most every 32 KiB).
- * The GPU translates each host page's address on its first read, and those translations
- * resolve slowly; the pass pays for them once, so the steps' retrieval does not.
- * Environment variable SPIN_STORE_WARM, read by spin_create, sets the number of passes:
- * 0 to 8, default 1; 0 turns the pass off. */
+ * request's tail tokens (zeros for an empty request). Asynchronous on `stream`; the
+ * layer's step counter t advances by one per call. Requires every request of `layer`
+ * to have been offloaded.
+ * The first step after any spin_index_offload or spin_index_offload_parts call (of
+ * any layer) first enqueues one read pass over the whole host store: a 4-byte load
+ * every host page (at most every 32 KiB). The GPU translates each host page's
+ * address on its first read, and those translations resolve slowly; the pass pays
+ * for them once, so the steps' retrieval does not. Environment variable
+ * SPIN_STORE_WARM, read by spin_create, sets the number of passes: 0 to 8, default
+ * 1; 0 turns the pass off. */
 int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream);
 
 /* The same step with host buffers: q_host [batch][q_heads][128] bf16 and
