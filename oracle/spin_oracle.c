@@ -19,14 +19,16 @@
  * plainest reading and says so ("reading:").
  *
  * Layout conventions (shared with the tests, not with the CUDA code):
- *   a partition = a page = 64 consecutive tokens of one KV head (reading of
- *   [XT] §1 "分区" + [GS] §2B "Páginas Físicas por Cabeça"); head_dim = 128;
- *   a page in page format is K[64][128] then V[64][128], bf16, token-major,
- *   zero padded past the last valid token.
+ *   a partition = a page of one KV head (reading of [XT] §1 "分区" + [GS] §2B
+ *   "Páginas Físicas por Cabeça"): 64 consecutive tokens, or, for variable
+ *   partitions, a group of 1 to 64 tokens given as a token order and
+ *   boundaries; head_dim = 128; a page in page format is K[64][128] then
+ *   V[64][128], bf16, token-major, zero padded past the last valid token.
  *
- * Parity pins: every function here is pinned by tests/test_oracle_pins.py
- * (dense-attention identity, brute-force top-k, LRU invariants, page-table
- * round trip, closed-form summaries, byte-equal retrieve).
+ * Parity pins: every function here is pinned by tests/oracle_pins.py, run by
+ * tests/test_oracle_pins.py and tests/test_oracle_properties.py (dense-attention
+ * identity, brute-force top-k, LRU invariants, page-table round trip,
+ * closed-form summaries, byte-equal retrieve, variable-partition means).
  */
 #include <math.h>
 #include <stdint.h>
