@@ -7,10 +7,12 @@
 //   * two-level page table: a static directory [units][ceil(Pmax/64)] whose
 //     entries point to 64-entry segments drawn on demand from one shared pool;
 //   * per-page state: slot -> partition, last-use step (bucketed-LRU timestamps);
-//   * fp32 partition summaries in HBM.
+//   * fp32 partition summaries in HBM;
+//   * with variable partitions (max_partitions > 0), one token count per host page.
 // A decode step of one layer enqueues up to three kernels on the caller's stream:
 // score (only for narrow layers) -> select+manage -> retrieve+attention+combine
-// (cooperative).
+// (cooperative); the first step after an offload call adds one read pass over the
+// host store, and a KV append (tail mode) adds the append kernel before the step.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
