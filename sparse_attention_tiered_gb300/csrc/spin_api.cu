@@ -12,7 +12,8 @@
 // A decode step of one layer enqueues up to three kernels on the caller's stream:
 // score (only for narrow layers) -> select+manage -> retrieve+attention+combine
 // (cooperative); the first step after an offload call adds one read pass over the
-// host store, and a KV append (tail mode) adds the append kernel before the step.
+// host store. A KV append (spin_append_kv, tail mode) is a kernel of its own that the
+// caller enqueues before the step.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
