@@ -3,12 +3,20 @@
 
 One step = one decode step of the whole workload: every layer's call of
 spin_decode_step (Select -> two-level resolve -> bucketed LRU -> Retrieve ->
-sparse attention -> combine) over the whole batch. The default workload is the
+sparse attention -> combine) over the whole batch. The headline workload is the
 Qwen3-14B-shaped batch (32 requests x 8 layers x 8 KV heads, 32K tokens,
-top-32 partitions, 5x buffer). Prints one JSON line.
+top-32 partitions, 5x buffer): W warm-up steps, then K timed steps, then K steps
+end to end through the host-buffer entry point. Prints one JSON line.
+
+The line's "configs" object then records every workload (Qwen3-14B, Llama-3.1-70B,
+the eviction/metadata stress at 1x and 5x buffer, the 1M-token request, tiny) over
+all its configured decode steps, each on a fresh context, next to the oracle timed on
+a bounded sample of the same workload, plus the Qwen workload with KV append, a 2x
+resident budget and tier-split metadata.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl spin|reference]
                   [--workload NAME] [--layers L] [--batch B] [--no-e2e] [--no-cpu-baseline]
+                  [--no-configs]
 
 --impl reference times the CPU oracle (the plain double-precision restatement)
 on the host cores on a bounded sample of the same workload.
@@ -56,6 +64,10 @@ def parse():
                     help="second-level segment entries in pinned host memory")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload record (every workload over all its decode steps)")
+    ap.add_argument("--config-cpu-seconds", type=float, default=3.0,
+                    help="target CPU work of each workload's oracle sample in the per-workload record")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU work of the oracle sample")
     ap.add_argument("--host-alloc", default="cuda", choices=["cuda", "hugepages"],
                     help="pinned host page store: cudaHostAlloc (default) or huge-page mmap + cudaHostRegister")
@@ -190,46 +202,75 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def host_link_peak_gbs(torch, dev, nbytes=1 << 30, reps=5):
-    """Pinned host -> device cudaMemcpyAsync bandwidth (1 GiB copies, best of reps)."""
-    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
-    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
-    best = 0.0
-    for _ in range(reps):
+def host_link_peaks(torch, dev):
+    """Host -> device link ceilings measured in this run (GB/s = 1e9 bytes/s), each the
+    best of a few repetitions:
+      copy_1x1GiB     one 1 GiB pinned -> HBM cudaMemcpyAsync
+      copy_2x256MiB   two concurrent 256 MiB copies on separate streams
+      copy_4x256MiB   four concurrent 256 MiB copies on separate streams
+      sm_read_4GiB    SM zero-copy 16-byte reads streaming 4 GiB of pinned memory
+                      (spin_measure_host_read, the retrievers' access path)
+    The peak used for the roofline is the largest of them."""
+    from sparse_attention_tiered_gb300 import spin_measure_host_read
+    GiB = 1 << 30
+    src = torch.empty(4 * GiB, dtype=torch.uint8).pin_memory()
+    src[::4096] = 1
+    dst = torch.empty(GiB, dtype=torch.uint8, device=dev)
+
+    def copies(n_streams, nbytes):
+        streams = [torch.cuda.Stream() for _ in range(n_streams)]
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
         a.record()
-        dst.copy_(src, non_blocking=True)
+        done = []
+        for i, st in enumerate(streams):
+            st.wait_event(a)
+            with torch.cuda.stream(st):
+                dst[i * nbytes:(i + 1) * nbytes].copy_(src[i * nbytes:(i + 1) * nbytes], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(st)
+            done.append(e)
+        for e in done:
+            torch.cuda.current_stream().wait_event(e)
         b.record()
         torch.cuda.synchronize()
-        best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+        return n_streams * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
+
+    out = {"copy_1x1GiB": max(copies(1, GiB) for _ in range(4)),
+           "copy_2x256MiB": max(copies(2, 256 << 20) for _ in range(4)),
+           "copy_4x256MiB": max(copies(4, 256 << 20) for _ in range(4)),
+           "sm_read_4GiB": max(spin_measure_host_read(src.data_ptr(), 4 * GiB, 1) for _ in range(3))}
     del src, dst
-    return best
+    torch.cuda.synchronize()
+    return {k: round(v, 2) for k, v in out.items()}
 
 
 def attention_traffic(ppl_bytes):
-    """Per-launch DRAM bytes of the attention kernel from the committed ncu summary, when it
-    was taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "attention_traffic.json")
-    src = os.path.join(ROOT, "sparse_attention_tiered_gb300", "csrc", "k_attend.cu")
+    """Per-launch DRAM bytes of the decode-step kernel from the committed ncu summary, when it
+    was taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()
-    if d.get("source_sha256") != h:
+    h = hashlib.sha256()
+    for name in ("k_step.cu", "select_dev.cuh"):
+        with open(os.path.join(ROOT, "sparse_attention_tiered_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if d.get("source_sha256") != h.hexdigest():
         return None
-    # scale the captured launch to this workload's per-launch selected bytes
-    return int(d["dram_bytes_per_selected_byte"] * ppl_bytes)
+    # scale the captured launch to this workload's per-launch algorithmic HBM bytes
+    return int(d["dram_bytes_per_algorithmic_byte"] * ppl_bytes)
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
 
-def run_oracle_sample(w, steps_budget, cpu_seconds):
+def run_oracle_sample(w, steps_budget, cpu_seconds, threads=0):
     """Times the oracle on the units of request 0 (all layers, all KV heads) for as many
-    decode steps as fit in about `cpu_seconds`; returns (tokens/s, threads, sample text)."""
+    decode steps as fit in about `cpu_seconds` (threads: 0 = every host core); returns
+    (tokens/s, threads used, sample text)."""
     import oracle as O
     units, qgroup = [], []
     for l in range(w.L):
@@ -244,7 +285,7 @@ def run_oracle_sample(w, steps_budget, cpu_seconds):
             qgroup.append((l, h))
         del k, v
     qs = w.queries()
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     done, elapsed, t = 0, 0.0, 0
     while t < max(1, steps_budget):
         qb = qs.bf16()
@@ -277,7 +318,7 @@ def bench_reference(args):
             "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 / tok_s if tok_s else None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator; no dataset)",
-            "config": {"workload": workload_desc(w), "sample": "oracle on host cores"},
+            "config": headline_config(w, args, int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -288,11 +329,137 @@ def bench_reference(args):
 # GPU path
 # ---------------------------------------------------------------------------
 
-def bench_spin(args):
+def make_context(w, args, local, extra_flags=0, append_tokens=0, rank=0):
+    """Context with every request of every layer indexed and offloaded (set-up, untimed)."""
     import torch
     from sparse_attention_tiered_gb300 import SpinContext
-    from sparse_attention_tiered_gb300._binding import (SPIN_FLAG_HOST_HUGEPAGES, SPIN_FLAG_STAGE_TIMING,
-                                                        SPIN_FLAG_TIER_SPLIT)
+    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_HOST_HUGEPAGES, SPIN_FLAG_STAGE_TIMING
+    flags = SPIN_FLAG_STAGE_TIMING | (SPIN_FLAG_HOST_HUGEPAGES if args.host_alloc == "hugepages" else 0) | extra_flags
+    ctx = SpinContext.for_workload(w, device=local, flags=flags,
+                                   **({"append_tokens": append_tokens} if append_tokens else {}))
+    kbuf = vbuf = None
+    keep = []
+    for l in range(w.L):
+        for b in range(w.B):
+            n = w.ctx_len[b]
+            if kbuf is None or kbuf.shape[1] != n:
+                torch.cuda.synchronize()
+                keep = [torch.empty((w.Hkv, n, 128), dtype=torch.int16).pin_memory() for _ in range(2)]
+                kbuf, vbuf = (t_.numpy().view(np.uint16) for t_ in keep)
+            w.request_kv(l, b, kbuf, vbuf)
+            if w.mean_part:
+                ctx.index_offload_parts(b, l, kbuf, vbuf, *w.request_parts(l, b))
+            else:
+                ctx.index_offload_host(b, l, kbuf, vbuf)
+            torch.cuda.synchronize()
+    return ctx
+
+
+def stats_delta(st1, st0):
+    keys = ("hits", "misses", "evictions", "retrieved_bytes", "selected_bytes", "timed_calls", "ms_score", "ms_manage",
+            "ms_pages", "ms_combine", "ms_kernel", "lru_rounds", "steps")
+    return {k2: st1[k2] - st0[k2] for k2 in keys}
+
+
+def roofline_terms(w, d, ms_total, hbm_gbs, host_gbs, steps):
+    """Combined roofline of `steps` decode steps measured in ms_total milliseconds:
+    (selected KV bytes / HBM GB/s + retrieved bytes / host-link GB/s) / measured time; the
+    stricter fraction also counts the summaries Select reads."""
+    ideal = d["selected_bytes"] / (hbm_gbs * 1e9) + d["retrieved_bytes"] / (host_gbs * 1e9)
+    summ = steps * w.summary_bytes_per_step() / (hbm_gbs * 1e9)
+    t = ms_total * 1e-3
+    return {"frac": ideal / t if t else None, "frac_with_summaries": (ideal + summ) / t if t else None}
+
+
+def run_config(w, args, local, hbm_gbs, host_gbs, extra_flags=0, budget=0, append=False, oracle_seconds=0.0,
+               warm_steps=0):
+    """Runs every decode step of a workload (its configured count) on a fresh context and
+    reports throughput over all steps and over the steps after `warm_steps`, the paging
+    record, the roofline fractions and, optionally, the oracle on a bounded sample."""
+    import torch
+    dev = torch.device(f"cuda:{local}")
+    steps = w.steps
+    t_setup = time.perf_counter()
+    ctx = make_context(w, args, local, extra_flags, append_tokens=steps if append else 0)
+    if budget:
+        for b in range(w.B):
+            ctx.set_buffer(b, budget)
+    setup_s = time.perf_counter() - t_setup
+    qs = w.queries()
+    q_dev = torch.empty((steps, w.L, w.B, w.Hq, 128), dtype=torch.int16)
+    for t in range(steps):
+        q_dev[t].copy_(torch.from_numpy(qs.bf16().view(np.int16)))
+        qs.advance()
+    q_dev = q_dev.to(dev)
+    kv = None
+    if append:
+        gen = torch.Generator().manual_seed(1000)
+        kv = torch.randn((steps, w.L, 2, w.B, w.Hkv, 128), generator=gen).to(torch.bfloat16).view(torch.int16).to(dev)
+    out = torch.empty((w.L, w.B, w.Hq, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    st0 = ctx.stats()
+    ev[0].record()
+    stw = None
+    for t in range(steps):
+        for l in range(w.L):
+            if append:
+                ctx.append_kv(l, kv[t, l, 0], kv[t, l, 1], stream)
+            ctx.decode_step(l, q_dev[t, l], out[l], stream)
+        ev[t + 1].record()
+        if t + 1 == warm_steps:
+            torch.cuda.synchronize()
+            stw = ctx.stats()
+    torch.cuda.synchronize()
+    st1 = ctx.stats()
+    ms_step = [ev[t].elapsed_time(ev[t + 1]) for t in range(steps)]
+    d_all = stats_delta(st1, st0)
+    d_w = stats_delta(st1, stw) if stw is not None else d_all
+    ms_all, ms_w = sum(ms_step), sum(ms_step[warm_steps:])
+    calls_w = max(1, d_w["timed_calls"])
+    r = {
+        "workload": workload_desc(w), "steps": steps, "steady_from_step": warm_steps,
+        "tokens_per_s_all_steps": w.B * steps / (ms_all * 1e-3),
+        "tokens_per_s_steady": w.B * (steps - warm_steps) / (ms_w * 1e-3) if ms_w else None,
+        "ms_per_step_first": ms_step[0], "ms_per_step_steady": ms_w / max(1, steps - warm_steps),
+        "combined_roofline_all_steps": roofline_terms(w, d_all, ms_all, hbm_gbs, host_gbs, steps),
+        "combined_roofline_steady": roofline_terms(w, d_w, ms_w, hbm_gbs, host_gbs, steps - warm_steps),
+        "host_link_gbs_steady": d_w["retrieved_bytes"] / (ms_w * 1e-3) / 1e9 if ms_w else None,
+        "hbm_selected_gbs_steady": d_w["selected_bytes"] / (ms_w * 1e-3) / 1e9 if ms_w else None,
+        "stages_ms_per_layer_call_steady": {k2[3:]: d_w[k2] / calls_w for k2 in
+                                            ("ms_score", "ms_manage", "ms_pages", "ms_combine", "ms_kernel")},
+        "paging_all_steps": {"hits": d_all["hits"], "misses": d_all["misses"], "evictions": d_all["evictions"],
+                             "lru_rounds": d_all["lru_rounds"], "retrieved_bytes": d_all["retrieved_bytes"]},
+        "metadata": {"metadata_bytes": st1["metadata_bytes"], "flat_table_bytes": st1["flat_table_bytes"],
+                     "flat_over_metadata": st1["flat_table_bytes"] / max(1, st1["metadata_bytes"]),
+                     "live_segments": st1["live_segments"], "pool_segments": st1["pool_segments"]},
+        "setup_s": setup_s, "device_error": st1["device_error"],
+    }
+    ctx.close()
+    del q_dev, out, kv
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if oracle_seconds > 0:
+        tok_s, threads, sample = run_oracle_sample(w, 100000, oracle_seconds)
+        r["oracle"] = {"tokens_per_s": tok_s, "cores": threads, "sample": sample}
+    return r
+
+
+def headline_config(w, args, world):
+    return {"workload": workload_desc(w), "l2": "inputs larger than L2 (selected KV per layer "
+            f"{w.selected_kv_bytes_per_step() // w.L / 2**20:.0f} MiB > 129 MB)",
+            "parallelism": f"dp{world} (independent requests per GPU)", "timed_decode_steps": args.steps,
+            "first_timed_step": max(3, args.warmup),
+            "host_store": "cudaHostAlloc" if args.host_alloc == "cuda" else "huge-page mmap + cudaHostRegister",
+            **({"append": "one token per request per layer before each decode step (tail mode)"} if args.append else {}),
+            **({"budget_pages_per_unit": args.budget} if args.budget else {}),
+            **({"metadata": "segment entries in pinned host memory"} if args.tier_split else {})}
+
+
+def bench_spin(args):
+    import torch
+    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_TIER_SPLIT
 
     R = Ranks()
     world, rank, local = R.world, R.rank, R.local
@@ -312,27 +479,14 @@ def bench_spin(args):
     if args.budget and not (w.topk <= args.budget <= w.cap):
         raise SystemExit(f"--budget must be in [{w.topk}, {w.cap}]")
 
+    hbm_gbs, peak_src = measured_peaks()
+    links = host_link_peaks(torch, dev)
+    host_gbs = max(links.values())
+
     # ---- set-up (untimed): Index + Offload of every request and layer ----
     t_setup = time.perf_counter()
-    flags = SPIN_FLAG_STAGE_TIMING | (SPIN_FLAG_HOST_HUGEPAGES if args.host_alloc == "hugepages" else 0)
-    flags |= SPIN_FLAG_TIER_SPLIT if args.tier_split else 0
-    ctx = SpinContext.for_workload(w, device=local, flags=flags,
-                                   **({"append_tokens": n_steps_total} if args.append else {}))
-    kbuf = vbuf = None
-    keep = []
-    for l in range(w.L):
-        for b in range(w.B):
-            n = w.ctx_len[b]
-            if kbuf is None or kbuf.shape[1] != n:
-                torch.cuda.synchronize()
-                keep = [torch.empty((w.Hkv, n, 128), dtype=torch.int16).pin_memory() for _ in range(2)]
-                kbuf, vbuf = (t_.numpy().view(np.uint16) for t_ in keep)
-            w.request_kv(l, b, kbuf, vbuf)
-            if w.mean_part:
-                ctx.index_offload_parts(b, l, kbuf, vbuf, *w.request_parts(l, b))
-            else:
-                ctx.index_offload_host(b, l, kbuf, vbuf)
-            torch.cuda.synchronize()
+    ctx = make_context(w, args, local, SPIN_FLAG_TIER_SPLIT if args.tier_split else 0,
+                       append_tokens=n_steps_total if args.append else 0, rank=rank)
     if args.budget:
         for b in range(w.B):
             ctx.set_buffer(b, args.budget)
@@ -364,9 +518,6 @@ def bench_spin(args):
                 ctx.append_kv(l, kv_dev[t, l, 0], kv_dev[t, l, 1], stream)
             ctx.decode_step(l, q_dev[t, l], out[l], stream)
 
-    hbm_gbs, peak_src = measured_peaks()
-    host_gbs = host_link_peak_gbs(torch, dev)
-
     for t in range(Wm):
         step(t)
     torch.cuda.synchronize()
@@ -388,20 +539,18 @@ def bench_spin(args):
     ms = R.max(ms_rank)
     value = job_tokens_per_s(w.B * K, world, ms)
 
-    d = {k2: st1[k2] - st0[k2] for k2 in ("hits", "misses", "evictions", "retrieved_bytes", "selected_bytes",
-                                          "timed_calls", "ms_select", "ms_manage", "ms_retrieve", "ms_attention",
-                                          "ms_combine", "lru_rounds")}
+    d = stats_delta(st1, st0)
     calls = max(1, d["timed_calls"])
-    att_ms = d["ms_attention"] / calls          # the fused retrieve + attention kernel, per layer call
-    sel_bytes_per_launch = d["selected_bytes"] / calls
-    ret_bytes_per_launch = d["retrieved_bytes"] / calls
-    hbm_achieved = sel_bytes_per_launch / (att_ms * 1e-3) / 1e9 if att_ms > 0 else 0.0
-    host_achieved = ret_bytes_per_launch / (att_ms * 1e-3) / 1e9 if att_ms > 0 else 0.0
-    host_bound = ret_bytes_per_launch / host_gbs >= sel_bytes_per_launch / hbm_gbs
-    traffic = attention_traffic(sel_bytes_per_launch)
-    combined_ideal_s = d["selected_bytes"] / (hbm_gbs * 1e9) + d["retrieved_bytes"] / (host_gbs * 1e9)
-    summ_ideal_s = K * w.summary_bytes_per_step() / (hbm_gbs * 1e9)
-    gpu_launches = K * w.L * ((2 if (w.B * w.Hkv >= 64 and w.p_max <= 4096) else 3) + (1 if args.append else 0))
+    kern_ms = d["ms_kernel"] / calls                    # the decode-step kernel, per layer call
+    sel_b = d["selected_bytes"] / calls                 # algorithmic bytes per launch
+    summ_b = w.summary_bytes_per_step() / w.L
+    ret_b = d["retrieved_bytes"] / calls
+    hbm_b = sel_b + summ_b
+    hbm_achieved = hbm_b / (kern_ms * 1e-3) / 1e9 if kern_ms > 0 else 0.0
+    host_achieved = ret_b / (kern_ms * 1e-3) / 1e9 if kern_ms > 0 else 0.0
+    host_bound = ret_b / host_gbs >= hbm_b / hbm_gbs
+    traffic = attention_traffic(hbm_b)
+    gpu_launches = K * w.L * (1 + (1 if args.append else 0))
 
     # ---- end to end through the host-buffer entry point ----
     e2e = None
@@ -424,54 +573,69 @@ def bench_spin(args):
                "d2h_bytes_per_step": int(o_host.numel() * 4)}
     st2 = ctx.stats()
     ctx.close()
+    del q_dev, q_host, out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
     cpu_base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tok_s, threads, sample = run_oracle_sample(w, 100000, args.cpu_seconds)
         cpu_base = {"value": tok_s, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample}
 
+    # ---- every workload, and the bench workload's variants, over all their decode steps ----
+    configs = None
+    if world == 1 and not args.no_configs and not (args.append or args.budget or args.tier_split or args.mean_part):
+        configs = {}
+        ocs = 0.0 if args.no_cpu_baseline else args.config_cpu_seconds
+        for name in ("qwen3_14b_32k", "llama31_70b_128k", "stress_m1", "stress_m5", "long_1m", "tiny"):
+            wc = W.by_name(name, seed=rank)
+            configs[name] = run_config(wc, args, local, hbm_gbs, host_gbs, oracle_seconds=ocs, warm_steps=3)
+        wq = W.by_name("qwen3_14b_32k", seed=rank)
+        configs["qwen3_14b_32k+append"] = run_config(wq, args, local, hbm_gbs, host_gbs, append=True, warm_steps=3)
+        configs["qwen3_14b_32k+budget_2x"] = run_config(wq, args, local, hbm_gbs, host_gbs, budget=2 * wq.topk,
+                                                        warm_steps=3)
+        configs["qwen3_14b_32k+tier_split"] = run_config(wq, args, local, hbm_gbs, host_gbs,
+                                                         extra_flags=SPIN_FLAG_TIER_SPLIT, warm_steps=3)
+        if not args.no_cpu_baseline:
+            tok1, th1, sample1 = run_oracle_sample(W.tiny(rank), 100000, 3.0, threads=1)
+            configs["tiny"]["oracle_1_thread"] = {"tokens_per_s": tok1, "cores": th1, "sample": sample1}
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": Wm,
             "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16 in, fp32 accumulate/out", "data": "synthetic (seeded generator; no dataset)",
-            "config": {"workload": workload_desc(w), "l2": "inputs larger than L2 (selected KV per layer "
-                       f"{w.selected_kv_bytes_per_step() // w.L / 2**20:.0f} MiB > 129 MB)",
-                       "parallelism": f"dp{world} (independent requests per GPU)", "timed_decode_steps": K,
-                       "first_timed_step": Wm,
-                       "host_store": ("cudaHostAlloc" if args.host_alloc == "cuda"
-                                      else "huge-page mmap + cudaHostRegister"),
-                       **({"append": "one token per request per layer before each decode step (tail mode)"}
-                          if args.append else {}),
-                       **({"budget_pages_per_unit": args.budget} if args.budget else {}),
-                       **({"metadata": "segment entries in pinned host memory"} if args.tier_split else {})},
-            "roofline": {"bound": "host_link" if host_bound else "hbm", "kernel": "attend_retrieve_kernel",
+            "config": headline_config(w, args, world),
+            "roofline": {"bound": "host_link" if host_bound else "hbm", "kernel": "decode_step_kernel",
                          "achieved": host_achieved if host_bound else hbm_achieved,
                          "peak": host_gbs if host_bound else hbm_gbs, "unit": "GB/s",
                          "frac": (host_achieved / host_gbs) if host_bound else (hbm_achieved / hbm_gbs),
                          "traffic": traffic,
-                         "peak_source": ("pinned H2D cudaMemcpyAsync peak measured in this run (1 GiB)" if host_bound
-                                         else (f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
-                                               else "fallback 6800 GB/s")),
-                         "algorithmic_bytes_per_launch": {"hbm_selected_kv": sel_bytes_per_launch,
-                                                          "host_retrieved": ret_bytes_per_launch},
+                         "peak_source": ("largest host-link rate measured in this run (host_link_peaks_gbs)"
+                                         if host_bound else
+                                         (f"{peak_src} hbm_gbs (MEASURED_PEAKS.json)" if peak_src == "measured"
+                                          else "fallback 6800 GB/s")),
+                         "algorithmic_bytes_per_launch": {"hbm_selected_kv": sel_b, "hbm_summaries": summ_b,
+                                                          "host_retrieved": ret_b},
                          "hbm": {"achieved": hbm_achieved, "peak": hbm_gbs, "frac": hbm_achieved / hbm_gbs},
-                         "host_link": {"achieved": host_achieved, "peak": host_gbs, "frac": host_achieved / host_gbs},
-                         "avg_launch_ms": att_ms},
-            "combined_roofline": {"frac": combined_ideal_s / (ms * 1e-3) if ms else None,
-                                  "frac_with_summaries": (combined_ideal_s + summ_ideal_s) / (ms * 1e-3),
+                         "host_link": {"achieved": host_achieved, "peak": host_gbs,
+                                       "frac": host_achieved / host_gbs},
+                         "avg_launch_ms": kern_ms},
+            "host_link_peaks_gbs": links,
+            "combined_roofline": {**roofline_terms(w, d, ms, hbm_gbs, host_gbs, K),
                                   "hbm_gbs": hbm_gbs, "host_link_gbs": host_gbs,
                                   "selected_bytes": d["selected_bytes"], "retrieved_bytes": d["retrieved_bytes"],
-                                  "definition": "(selected KV bytes / HBM GB/s + retrieved bytes / pinned H2D GB/s) "
-                                                "/ measured time, over the timed steps"},
+                                  "definition": "(selected KV bytes / HBM GB/s + retrieved bytes / host-link GB/s) "
+                                                "/ measured time, over the timed steps; frac_with_summaries also "
+                                                "counts the summary bytes Select reads"},
             "stages_ms_per_layer_call": {k2[3:]: d[k2] / calls for k2 in
-                                         ("ms_select", "ms_manage", "ms_retrieve", "ms_attention", "ms_combine")},
+                                         ("ms_score", "ms_manage", "ms_pages", "ms_combine", "ms_kernel")},
             "paging": {"hits": d["hits"], "misses": d["misses"], "evictions": d["evictions"],
                        "lru_rounds": d["lru_rounds"], "live_segments": st2["live_segments"],
                        "pool_segments": st2["pool_segments"], "metadata_bytes": st2["metadata_bytes"],
                        "flat_table_bytes": st2["flat_table_bytes"]},
             "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clk, "cpu_baseline": cpu_base,
-            "setup_s": setup_s,
+            "setup_s": setup_s, "configs": configs,
         }
         print(json.dumps(line), flush=True)
     R.close()

@@ -90,7 +90,7 @@ typedef enum spin_flags {
 
 /* Configuration of one context. All counts are per context. */
 typedef struct spin_config {
-  int32_t batch;             /* B >= 1 requests */
+  int32_t batch;             /* 1 <= B <= 16384 requests */
   int32_t layers;            /* L >= 1 */
   int32_t q_heads;           /* Hq; Hq % Hkv == 0 and Hq / Hkv <= SPIN_MAX_GROUP */
   int32_t kv_heads;          /* Hkv >= 1 */
@@ -134,11 +134,14 @@ typedef struct spin_stats_t {
   int64_t host_store_bytes;  /* pinned host page store */
   int64_t summary_bytes;     /* HBM partition summaries (fp32) */
   int64_t timed_calls;       /* decode calls with stage timing */
-  double ms_select;          /* summed stage times (SPIN_FLAG_STAGE_TIMING), milliseconds */
-  double ms_manage;
-  double ms_retrieve;
-  double ms_attention;
-  double ms_combine;
+  /* Summed stage times of the timed calls (SPIN_FLAG_STAGE_TIMING), milliseconds. A decode
+     step is one kernel whose phases overlap across SMs; the stages are consecutive spans of
+     its critical path, from in-kernel timer stamps: */
+  double ms_score;           /* first CTA starts -> every partition scored */
+  double ms_manage;          /* -> the last unit's top-k and page manager done (misses published) */
+  double ms_pages;           /* -> the last page retrieved and attended (retrieval overlaps attention) */
+  double ms_combine;         /* -> the last output row combined */
+  double ms_kernel;          /* the whole kernel, from CUDA events around it */
   uint32_t device_error;     /* raw device error word (0 = none) */
   int64_t appended_tokens;   /* tokens appended through spin_append_kv (all layers, all requests) */
   int64_t tail_flushes;      /* tails that filled and became partitions (per layer and request) */
@@ -273,24 +276,38 @@ int spin_debug_summaries(spin_ctx* ctx, int32_t layer, int32_t b, int32_t h, flo
  * needs the buffers spin_create allocates. No counterpart on the SPIN pages: this
  * is the decode step's Select (fp32 score = (sum of the group's queries) . summary,
  * per-unit top-k, equal scores to the lower index, ascending output) without the
- * context. It calls no allocator of any kind.
+ * context, computed by the same device code as the decode step. It calls no
+ * allocator of any kind.
  *   summ  device fp32 [units][parts][128] partition summaries (16-byte aligned)
- *   q     device bf16 [units][group][128] queries of each unit's query heads
+ *   q     device bf16 [units][group][128] queries of each unit's query heads (8-byte aligned)
  *   sel   device int32 [units][topk] output: selected partitions, ascending, -1 padded
  *         when parts < topk
  * Limits: units * parts <= SPIN_NOALLOC_MAX_SCORES, parts <= 32768, group <= 16,
  * topk <= 512; larger sizes return SPIN_ERR_INVALID. The scores live in one static
- * device array of SPIN_NOALLOC_MAX_SCORES floats (4 MiB) that every GPU loading the
- * library holds until exit. All calls share it and it keeps the last call's
- * contents; calls whose work overlaps on the GPU (different streams, different
- * host threads on one device) race on it and must be serialised by the caller.
- * The first call on a device looks up that array's device address and sets a
- * kernel attribute (once per device, on the current device); make that first call
- * before any stream capture. Asynchronous on `stream`; on failure
+ * device array of SPIN_NOALLOC_MAX_SCORES floats (4 MiB). CUDA reserves it when the
+ * library's kernels are loaded into a context: with lazy module loading (the CUDA
+ * default) that happens on the first call in each context, so a caller whose pool
+ * will claim the device, or that will capture a graph, makes one call first (or sets
+ * CUDA_MODULE_LOADING=EAGER). The context holds the array until it is destroyed. All
+ * calls share it and it keeps the last call's contents; calls whose work overlaps on
+ * the GPU (different streams, different host threads on one device) race on it and
+ * must be serialised by the caller. Each call looks the array's device address up in
+ * the current context. A CUDA error left pending by earlier work is reported as
+ * SPIN_ERR_CUDA without launching anything. Asynchronous on `stream`; on failure
  * spin_last_error(NULL) gives the reason. */
 #define SPIN_NOALLOC_MAX_SCORES (1 << 20)
 int spin_select_noalloc(const float* summ, const uint16_t* q, int32_t units, int32_t parts, int32_t group,
                         int32_t topk, int32_t* sel, spin_stream_t stream);
+
+/* Host-link probe ([XT] "理想与现实的差距", Figure 1: the pages measure against an
+ * envelope with retrieval at the link's peak). Streams `bytes` of the pinned,
+ * device-mapped host buffer `host` (16-byte aligned) through the SMs with 16-byte
+ * zero-copy loads, ctas_per_sm (1..4) CTAs of 512 threads per SM, twice on `stream`
+ * (the first pass resolves the pages' address translations), and writes the second
+ * pass's rate in GB/s (1e9 bytes/s) to *gbs. Synchronises `stream`. Uses the current
+ * device; allocates nothing. SPIN_ERR_INVALID for a buffer that is not pinned host
+ * memory mapped for the device. */
+int spin_measure_host_read(const void* host, int64_t bytes, int32_t ctas_per_sm, double* gbs, spin_stream_t stream);
 
 /* Releases everything the context owns (synchronises first). NULL is a no-op. */
 void spin_destroy(spin_ctx* ctx);

@@ -336,6 +336,33 @@ def step_units_parallel(units, qs, k: int, t: int, threads: int = 0, lib=None):
     return used, keep
 
 
+def step_units_full(units, qs, k: int, t: int, threads: int = 0, lib=None):
+    """One decode step on many units with the oracle's thread pool, keeping every output:
+    a list of dicts (scores, sel, sel_slot, sel_hit, out, mo) in the order of `units`."""
+    lib = lib or load()
+    n = len(units)
+    handles = (ctypes.c_void_p * n)(*[u.h for u in units])
+    ios = (StepIO * n)()
+    keep = []
+    for i, (u, q) in enumerate(zip(units, qs)):
+        q = np.ascontiguousarray(q, np.uint16)
+        sc = np.empty(max(u.P, 1), np.float64)
+        sel = np.empty(max(k, 1), np.int32)
+        ss = np.empty(max(k, 1), np.int32)
+        sh = np.empty(max(k, 1), np.uint8)
+        out = np.empty((q.shape[0], D), np.float64)
+        keep.append((q, sc, sel, ss, sh, out))
+        ios[i] = StepIO(u.summ.ctypes.data, u.host_pages.ctypes.data, q.ctypes.data, q.shape[0], k, t, sc.ctypes.data,
+                        sel.ctypes.data, ss.ctypes.data, sh.ctypes.data, None, out.ctypes.data)
+    lib.oracle_step_units(handles, ios, n, threads)
+    res = []
+    for i, (u, (q, sc, sel, ss, sh, out)) in enumerate(zip(units, keep)):
+        keff = ios[i].keff
+        res.append(dict(scores=sc[:u.P], sel=sel[:keff].copy(), sel_slot=ss[:keff].copy(),
+                        sel_hit=sh[:keff].astype(bool), out=out, mo=ios[i].mo))
+    return res
+
+
 class TailUnit:
     """Oracle unit with KV append: complete 64-token partitions are selectable; the tail
     (fewer than 64 newest tokens) is attended at every step and becomes a partition

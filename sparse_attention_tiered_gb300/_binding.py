@@ -38,7 +38,7 @@ SPIN_NOALLOC_MAX_SCORES_DEFAULT = 1 << 20  # SPIN_NOALLOC_MAX_SCORES in include/
 # Every symbol include/spin.h declares.
 EXPORTS = ("spin_create", "spin_index_offload", "spin_index_offload_parts", "spin_append_kv", "spin_set_buffer", "spin_decode_step", "spin_decode_step_host", "spin_stats",
            "spin_debug_export", "spin_debug_read_page", "spin_debug_summaries", "spin_destroy", "spin_last_error",
-           "spin_select_noalloc")
+           "spin_select_noalloc", "spin_measure_host_read")
 
 
 class SpinError(RuntimeError):
@@ -72,7 +72,7 @@ class spin_stats_t(ctypes.Structure):
         "steps", "hits", "misses", "evictions", "lru_rounds", "retrieved_bytes", "selected_bytes",
         "live_segments", "pool_segments", "metadata_bytes", "flat_table_bytes", "hbm_pool_bytes",
         "host_store_bytes", "summary_bytes", "timed_calls")] + [
-        (n, ctypes.c_double) for n in ("ms_select", "ms_manage", "ms_retrieve", "ms_attention", "ms_combine")] + [
+        (n, ctypes.c_double) for n in ("ms_score", "ms_manage", "ms_pages", "ms_combine", "ms_kernel")] + [
         ("device_error", ctypes.c_uint32), ("appended_tokens", ctypes.c_int64), ("tail_flushes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -136,6 +136,8 @@ def load(build_if_missing: bool = True):
             L.spin_destroy.restype = None
             L.spin_select_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp]
             L.spin_select_noalloc.restype = ctypes.c_int
+            L.spin_measure_host_read.argtypes = [vp, i64, i32, ctypes.POINTER(ctypes.c_double), vp]
+            L.spin_measure_host_read.restype = ctypes.c_int
             L.spin_last_error.argtypes = [vp]
             L.spin_last_error.restype = ctypes.c_char_p
             _lib = L
@@ -213,6 +215,13 @@ def spin_select_noalloc(summ_ptr: int, q_ptr: int, units: int, parts: int, group
 
 def spin_destroy(ctx: int):
     load().spin_destroy(ctx)
+
+
+def spin_measure_host_read(host_ptr: int, nbytes: int, ctas_per_sm: int = 1, stream: int = 0) -> float:
+    """GB/s of SM zero-copy reads of a pinned host buffer (see include/spin.h)."""
+    g = ctypes.c_double(0.0)
+    _check(load().spin_measure_host_read(host_ptr, nbytes, ctas_per_sm, ctypes.byref(g), stream))
+    return g.value
 
 
 def spin_last_error(ctx=None) -> str:

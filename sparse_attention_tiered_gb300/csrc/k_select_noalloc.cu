@@ -7,15 +7,14 @@
 // entry point of this library needs a context whose buffers spin_create
 // allocates. This one takes only caller-owned inputs and outputs; the fp32 score
 // array it needs between its two kernels lives in a fixed static device array
-// (kNoAllocMaxScores floats = 4 MiB), which every GPU that loads the library
-// holds until the process exits.
+// (kNoAllocMaxScores floats = 4 MiB), which every CUDA context that loads this
+// module holds until it is destroyed.
 //
-// The arithmetic matches the decode step's Select exactly (same summation
-// order, same radix top-k and tie rule), so its result equals the selection a
-// decode step makes for the same summaries and queries.
-#include <mutex>
-
+// The scores and the top-k are the decode step's own device code (select_dev.cuh:
+// same summation order, same radix select and tie rule), so the result equals the
+// selection a decode step makes for the same summaries and queries.
 #include "../../include/spin.h"
+#include "select_dev.cuh"
 #include "spin_internal.cuh"
 
 namespace spin {
@@ -26,224 +25,77 @@ namespace {
 
 constexpr int64_t kNoAllocMaxScores = SPIN_NOALLOC_MAX_SCORES;
 constexpr int kNoAllocMaxParts = 32768;
-constexpr int kMaxDevices = 64;
 
 // The scratch: one score per (unit, partition) of the current call. Every call
 // overwrites the entries it reads before reading them, so nothing has to be
 // cleared between calls; calls that overlap on the GPU share it and race.
 static __device__ __align__(256) float g_noalloc_scores[SPIN_NOALLOC_MAX_SCORES];
 
-__device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+constexpr int kScoreWarps = 8;
+constexpr int kScoreRows = kScoreWarps * sel::kRowsPerBatch;  // partitions per CTA
 
-__device__ __forceinline__ uint32_t float_key(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
-constexpr int kScoreThreads = 256;
-constexpr int kScorePerWarp = 8;
-constexpr int kScoreChunk = (kScoreThreads / 32) * kScorePerWarp;
-
-// grid (units, ceil(P / 64)); summ [units][P][128] fp32, q [units][G][128] bf16.
-__global__ void __launch_bounds__(kScoreThreads)
+// grid (units, ceil(P / kScoreRows)); summ [units][P][128] fp32, q [units][G][128] bf16.
+__global__ void __launch_bounds__(kScoreWarps * 32)
 noalloc_score_kernel(const float* __restrict__ summ, const uint16_t* __restrict__ q, int P, int G,
                      float* __restrict__ scores) {
   const int u = blockIdx.x;
-  const int p_base = blockIdx.y * kScoreChunk;
-  __shared__ __align__(16) float qs[kD];
-  if (threadIdx.x < kD) {
-    const uint16_t* qq = q + (int64_t)u * G * kD + threadIdx.x;
-    float s = 0.f;
-    for (int g = 0; g < G; ++g) s += bf16f(qq[g * kD]);
-    qs[threadIdx.x] = s;
-  }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float4 qv = reinterpret_cast<const float4*>(qs)[lane];
-  const float4* su = reinterpret_cast<const float4*>(summ + (int64_t)u * P * kD);
-  const int p0 = p_base + warp * kScorePerWarp;
-  float4 sv[kScorePerWarp];
-#pragma unroll
-  for (int i = 0; i < kScorePerWarp; ++i) {
-    const int p = p0 + i;
-    sv[i] = p < P ? __ldg(su + (int64_t)p * (kD / 4) + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  float d[kScorePerWarp];
-#pragma unroll
-  for (int i = 0; i < kScorePerWarp; ++i) {
-    float x = sv[i].x * qv.x;
-    x = fmaf(sv[i].y, qv.y, x);
-    x = fmaf(sv[i].z, qv.z, x);
-    x = fmaf(sv[i].w, qv.w, x);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    d[i] = x;
-  }
-  if (lane < kScorePerWarp) {
-    float x = d[0];
-#pragma unroll
-    for (int i = 1; i < kScorePerWarp; ++i) x = (lane == i) ? d[i] : x;
-    const int p = p0 + lane;
-    if (p < P) scores[(int64_t)u * P + p] = (x == 0.f) ? 0.f : x;
-  }
+  const int p0 = blockIdx.y * kScoreRows + warp * sel::kRowsPerBatch;
+  if (p0 >= P) return;
+  const int n = min(sel::kRowsPerBatch, P - p0);
+  float4 sv[sel::kRowsPerBatch];
+  sel::load_rows(sv, reinterpret_cast<const float4*>(summ + ((int64_t)u * P + p0) * kD), n, lane);
+  const float4 qv = sel::qsum_lane(q + (int64_t)u * G * kD, G, lane);
+  const float x = sel::score_batch(sv, qv, lane);
+  if (lane < n) scores[(int64_t)u * P + p0 + lane] = x;
 }
 
 constexpr int kTopkThreads = 512;
-constexpr int kTopkWarps = kTopkThreads / 32;
 
-// One CTA per unit: radix select of the k-th largest key, then compaction in
-// ascending partition order with equal keys taken from the lowest index up.
+// Shared memory of the top-k kernel for P partitions: group scalars, keys [P], histograms,
+// candidates (units wider than the wide-unit threshold).
+__host__ __device__ inline size_t topk_smem_layout(int P, uint8_t* base, sel::GroupScalars** gs, uint32_t** keys,
+                                                   uint32_t** whist, uint32_t** cand) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = base ? base + off : nullptr;
+    off += sel::align16(bytes);
+    return p;
+  };
+  uint8_t* g = take(sizeof(sel::GroupScalars));
+  uint8_t* k = take(sizeof(uint32_t) * (size_t)P);
+  uint8_t* w = take(sizeof(uint32_t) * (kTopkThreads / 32) * 256);
+  const int cc = sel::cand_capacity(kTopkThreads, P);
+  uint8_t* c = take(sizeof(uint32_t) * (size_t)(cc > 0 ? cc : 1));
+  if (base) {
+    *gs = (sel::GroupScalars*)g;
+    *keys = (uint32_t*)k;
+    *whist = (uint32_t*)w;
+    *cand = (uint32_t*)c;
+  }
+  return off;
+}
+
+// One CTA per unit: the decode step's group top-k over the unit's keys; sel [units][k].
 __global__ void __launch_bounds__(kTopkThreads)
-noalloc_topk_kernel(const float* __restrict__ scores, int P, int k, int32_t* __restrict__ sel) {
+noalloc_topk_kernel(const float* __restrict__ scores, int P, int k, int32_t* __restrict__ sel_out) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  uint32_t* whist = reinterpret_cast<uint32_t*>(smem_raw);   // [kTopkWarps][256]
-  uint32_t* keys = whist + kTopkWarps * 256;                   // [P]
-  __shared__ int s_bin, s_above;
-  __shared__ int s_wgt[kTopkWarps], s_weq[kTopkWarps], s_wpos[kTopkWarps], s_wtake[kTopkWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  sel::GroupScalars* gs;
+  uint32_t *keys, *whist, *cand;
+  topk_smem_layout(P, smem_raw, &gs, &keys, &whist, &cand);
+  const int tid = threadIdx.x;
   const int u = blockIdx.x;
   const int keff = P < k ? P : k;
-  for (int p = tid; p < P; p += kTopkThreads) keys[p] = float_key(scores[(int64_t)u * P + p]);
-  uint32_t prefix = 0, mask = 0;
-  int krem = keff;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) whist[i] = 0;
-    __syncthreads();
-    for (int p = tid; p < P; p += kTopkThreads) {
-      const uint32_t key = keys[p];
-      if ((key & mask) == prefix) atomicAdd(&whist[warp * 256 + ((key >> shift) & 255u)], 1u);
-    }
-    __syncthreads();
-    if (tid < 256) {
-      uint32_t s = 0;
-      for (int w = 0; w < kTopkWarps; ++w) s += whist[w * 256 + tid];
-      whist[tid] = s;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      int c[8], lsum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = (int)whist[255 - 8 * lane - i];
-        lsum += c[i];
-      }
-      int incl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const int excl = incl - lsum;
-      const uint32_t hitm = __ballot_sync(0xffffffffu, excl < krem && incl >= krem);
-      if (lane == __ffs(hitm) - 1) {
-        int above = excl;
-        for (int i = 0; i < 8; ++i) {
-          if (above + c[i] >= krem) {
-            s_bin = 255 - 8 * lane - i;
-            s_above = above;
-            break;
-          }
-          above += c[i];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= (uint32_t)s_bin << shift;
-    mask |= 0xFFu << shift;
-    krem -= s_above;
-    __syncthreads();
-  }
-  const uint32_t T = prefix;
-  const int chunk = ((P + kTopkThreads - 1) / kTopkThreads) * 32;
-  const int wb = warp * chunk, we = min(P, wb + chunk);
-  int gt = 0, eq = 0;
-  for (int base = wb; base < we; base += 32) {
-    const int p = base + lane;
-    const uint32_t key = p < we ? keys[p] : 0u;
-    gt += __popc(__ballot_sync(0xffffffffu, p < we && key > T));
-    eq += __popc(__ballot_sync(0xffffffffu, p < we && key == T));
-  }
-  if (lane == 0) {
-    s_wgt[warp] = gt;
-    s_weq[warp] = eq;
-  }
+  for (int p = tid; p < P; p += kTopkThreads) keys[p] = sel::float_key(scores[(int64_t)u * P + p]);
   __syncthreads();
-  if (tid == 0) {
-    int eq_before = 0, pos = 0;
-    for (int w = 0; w < kTopkWarps; ++w) {
-      const int take = max(0, min(krem - eq_before, s_weq[w]));
-      s_wpos[w] = pos;
-      s_wtake[w] = take;
-      pos += s_wgt[w] + take;
-      eq_before += s_weq[w];
-    }
-  }
-  __syncthreads();
-  int32_t* out = sel + (int64_t)u * k;
-  int pos = s_wpos[warp], eq_left = s_wtake[warp];
-  for (int base = wb; base < we; base += 32) {
-    const int p = base + lane;
-    const uint32_t key = p < we ? keys[p] : 0u;
-    const bool isgt = p < we && key > T;
-    const bool iseq = p < we && key == T;
-    const uint32_t meq = __ballot_sync(0xffffffffu, iseq);
-    const bool take = isgt || (iseq && __popc(meq & lanemask_lt()) < eq_left);
-    const uint32_t msel = __ballot_sync(0xffffffffu, take);
-    if (take) out[pos + __popc(msel & lanemask_lt())] = p;
-    pos += __popc(msel);
-    eq_left -= min(eq_left, __popc(meq));
-  }
-  for (int j = keff + tid; j < k; j += kTopkThreads) out[j] = -1;
+  int32_t* out = sel_out + (int64_t)u * k;
+  __shared__ int32_t s_sel[kMaxTopk];
+  const bool ok = sel::group_topk<kTopkThreads>(keys, P, keff, whist, cand, sel::cand_capacity(kTopkThreads, P), gs,
+                                                1, tid, s_sel);
+  for (int j = tid; j < k; j += kTopkThreads) out[j] = (ok && j < keff) ? s_sel[j] : -1;
 }
 
-struct DeviceScratch {
-  bool ready = false;
-  float* scores = nullptr;  // device address of g_noalloc_scores on that device
-};
-DeviceScratch g_scratch[kMaxDevices];
-std::mutex g_scratch_mu;
-
-// Once per device, with that device current: the device address of the static
-// scratch (the host-side symbol is only a stand-in) and the top-k kernel's
-// shared-memory limit.
-int scratch_for_current_device(float** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    cudaGetLastError();
-    set_global_error("spin_select_noalloc: no usable current CUDA device");
-    return SPIN_ERR_CUDA;
-  }
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  DeviceScratch& s = g_scratch[dev];
-  if (!s.ready) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scores);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      set_global_error("spin_select_noalloc: cudaGetSymbolAddress of the static score scratch failed");
-      return SPIN_ERR_CUDA;
-    }
-    const int smem = (int)(sizeof(uint32_t) * (kTopkWarps * 256 + kNoAllocMaxParts));
-    e = cudaFuncSetAttribute(noalloc_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      set_global_error("spin_select_noalloc: configuring the top-k kernel failed");
-      return SPIN_ERR_CUDA;
-    }
-    s.scores = static_cast<float*>(p);
-    s.ready = true;
-  }
-  *out = s.scores;
-  return SPIN_OK;
-}
+size_t topk_smem_bytes(int P) { return topk_smem_layout(P, nullptr, nullptr, nullptr, nullptr, nullptr); }
 
 }  // namespace
 }  // namespace spin
@@ -264,22 +116,49 @@ extern "C" int spin_select_noalloc(const float* summ, const uint16_t* q, int32_t
                      "scores (or parts > 32768)");
     return SPIN_ERR_INVALID;
   }
-  if ((reinterpret_cast<uintptr_t>(summ) & 15) || (reinterpret_cast<uintptr_t>(q) & 1) ||
+  if ((reinterpret_cast<uintptr_t>(summ) & 15) || (reinterpret_cast<uintptr_t>(q) & 7) ||
       (reinterpret_cast<uintptr_t>(sel) & 3)) {
-    set_global_error("spin_select_noalloc: summ must be 16-byte, q 2-byte and sel 4-byte aligned");
+    set_global_error("spin_select_noalloc: summ must be 16-byte, q 8-byte and sel 4-byte aligned");
     return SPIN_ERR_INVALID;
   }
-  float* scores = nullptr;
-  int rc = scratch_for_current_device(&scores);
-  if (rc != SPIN_OK) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  dim3 g1((unsigned)units, (unsigned)((parts + kScoreChunk - 1) / kScoreChunk));
-  noalloc_score_kernel<<<g1, kScoreThreads, 0, st>>>(summ, q, parts, group, scores);
-  const size_t smem = sizeof(uint32_t) * (kTopkWarps * 256 + (size_t)parts);
-  noalloc_topk_kernel<<<(unsigned)units, kTopkThreads, smem, st>>>(scores, parts, topk, sel);
+  // An error left by earlier, unrelated work would be reported as this call's launch
+  // failure; report it as what it is and launch nothing.
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
-    set_global_error("spin_select_noalloc: kernel launch failed");
+    set_global_error("spin_select_noalloc: a CUDA error from earlier work was pending; nothing was launched");
+    return SPIN_ERR_CUDA;
+  }
+  // The device address of the static scratch in the current context (the host-side
+  // symbol is only a stand-in for it). Looked up on every call, so the address always
+  // belongs to the context the kernels run in; the first lookup in a context loads this
+  // module, which reserves the array.
+  void* scratch = nullptr;
+  e = cudaGetSymbolAddress(&scratch, g_noalloc_scores);
+  if (e != cudaSuccess || !scratch) {
+    cudaGetLastError();
+    set_global_error("spin_select_noalloc: cudaGetSymbolAddress of the static score scratch failed");
+    return SPIN_ERR_CUDA;
+  }
+  const size_t smem = topk_smem_bytes(parts);
+  e = cudaFuncSetAttribute(noalloc_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    set_global_error("spin_select_noalloc: configuring the top-k kernel failed");
+    return SPIN_ERR_CUDA;
+  }
+  float* scores = static_cast<float*>(scratch);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  dim3 g1((unsigned)units, (unsigned)((parts + kScoreRows - 1) / kScoreRows));
+  noalloc_score_kernel<<<g1, kScoreWarps * 32, 0, st>>>(summ, q, parts, group, scores);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_global_error("spin_select_noalloc: launching the score kernel failed; the top-k kernel was not launched");
+    return SPIN_ERR_CUDA;
+  }
+  noalloc_topk_kernel<<<(unsigned)units, kTopkThreads, smem, st>>>(scores, parts, topk, sel);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_global_error("spin_select_noalloc: launching the top-k kernel failed");
     return SPIN_ERR_CUDA;
   }
   return SPIN_OK;

@@ -1,26 +1,38 @@
+// One decode step of one layer in one persistent kernel: Select (scores, per-KV-head
+// top-k), the page manager (two-level resolve, bump, bucketed LRU, slot assignment),
 // Retrieve (host -> HBM page copies), paged split-KV decode attention and combine.
 //
-// Retrieve brings the critical partitions that are not resident from CPU memory
-// into their HBM pages; Attention is exact softmax attention over the tokens of
-// the selected partitions only (m.x-techcon.com SPIN article, section
-// "Spin的核心设计" 1 and Figure 3, 2 and Figure 5 step 4; gist.science/pt section
-// 2A). The pages give no kernel design; everything below is this library's.
+// Select picks the critical partitions for the query, Retrieve brings the missing
+// ones from CPU memory into HBM pages and Attention is exact softmax attention over
+// the tokens of the selected partitions only (m.x-techcon.com SPIN article, section
+// "Spin的核心设计" 1 and Figure 3, 2 and Figure 5 steps 1-4, 3 and Figure 6;
+// gist.science/pt section 2A-2C). The pages give no kernel design; everything below
+// is this library's.
 //
-// One cooperative persistent kernel per layer step does both, one CTA per SM:
-//   * retriever warps walk the step's miss list (host page -> HBM slot, 16-byte
-//     zero-copy loads over the host link), and publish each copied page with a
-//     release store of the step tag into its ready flag; two start at once, the
-//     others join when the CTA's resident pages have all been issued;
-//   * two consumer groups of four warps take alternate stages of a 6-stage
-//     shared-memory ring guarded by mbarriers, so two pages are in the math at once;
-//   * each group has a producer warp that stages its pages through TMA: first
-//     resident pages (hits) in tasks of up to `ppt` pages of one unit, then
-//     retrieved pages in miss-list order, each after an acquire of its ready flag.
-//     Nothing on the issue path waits for a fresh global load: tasks are claimed
-//     two ahead, the next task's page descriptors sit in the lanes' registers, and a
-//     retrieved page's miss-list entry is loaded before its flag is awaited.
-// So the attention over the hits (HBM bound) hides under the retrieval (host-link
-// bound) and each retrieved page is attended as soon as it lands (and from L2).
+// The kernel is cooperative (every CTA is resident, one per SM) and runs three
+// phases per CTA:
+//   A. scoring: every warp of the grid takes items of 16 partitions in unit-major
+//      order, writes their fp32 scores and adds the rows to the unit's counter;
+//   B. managing: groups of GS threads claim units in order; a group waits until its
+//      unit's rows are all scored, runs top-k and the page manager on it (shared
+//      memory overlaying the ring of phase C), appends the unit's misses to the
+//      step's miss list (each entry published with the step tag) and publishes the
+//      unit (its ready flag);
+//   C. retrieval and attention, per CTA once its groups are done:
+//      * retriever warps walk the miss list as entries appear (host page -> HBM
+//        slot, 16-byte zero-copy loads over the host link) and publish each copied
+//        page with a release store of the step tag into its ready flag; two start
+//        at once, the others join when the CTA's resident pages have all been issued;
+//      * two consumer groups of four warps take alternate stages of a 6-stage
+//        shared-memory ring guarded by mbarriers, so two pages are in the math at once;
+//      * each consumer group has a producer warp that stages its pages through TMA:
+//        first resident pages (hits) in tasks of up to `ppt` pages of one unit (after
+//        the unit's ready flag), then retrieved pages in miss-list order, each after
+//        an acquire of its ready flag.
+// So retrieval starts as soon as the first units are managed, the attention over the
+// hits (HBM bound) hides under the retrieval (host-link bound) and each retrieved page
+// is attended as soon as it lands (and from L2). When every CTA is done with its
+// pages (an arrival counter), every consumer warp combines (unit, query head) pairs.
 //
 // Attention data layout. A page (32 KiB) holds K[64][128] then V[64][128] bf16.
 // A TMA tensor map views the whole HBM pool as a 2-D bf16 tensor of 128 columns
@@ -35,15 +47,14 @@
 //   O^T[128][8 heads] += V^T P             P transposed in registers (movmatrix) and
 //                                          split into bf16 hi + lo parts, two mma each
 // At the end of a task the group's four warps merge (m, l, O) in the stage of the
-// task's last page and write one partial (m, l, acc[128]) per query head. When
-// every CTA has finished its pages (an arrival counter; all CTAs are co-resident
-// under the cooperative launch), every consumer warp of the grid combines
-// (unit, query head) pairs of partials into the output:
-//   out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
+// task's last page and write one partial (m, l, acc[128]) per query head; the
+// combine computes out_g = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c.
 //
-// Every wait (mbarrier, ready flag, arrival counter) is bounded in time; a wait
-// that runs out sets the device error word, stops issuing work and drains the
-// copies already issued.
+// Every wait (scored rows, unit and miss-list flags, mbarriers, page flags, the
+// arrival counter) is bounded in time; a wait that runs out sets the device error
+// word, after which every other wait gives up at once, stops issuing work and drains
+// the copies already issued.
+#include "select_dev.cuh"
 #include "spin_internal.cuh"
 
 namespace spin {
@@ -56,7 +67,7 @@ constexpr int kMaxGroups = 2;
 // Roles per CTA. One 8-head tile (NT = 1, at most 128 registers a thread): two
 // consumer groups that take alternate ring stages, so two pages are in the math at
 // once, each fed by its own producer warp, and six retriever warps (two saturate the
-// host link alone). Two tiles (168 registers): one group, one producer, four
+// host link alone). Two tiles (G > 8, 168 registers): one group, one producer, four
 // retrievers. Threads x registers stay within 64 K.
 template <int NT>
 struct Roles {
@@ -67,6 +78,7 @@ struct Roles {
 };
 constexpr int kQBytes = kMaxGroup * kD * 2;            // query rows of one unit (<= 16 heads)
 constexpr int kStageBytes = kPageBytes + kQBytes;       // 36 KiB, a multiple of 1024
+constexpr int kRingBytes = kStages * kStageBytes;
 constexpr int kMergeRow = kD + 4;                       // padded row of the merge buffer
 constexpr int kMergeFloats = 16 * kMergeRow + 32;       // O[16 heads][128+4], m[16], l[16]
 static_assert(kCWarps * kMergeFloats * 4 <= kStageBytes, "a task's merge must fit in its last page's stage");
@@ -77,8 +89,9 @@ struct StageMeta {
   int part, ul, valid, first, last;  // partial slot of the task, unit, valid tokens, first / last page of the task
 };
 
-struct AttnSmem {
-  uint8_t* ring;      // kStages x kStageBytes, 1024-aligned (a task's last stage also holds its merge)
+// Dynamic shared memory: a header (barriers, stage descriptors, flags) then, 1024-byte
+// aligned, the region that holds the manager groups in phase B and the ring in phase C.
+struct StepSmem {
   uint64_t* full;     // [kStages]
   uint64_t* empty;    // [kStages]
   uint64_t* mrg;      // [groups][2]: written, read
@@ -86,36 +99,30 @@ struct AttnSmem {
   int* abort_flag;
   int* hits_done;     // set once every producer of this CTA has issued its resident-page tasks
   int* hits_groups;   // producers past their resident pages
+  uint8_t* region;    // ring (kStages x kStageBytes) / manager groups
 };
 
-__host__ __device__ inline size_t attn_smem_layout(AttnSmem* s, uint8_t* base) {
+constexpr size_t kHeaderBytes = 1024;
+
+__host__ __device__ inline void step_smem_layout(StepSmem* s, uint8_t* base) {
   size_t off = 0;
   auto take = [&](size_t bytes, size_t align) {
     off = (off + align - 1) & ~(align - 1);
-    uint8_t* p = base ? base + off : nullptr;
+    uint8_t* p = base + off;
     off += bytes;
     return p;
   };
-  uint8_t* ring = take((size_t)kStages * kStageBytes, 1024);
-  uint8_t* full = take(sizeof(uint64_t) * kStages, 8);
-  uint8_t* empty = take(sizeof(uint64_t) * kStages, 8);
-  uint8_t* mrg = take(sizeof(uint64_t) * 2 * kMaxGroups, 8);
-  uint8_t* meta = take(sizeof(StageMeta) * kStages, 16);
-  uint8_t* ab = take(sizeof(int), 4);
-  uint8_t* hd = take(sizeof(int), 4);
-  uint8_t* hg = take(sizeof(int), 4);
-  if (s) {
-    s->ring = ring;
-    s->full = (uint64_t*)full;
-    s->empty = (uint64_t*)empty;
-    s->mrg = (uint64_t*)mrg;
-    s->meta = (StageMeta*)meta;
-    s->abort_flag = (int*)ab;
-    s->hits_done = (int*)hd;
-    s->hits_groups = (int*)hg;
-  }
-  return off;
+  s->full = (uint64_t*)take(sizeof(uint64_t) * kStages, 8);
+  s->empty = (uint64_t*)take(sizeof(uint64_t) * kStages, 8);
+  s->mrg = (uint64_t*)take(sizeof(uint64_t) * 2 * kMaxGroups, 8);
+  s->meta = (StageMeta*)take(sizeof(StageMeta) * kStages, 16);
+  s->abort_flag = (int*)take(sizeof(int), 4);
+  s->hits_done = (int*)take(sizeof(int), 4);
+  s->hits_groups = (int*)take(sizeof(int), 4);
+  s->region = base + kHeaderBytes;
 }
+static_assert(sizeof(uint64_t) * (2 * kStages + 2 * kMaxGroups) + 16 * (kStages + 1) + 16 <= kHeaderBytes,
+              "header overflow");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -186,12 +193,29 @@ __device__ __forceinline__ int ld_relaxed(const int* p) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
-// Wait until *p reaches `want` (== when exact, else >=), bounded by kWaitNs. Polls with
-// relaxed loads and a short sleep, then one acquire fence: acquire loads and fences in a
-// tight loop hold up the SM's other memory traffic (the retrievers' host loads).
-__device__ __noinline__ bool wait_flag(const int* p, int want, bool exact) {
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *p reaches `want` (== when exact, else >=), bounded by kWaitNs, or (err != nullptr)
+// until another wait has run out (the timeout bit of the error word). Polls with relaxed loads and a short
+// sleep, then one acquire fence: acquire loads and fences in a tight loop hold up the SM's
+// other memory traffic (the retrievers' host loads).
+__device__ __noinline__ bool wait_flag(const int* p, int want, bool exact, const uint32_t* err) {
   auto hit = [&](int v) { return exact ? v == want : v >= want; };
   bool ok = hit(ld_relaxed(p));
   if (!ok) {
@@ -199,11 +223,32 @@ __device__ __noinline__ bool wait_flag(const int* p, int want, bool exact) {
     for (uint32_t it = 1; it < (1u << 30) && !ok; ++it) {
       __nanosleep(128);
       ok = hit(ld_relaxed(p));
-      if (!ok && (it & 63u) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
+      if (!ok && (it & 63u) == 0 &&
+          (globaltimer_ns() - t0 > kWaitNs || (err != nullptr && (ld_relaxed_u32(err) & kErrTimeout))))
+        break;
     }
   }
   if (ok) fence_acq_rel();
   return ok;
+}
+
+// State of miss-list entry m of this step: 1 = written (its fields may be read after an
+// acquire), 0 = past the end of the step's final list, -1 = the bounded wait ran out.
+// The list is final once every unit of the layer is managed.
+__device__ __noinline__ int miss_entry(const LayerArgs& a, int m, int tag, int U, int kmax) {
+  if (m >= kmax) return 0;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (ld_relaxed(a.miss_tag + m) == tag) return 1;
+    if (ld_relaxed(a.counters + kCtrManaged) >= U) {
+      fence_acq_rel();
+      if (m >= ld_relaxed(a.counters + kCtrMiss)) return 0;
+      continue;  // every entry below the final count is published before its unit: the tag is there
+    }
+    if ((it & 63u) == 63u && (globaltimer_ns() - t0 > kWaitNs || (ld_relaxed_u32(a.err) & kErrTimeout))) return -1;
+    __nanosleep(64);
+  }
+  return -1;
 }
 
 __device__ __forceinline__ void st_release(int* p, int v) {
@@ -260,7 +305,7 @@ __device__ __forceinline__ uint32_t swz(int r, int cd) {
 __device__ void combine_head(const LayerArgs& a, int ul, int g, int lane) {
   const int b = ul / a.Hkv, h = ul - b * a.Hkv;
   const int has_tail = (a.tail_n != nullptr && a.tail_n[b] > 0) ? 1 : 0;
-  const int keff = a.keff[ul] + has_tail, nh = a.n_hit[ul];  // attended pages; resident ones (tail included)
+  const int keff = __ldcg(a.keff + ul) + has_tail, nh = __ldcg(a.n_hit + ul);  // attended; resident (tail incl.)
   const int nc = (nh + a.ppt - 1) / a.ppt;
   const int U = a.B * a.Hkv;
   const int n = nc + (keff - nh);
@@ -312,22 +357,120 @@ __device__ void combine_head(const LayerArgs& a, int ul, int g, int lane) {
   out[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
+
+// Combine of one (unit, query head) by the nw consumer warps of a CTA (named barrier
+// `bar`), for units with many partials: warp w folds partials w, w + nw, ... (their loads
+// all in flight at once) into (M_w, L_w, acc_w), the warps' results meet in shared memory
+// `red` and are folded again: out = sum_w 2^(M_w - M) acc_w / sum_w 2^(M_w - M) L_w.
+__device__ void combine_head_cta(const LayerArgs& a, int ul, int g, int w, int nw, int lane, float* red, int bar) {
+  const int b = ul / a.Hkv, h = ul - b * a.Hkv;
+  const int has_tail = (a.tail_n != nullptr && a.tail_n[b] > 0) ? 1 : 0;
+  const int keff = __ldcg(a.keff + ul) + has_tail, nh = __ldcg(a.n_hit + ul);
+  const int nc = (nh + a.ppt - 1) / a.ppt;
+  const int U = a.B * a.Hkv;
+  const int n = nc + (keff - nh);
+  auto part_ptr = [&](int i) -> const float* {
+    const int64_t slot =
+        i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.ka + nh + (i - nc);
+    return a.partials + (slot * a.G + g) * kPartialStride;
+  };
+  constexpr int kMaxPer = 8;
+  float Mw = -INFINITY, Lw = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = w; i0 < n; i0 += kMaxPer * nw) {
+    float m[kMaxPer], l[kMaxPer];
+    float4 v[kMaxPer];
+#pragma unroll
+    for (int u = 0; u < kMaxPer; ++u) {
+      const int i = i0 + u * nw;
+      if (i < n) {
+        const float* pp = part_ptr(i);
+        m[u] = __ldcg(pp);
+        l[u] = __ldcg(pp + 1);
+        v[u] = __ldcg(reinterpret_cast<const float4*>(pp + 4) + lane);
+      } else {
+        m[u] = -INFINITY;
+        l[u] = 0.f;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float Mn = Mw;
+#pragma unroll
+    for (int u = 0; u < kMaxPer; ++u) Mn = fmaxf(Mn, m[u]);
+    if (Mn != -INFINITY) {
+      const float al = exp2f(Mw - Mn);  // Mw = -inf gives 0
+      Lw *= al;
+      acc.x *= al;
+      acc.y *= al;
+      acc.z *= al;
+      acc.w *= al;
+#pragma unroll
+      for (int u = 0; u < kMaxPer; ++u) {
+        const float sc = exp2f(m[u] - Mn);  // padding entries: m = -inf gives 0
+        Lw = fmaf(sc, l[u], Lw);
+        acc.x = fmaf(sc, v[u].x, acc.x);
+        acc.y = fmaf(sc, v[u].y, acc.y);
+        acc.z = fmaf(sc, v[u].z, acc.z);
+        acc.w = fmaf(sc, v[u].w, acc.w);
+      }
+      Mw = Mn;
+    }
+  }
+  float* rw = red + w * (kD + 4);
+  reinterpret_cast<float4*>(rw + 4)[lane] = acc;
+  if (lane == 0) {
+    rw[0] = Mw;
+    rw[1] = Lw;
+  }
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nw * 32) : "memory");
+  if (w == 0) {
+    float M = -INFINITY;
+    for (int ww = 0; ww < nw; ++ww) M = fmaxf(M, red[ww * (kD + 4)]);
+    float L = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int ww = 0; ww < nw; ++ww) {
+        const float* r = red + ww * (kD + 4);
+        const float sc = exp2f(r[0] - M);
+        L = fmaf(sc, r[1], L);
+        const float4 x = reinterpret_cast<const float4*>(r + 4)[lane];
+        o.x = fmaf(sc, x.x, o.x);
+        o.y = fmaf(sc, x.y, o.y);
+        o.z = fmaf(sc, x.z, o.z);
+        o.w = fmaf(sc, x.w, o.w);
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    reinterpret_cast<float4*>(a.out + ((int64_t)b * a.Hq + (int64_t)h * a.G + g) * kD)[lane] =
+        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+  }
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nw * 32) : "memory");
+}
+
 // ---------------------------------------------------------------------------
-// Retrieve + attention kernel. NT = number of 8-head tiles (G <= 8 * NT).
+// The decode-step kernel. NT = number of 8-head tiles (G <= 8 * NT); GS = threads of
+// one manager group in phase B.
 // ---------------------------------------------------------------------------
-template <int NT>
+template <int NT, int GS>
 __global__ void __launch_bounds__(Roles<NT>::kThreads, 1)
-attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_hit_tasks) {
+decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_hit_tasks) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  AttnSmem sm;
-  attn_smem_layout(&sm, base);
+  StepSmem sm;
+  step_smem_layout(&sm, base);
+  constexpr int kThreads = Roles<NT>::kThreads;
   constexpr int NG = Roles<NT>::kGroups, NC = Roles<NT>::kConsumers;
+  constexpr int kWarps = kThreads / 32;
+  constexpr uint32_t kAll = 0xffffffffu;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n_miss = a.counters[kCtrMiss];
-  const int tag = a.counters[kCtrStep] + 1;  // ready-flag value of this step (flags are never reset)
+  const int t = a.counters[kCtrStep];
+  const int tag = t + 1;  // flag value of this step (flags are never reset)
+  const int U = a.B * a.Hkv;
+  const int kmax = U * a.k;  // miss-list capacity
+  unsigned long long* tl = a.timeline;
 
   if (tid == 0) {
+    if (tl) atomicMax(tl + 0, ~globaltimer_ns());
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), kCWarps);  // the four warps of the stage's group
@@ -338,16 +481,155 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
     *sm.hits_groups = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+
+  // ------------------------------ A. scoring ------------------------------
+  // The layer's partitions, request-major then head then partition, are split into
+  // equal contiguous row ranges, one per warp of the grid. A warp scores its range in
+  // batches of up to 8 rows of one unit, the next batch's loads in flight while the
+  // current one is reduced; it adds its rows to a unit's counter (release) when it
+  // leaves the unit. Wide units also count their keys' top 12 bits.
+  {
+    int64_t* s_pre = reinterpret_cast<int64_t*>(sm.region);  // [B + 1] rows before request b
+    if (warp == 0) {
+      int64_t run = 0;
+      for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int64_t v = b < a.B ? (int64_t)a.Hkv * a.P_b[b] : 0;
+        int64_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t y = __shfl_up_sync(kAll, x, o);
+          if (lane >= o) x += y;
+        }
+        if (b < a.B) s_pre[b] = run + x - v;
+        run += __shfl_sync(kAll, x, 31);
+      }
+      if (lane == 0) s_pre[a.B] = run;
+    }
+    __syncthreads();
+    const int64_t R = s_pre[a.B];
+    const int64_t TW = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
+    int64_t r = R * gw / TW;
+    const int64_t r_end = R * (gw + 1) / TW;
+    if (r < r_end) {
+      int lo = 0, hi = a.B;  // the request of row r: the largest b with s_pre[b] <= r
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pre[mid] <= r) lo = mid;
+        else hi = mid;
+      }
+      int b = lo, Pb = a.P_b[b];
+      const int64_t off = r - s_pre[b];
+      int h = (int)(off / Pb), p = (int)(off - (int64_t)h * Pb);
+      int n = (int)min((int64_t)min(sel::kRowsPerBatch, Pb - p), r_end - r);
+      float4 cur[sel::kRowsPerBatch], nxt[sel::kRowsPerBatch];
+      sel::load_rows(cur, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, p) * kD), n, lane);
+      float4 qv = sel::qsum_lane(a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
+      int counted = 0;
+      for (;;) {
+        // the next batch: the rest of this unit, else the start of the next non-empty unit
+        const int64_t r2 = r + n;
+        const bool more = r2 < r_end;
+        int b2 = b, h2 = h, p2 = p + n, Pb2 = Pb, n2 = 0;
+        if (more) {
+          if (p2 >= Pb) {
+            p2 = 0;
+            if (++h2 == a.Hkv) {
+              h2 = 0;
+              do {
+                Pb2 = a.P_b[++b2];
+              } while (Pb2 == 0);
+            }
+          }
+          n2 = (int)min((int64_t)min(sel::kRowsPerBatch, Pb2 - p2), r_end - r2);
+          sel::load_rows(nxt, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b2, h2, p2) * kD), n2, lane);
+        }
+        const int ul = b * a.Hkv + h;
+        const float x = sel::score_batch(cur, qv, lane);
+        if (lane < n) {
+          a.scores[(int64_t)ul * a.P_max + p + lane] = x;
+          if (a.hist12) atomicAdd(a.hist12 + (int64_t)ul * sel::kHistBins + (sel::float_key(x) >> (32 - sel::kHistBits)), 1);
+        }
+        counted += n;
+        const bool leave = !more || b2 != b || h2 != h;
+        if (leave) {
+          __syncwarp();
+          if (lane == 0) red_release_add(a.unit_rows + ul, counted);
+          counted = 0;
+        }
+        if (!more) break;
+        if (leave) qv = sel::qsum_lane(a.q + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
+        r = r2;
+        b = b2;
+        h = h2;
+        p = p2;
+        Pb = Pb2;
+        n = n2;
+#pragma unroll
+        for (int i = 0; i < sel::kRowsPerBatch; ++i) cur[i] = nxt[i];
+      }
+    }
+  }
+  __syncthreads();
+  if (tl && tid == 0) atomicMax(tl + 1, globaltimer_ns());
+
+  // ------------------------------ B. managing ------------------------------
+  {
+    constexpr int kGroupsB = kThreads / GS;
+    const int grp = tid / GS, gt = tid - grp * GS;
+    if (grp < kGroupsB) {
+      sel::MgrSmem ms;
+      const size_t gbytes = sel::mgr_smem_layout(GS, a.P_max, a.cap, a.k, a.D, nullptr, nullptr);
+      sel::mgr_smem_layout(GS, a.P_max, a.cap, a.k, a.D, &ms, sm.region + (size_t)grp * gbytes);
+      const int bar = 1 + grp;
+      for (;;) {
+        if (gt == 0) {
+          int ul = atomicAdd(&a.counters[kCtrManage], 1);
+          int ok = 1;
+          if (ul < U) {
+            // wait until every partition of the unit is scored
+            const int P = a.P_b[ul / a.Hkv];
+            ok = wait_flag(a.unit_rows + ul, P, false, a.err) ? 1 : 0;
+            a.unit_rows[ul] = 0;  // every row of this step is in: ready for the next step
+          }
+          ms.gs->unit = ul;
+          ms.gs->ok = ok;
+        }
+        sel::gsync<GS>(bar);
+        const int ul = ms.gs->unit;
+        const int ok = ms.gs->ok;
+        sel::gsync<GS>(bar);
+        if (ul >= U) break;
+        if (!ok) {
+          if (gt == 0) {
+            atomicOr(a.err, kErrTimeout);
+            // publish the unit with nothing selected, so nobody waits for it
+            a.keff[ul] = 0;
+            a.n_hit[ul] = 0;
+            __threadfence();
+            st_release(a.unit_ready + ul, tag);
+            atomicAdd(&a.counters[kCtrManaged], 1);
+          }
+          continue;
+        }
+        sel::manage_unit<GS>(a, ul, t, tag, ms, bar, gt);
+        if (tl && gt == 0) atomicMax(tl + 2, globaltimer_ns());
+      }
+    }
+  }
+  // the manager groups wrote the region with generic stores; TMA writes it next
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
   volatile int* abort_flag = sm.abort_flag;
 
+  // ------------------------------ C. retrieval + attention ------------------------------
   if (warp >= NC + NG) {
     // ------------------------------ retrievers ------------------------------
-    // retr_warps warps copy from the start; retr_late more join once this CTA's
-    // resident pages are issued (so they do not slow the HBM-bound hits); the rest idle.
+    // kEarly warps copy from the start; the others join once this CTA's resident pages
+    // are issued (so they do not slow the HBM-bound hits).
     const int rw = warp - NC - NG;
-    bool active = rw < a.retr_warps && !a.retrieve_in_select;
-    if (!active && rw < a.retr_warps + a.retr_late && !a.retrieve_in_select) {
+    bool active = rw < a.retr_warps;
+    if (!active && rw < a.retr_warps + a.retr_late) {
       volatile int* hd = sm.hits_done;
       const unsigned long long t0 = globaltimer_ns();
       for (uint32_t it = 1; it < (1u << 30) && !*hd; ++it) {
@@ -361,9 +643,21 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
     for (; active;) {
       int m = 0;
       if (lane == 0) m = atomicAdd(&a.counters[kCtrRetrieve], 1);
-      m = __shfl_sync(0xffffffffu, m, 0);
-      if (m >= n_miss) break;
-      const int64_t sp = a.miss_src[m], dp = a.miss_dst[m];
+      m = __shfl_sync(kAll, m, 0);
+      int st = 0;
+      if (lane == 0) st = miss_entry(a, m, tag, U, kmax);
+      st = __shfl_sync(kAll, st, 0);
+      if (st == 0) break;
+      if (st < 0) {
+        if (lane == 0) {
+          atomicOr(a.err, kErrTimeout);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      __syncwarp();
+      (void)ld_acquire(a.miss_tag + m);
+      const int64_t sp = __ldcg(a.miss_src + m), dp = __ldcg(a.miss_dst + m);
       const bool in_range = sp >= 0 && sp < a.host_pages && dp >= 0 && dp < a.pool_slots;
       if (!in_range && lane == 0) atomicOr(a.err, kErrIndex);  // never expected: skip the copy
       const uint4* src = reinterpret_cast<const uint4*>(a.host_store + sp * kPageElems);
@@ -384,46 +678,71 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
     // ------------------------------ producers ------------------------------
     // Producer warp g feeds consumer group g: stage indices i = g, g + NG, ... use ring
     // stage i % kStages. Its stream: resident-page tasks (up to ppt pages of one unit,
-    // claimed from a shared counter), then retrieved pages (one page each, in miss-list
-    // order, once its ready flag is published), then a sentinel.
+    // claimed from a shared counter, after the unit's ready flag), then retrieved pages
+    // (one page each, in miss-list order, once the entry is written and its page
+    // published), then a sentinel.
     // The whole warp runs the loop so that nothing the issue path needs is a fresh
     // global load: tasks are claimed two ahead, the next task's page descriptors load
-    // into the lanes' registers (lane j: page j) while the current task issues, and the
-    // next retrieved page's miss-list entry loads before its flag is awaited. Lane 0
-    // alone waits on the ring barriers and issues the copies.
-    constexpr uint32_t kAll = 0xffffffffu;
+    // into the lanes' registers (lane j: page j) while the current task issues (if its
+    // unit is managed by then; else when it becomes current), and the next retrieved
+    // page's miss-list entry loads before its flag is awaited. Lane 0 alone waits on
+    // the ring barriers and issues the copies.
     const int g = warp - NC;
     const uint32_t qbytes = (uint32_t)a.G * kD * 2;
-    const int U = a.B * a.Hkv;
+    bool ok = true, done = false;
     if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-    auto load_task = [&](int T, int& slot, int& valid, int& nhit) {
-      if (T < n_hit_tasks) {
-        const int tu = T / a.n_chunks, j0 = (T - tu * a.n_chunks) * a.ppt;
-        nhit = a.n_hit[tu];
-        const bool in = lane < a.ppt && j0 + lane < a.ka;
-        slot = in ? a.att_slot[tu * a.ka + j0 + lane] : 0;
-        valid = in ? a.att_valid[tu * a.ka + j0 + lane] : 0;
+    // Descriptors of hit task T (lane j: its page j) once the task's unit is managed;
+    // `block` waits for that (bounded), else returns false when it is not managed yet.
+    auto load_task = [&](int T, bool block, int& slot, int& valid, int& nhit) -> bool {
+      if (T >= n_hit_tasks) return true;
+      const int tu = T / a.n_chunks, j0 = (T - tu * a.n_chunks) * a.ppt;
+      int r = 0;
+      if (lane == 0) {
+        if (block) {
+          r = wait_flag(a.unit_ready + tu, tag, true, a.err) ? 1 : -1;
+        } else {
+          r = ld_relaxed(a.unit_ready + tu) == tag ? 1 : 0;
+        }
       }
+      r = __shfl_sync(kAll, r, 0);
+      if (r < 0) ok = false;
+      if (r <= 0) return false;
+      __syncwarp();
+      (void)ld_acquire(a.unit_ready + tu);
+      nhit = __ldcg(a.n_hit + tu);
+      const bool in = lane < a.ppt && j0 + lane < a.ka;
+      slot = in ? __ldcg(a.att_slot + (int64_t)tu * a.ka + j0 + lane) : 0;
+      valid = in ? __ldcg(a.att_valid + (int64_t)tu * a.ka + j0 + lane) : 0;
+      return true;
     };
     int cur_task = 0, cur_ul = 0, cur_n = 0, cur_j = 0, cur_y = 0, cur_valid = 0;
-    int nx_task, nx_slot = 0, nx_valid = 0, nx_nhit = 0, c2_raw;
+    int nx_task, nx_slot = 0, nx_valid = 0, nx_nhit = 0, c2_raw = 0;
+    bool nx_loaded;
+    // Tasks are claimed two ahead when there are several per producer; with few tasks a
+    // producer holds one claim at a time, so the tasks spread over every producer.
+    const bool ahead2 = n_hit_tasks >= 4 * (int)gridDim.x * NG;
     {
       const int t0 = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
       nx_task = __shfl_sync(kAll, t0, 0);
-      load_task(nx_task, nx_slot, nx_valid, nx_nhit);
-      c2_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
+      nx_loaded = load_task(nx_task, false, nx_slot, nx_valid, nx_nhit);
+      if (ahead2) c2_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
     }
     bool in_miss = false;
     // retrieved pages: the next entry claimed and loading ahead
-    int mq = 0, mq_att = 0, mq_valid = 0, m_raw = 0;
+    int mq = 0, mq_att = 0, mq_valid = 0, mq_state = 0, m_raw = 0;
     int64_t mq_dst = 0;
     bool m_init = false;
     auto miss_advance = [&]() {
       mq = __shfl_sync(kAll, m_raw, 0);
-      if (mq < n_miss) {
-        mq_att = a.miss_att[mq];
-        mq_dst = a.miss_dst[mq];
-        mq_valid = a.miss_valid[mq];
+      int st = 0;
+      if (lane == 0) st = miss_entry(a, mq, tag, U, kmax);
+      mq_state = __shfl_sync(kAll, st, 0);
+      if (mq_state == 1) {
+        __syncwarp();
+        (void)ld_acquire(a.miss_tag + mq);
+        mq_att = __ldcg(a.miss_att + mq);
+        mq_dst = __ldcg(a.miss_dst + mq);
+        mq_valid = __ldcg(a.miss_valid + mq);
       }
       m_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskMisses], 1) : 0;
     };
@@ -433,7 +752,6 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
     int last_issue[kStages];  // lane 0: last stage index that staged a page in each ring stage
 #pragma unroll
     for (int st = 0; st < kStages; ++st) last_issue[st] = -1;
-    bool ok = true, done = false;
     for (int i = g; ok && !done; i += NG) {
       if (__shfl_sync(kAll, *abort_flag, 0)) {
         ok = false;
@@ -453,12 +771,18 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
             last_page = j == cur_n - 1;
             have = true;
           } else {
+            if (nx_task < 0) {  // one claim at a time: the next task is claimed only now
+              const int tn = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
+              nx_task = __shfl_sync(kAll, tn, 0);
+              nx_loaded = false;
+            }
             const int T = nx_task;
             if (T >= n_hit_tasks) {
               in_miss = true;
               leave_hits();
               continue;
             }
+            if (!nx_loaded && !load_task(T, true, nx_slot, nx_valid, nx_nhit)) break;  // ran out of time
             const int tu = T / a.n_chunks, j0 = (T - tu * a.n_chunks) * a.ppt;
             cur_task = T;
             cur_ul = tu;
@@ -475,9 +799,14 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
               cur_y = (int)(((a.unit_base + tu) * a.cap + slot) * 128);
             }
             cur_valid = nx_valid;
-            nx_task = __shfl_sync(kAll, c2_raw, 0);  // claimed a task ago: no wait
-            load_task(nx_task, nx_slot, nx_valid, nx_nhit);
-            c2_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
+            if (ahead2) {
+              nx_task = __shfl_sync(kAll, c2_raw, 0);  // claimed a task ago: no wait
+              c2_raw = lane == 0 ? atomicAdd(&a.counters[kCtrTaskHits], 1) : 0;
+              nx_loaded = load_task(nx_task, false, nx_slot, nx_valid, nx_nhit);
+            } else {
+              nx_task = -1;
+              nx_loaded = false;
+            }
           }
         } else {
           if (!m_init) {
@@ -485,12 +814,16 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
             miss_advance();
             m_init = true;
           }
-          if (mq >= n_miss) {
+          if (mq_state == 0) {
             done = true;
             break;
           }
+          if (mq_state < 0) {
+            ok = false;
+            break;
+          }
           int okf = 1;
-          if (lane == 0) okf = wait_flag(a.ready + mq, tag, true) ? 1 : 0;
+          if (lane == 0) okf = wait_flag(a.ready + mq, tag, true, a.err) ? 1 : 0;
           if (!__shfl_sync(kAll, okf, 0)) {
             ok = false;
             break;
@@ -538,7 +871,7 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
         sm.meta[st] = m;
         const uint32_t fb = smem_u32(&sm.full[st]);
         mbar_arrive_expect_tx(fb, kPageBytes + (first ? qbytes : 0u));
-        const uint32_t dst = smem_u32(sm.ring + (size_t)st * kStageBytes);
+        const uint32_t dst = smem_u32(sm.region + (size_t)st * kStageBytes);
         tma_load_2d(dst, &tmap, fb, 0, y);
         tma_load_2d(dst + 8192, &tmap, fb, 64, y);
         tma_load_2d(dst + 16384, &tmap, fb, 0, y + 64);
@@ -587,7 +920,7 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
       }
       const StageMeta m = sm.meta[st];
       if (m.part < 0) break;  // the group's sentinel
-      uint8_t* stage = sm.ring + (size_t)st * kStageBytes;
+      uint8_t* stage = sm.region + (size_t)st * kStageBytes;
       if (m.first) {
         // query rows of the unit, brought with the task's first page: B operand fragments
         const uint8_t* qs = stage + kPageBytes;
@@ -735,57 +1068,132 @@ attend_retrieve_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, in
   }
 
   // ---------------- all pages of all CTAs done: combine the partials ----------------
-  // Every warp of the CTA (retrievers after their last claim, the producer, the
+  // Every warp of the CTA (retrievers after their last claim, the producers, the
   // consumers after their last page) meets here before the CTA arrives, so block 0's
   // counter reset below cannot race with a late claim of this step.
   __syncthreads();
   if (tid == 0) {
+    if (tl) atomicMax(tl + 3, globaltimer_ns());
     __threadfence();
     atomicAdd(&a.counters[kCtrArrive], 1);
     const int target = (int)gridDim.x * tag;  // the counter grows by gridDim.x every step
-    if (!wait_flag(&a.counters[kCtrArrive], target, false)) atomicOr(a.err, kErrTimeout);
+    // no early exit on another wait's timeout here: block 0 resets the step's counters only
+    // once every CTA has stopped claiming work
+    if (!wait_flag(&a.counters[kCtrArrive], target, false, nullptr)) atomicOr(a.err, kErrTimeout);
     if (blockIdx.x == 0) {  // the step's counters are no longer read by anyone
       a.counters[kCtrMiss] = 0;
       a.counters[kCtrTaskHits] = 0;
       a.counters[kCtrTaskMisses] = 0;
       a.counters[kCtrRetrieve] = 0;
+      a.counters[kCtrManage] = 0;
+      a.counters[kCtrManaged] = 0;
       a.counters[kCtrStep] += 1;
     }
   }
   __syncthreads();
   if (warp >= NC) return;
-  // (unit, head) pairs spread over every consumer warp of the grid
-  const int pairs = a.B * a.Hkv * a.G;
-  for (int p = blockIdx.x * NC + warp; p < pairs; p += gridDim.x * NC) combine_head(a, p / a.G, p % a.G, lane);
+  const int pairs = U * a.G;
+  if (pairs <= (int)gridDim.x && a.n_chunks + a.k > 16) {
+    // few (unit, head) pairs with many partials each: one pair per CTA, all its consumer warps
+    // (the ring is free: every CTA is past its pages)
+    float* red = reinterpret_cast<float*>(sm.region);
+    for (int p = blockIdx.x; p < pairs; p += gridDim.x) combine_head_cta(a, p / a.G, p % a.G, warp, NC, lane, red, 5);
+  } else {
+    // (unit, head) pairs spread over every consumer warp of the grid
+    for (int p = blockIdx.x * NC + warp; p < pairs; p += gridDim.x * NC) combine_head(a, p / a.G, p % a.G, lane);
+  }
+  if (tl && lane == 0) atomicMax(tl + 4, globaltimer_ns());
+}
+
+// ---------------------------------------------------------------------------
+// Debug: resolve every partition through the two-level table; live segments per unit.
+// ---------------------------------------------------------------------------
+__global__ void resolve_all_kernel(LayerArgs a, int32_t* resolve, int32_t* live) {
+  __shared__ int s_live;
+  const int ul = blockIdx.x;
+  const int b = ul / a.Hkv;
+  const int P = a.P_b[b];
+  const int64_t unit = a.unit_base + ul;
+  if (threadIdx.x == 0) s_live = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < a.P_max; p += blockDim.x) {
+    int s = -1;
+    if (p < P) {
+      const int sg = a.dir[unit * a.D + (p >> 6)];
+      s = sg < 0 ? -1 : a.seg[(int64_t)sg * kSeg + (p & 63)];
+    }
+    resolve[(int64_t)ul * a.P_max + p] = s;
+  }
+  for (int d = threadIdx.x; d < a.D; d += blockDim.x)
+    if (a.dir[unit * a.D + d] >= 0) atomicAdd(&s_live, 1);
+  __syncthreads();
+  if (threadIdx.x == 0) live[ul] = s_live;
+}
+
+__global__ void set_int_kernel(int32_t* p, int32_t v) { *p = v; }
+
+template <int NT, int GS>
+const void* kernel_ptr() {
+  return (const void*)decode_step_kernel<NT, GS>;
+}
+
+// The kernel instance for a layer: NT from the group size G, GS from mgr_gs.
+const void* pick_kernel(const LayerArgs& a) {
+  if (a.G <= 8) {
+    switch (a.mgr_gs) {
+      case 32: return kernel_ptr<1, 32>();
+      case 128: return kernel_ptr<1, 128>();
+      default: return kernel_ptr<1, 512>();
+    }
+  }
+  switch (a.mgr_gs) {
+    case 32: return kernel_ptr<2, 32>();
+    case 128: return kernel_ptr<2, 128>();
+    default: return kernel_ptr<2, 256>();
+  }
 }
 
 }  // namespace
 
-size_t attention_smem_bytes() { return attn_smem_layout(nullptr, nullptr) + 1024; }
+int step_threads(int G) { return G <= 8 ? Roles<1>::kThreads : Roles<2>::kThreads; }
 
-cudaError_t attention_configure() {
-  const int kMaxShared = 100;  // cudaSharedmemCarveoutMaxShared
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(attend_retrieve_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)attention_smem_bytes())) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(attend_retrieve_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)attention_smem_bytes())) != cudaSuccess)
-    return e;
-  (void)kMaxShared;
-  return cudaSuccess;
+int step_full_group(int G) { return G <= 8 ? 512 : 256; }
+
+size_t step_ring_bytes() { return (size_t)kRingBytes; }
+
+// Dynamic shared memory of the decode-step kernel: header + max(ring, manager groups) +
+// 1 KiB for aligning the base.
+size_t step_smem_bytes(const LayerArgs& a) {
+  const int groups = step_threads(a.G) / a.mgr_gs;
+  const size_t mgr = (size_t)groups * sel::mgr_smem_layout(a.mgr_gs, a.P_max, a.cap, a.k, a.D, nullptr, nullptr);
+  return kHeaderBytes + (mgr > (size_t)kRingBytes ? mgr : (size_t)kRingBytes) + 1024;
 }
 
-cudaError_t launch_attend_retrieve(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st) {
+size_t mgr_group_bytes(int gs, const LayerArgs& a) {
+  return sel::mgr_smem_layout(gs, a.P_max, a.cap, a.k, a.D, nullptr, nullptr);
+}
+
+cudaError_t step_configure(const LayerArgs& a) {
+  const size_t smem = step_smem_bytes(a);
+  return cudaFuncSetAttribute(pick_kernel(a), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+cudaError_t launch_decode_step(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st) {
   int n_hit_tasks = a.B * a.Hkv * a.n_chunks;
   LayerArgs args = a;
   void* params[] = {const_cast<CUtensorMap*>(tmap), &args, &n_hit_tasks};
-  if (a.G <= 8)
-    return cudaLaunchCooperativeKernel((const void*)attend_retrieve_kernel<1>, dim3(grid),
-                                       dim3(Roles<1>::kThreads), params, attention_smem_bytes(), st);
-  return cudaLaunchCooperativeKernel((const void*)attend_retrieve_kernel<2>, dim3(grid), dim3(Roles<2>::kThreads),
-                                     params, attention_smem_bytes(), st);
+  return cudaLaunchCooperativeKernel(pick_kernel(a), dim3(grid), dim3(step_threads(a.G)), params,
+                                     step_smem_bytes(a), st);
 }
 
+cudaError_t launch_set_int(int32_t* p, int32_t v, cudaStream_t st) {
+  set_int_kernel<<<1, 1, 0, st>>>(p, v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_resolve_all(const LayerArgs& a, int32_t* resolve, int32_t* live_segs, cudaStream_t st) {
+  resolve_all_kernel<<<a.B * a.Hkv, 256, 0, st>>>(a, resolve, live_segs);
+  return cudaGetLastError();
+}
 
 }  // namespace spin

@@ -9,10 +9,9 @@
 //   * per-page state: slot -> partition, last-use step (bucketed-LRU timestamps);
 //   * fp32 partition summaries in HBM;
 //   * with variable partitions (max_partitions > 0), one token count per host page.
-// A decode step of one layer enqueues up to three kernels on the caller's stream:
-// score (only for narrow layers) -> select+manage -> retrieve+attention+combine
-// (cooperative); the first step after an offload call adds one read pass over the
-// host store. A KV append (spin_append_kv, tail mode) is a kernel of its own that the
+// A decode step of one layer is one cooperative kernel on the caller's stream
+// (score -> select + manage -> retrieve + attention -> combine); the first step after
+// an offload call adds one read pass over the host store before it. A KV append (spin_append_kv, tail mode) is a kernel of its own that the
 // caller enqueues before the step.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -65,6 +64,10 @@ struct LayerBuf {
   int32_t* miss_att = nullptr;
   int32_t* miss_valid = nullptr;
   int32_t* ready = nullptr;
+  int32_t* miss_tag = nullptr;
+  int32_t* unit_rows = nullptr;
+  int32_t* unit_ready = nullptr;
+  int32_t* hist12 = nullptr;
   int32_t* att_slot = nullptr;
   int32_t* att_valid = nullptr;
   int32_t* n_hit = nullptr;
@@ -75,13 +78,13 @@ struct LayerBuf {
   LayerArgs args{};
 };
 
-constexpr int kNumStages = 5;  // select, manage, retrieve, attention, combine
+constexpr int kNumStages = 5;  // score, manage, pages (retrieval + attention), combine, whole kernel
+constexpr int kTimelineCalls = 4096;  // stage-stamp records of timed calls between two synchronisations
 
-// Events of one timed call: 0 start, 1 after score, 2 after select/manage,
-// 3 after retrieve + attention + combine (one kernel).
-constexpr int kTimedEvents = 4;
+// One timed call: CUDA events around the kernel and the slot of its stage stamps.
 struct TimedCall {
-  cudaEvent_t ev[kTimedEvents];
+  cudaEvent_t ev[2];
+  int rec;
 };
 
 }  // namespace
@@ -92,10 +95,9 @@ struct spin_ctx {
   uint32_t flags = 0;
   int B = 0, L = 0, Hq = 0, Hkv = 0, G = 0, k = 0, cap = 0, D = 0, P_max = 0, ppt = 1, n_chunks = 1;
   int sm_count = 0;
-  int select_group = 0;  // SPIN_SELECT_GROUP: threads of the top-k/manager group (0 = by unit size)
-  int retr_warps = 2;  // SPIN_RETRIEVE_WARPS (1..8): retriever warps per attend CTA from its start
-  int retr_late = 8;   // SPIN_RETRIEVE_LATE (0..8): retriever warps that join after the CTA's resident pages
-  int retrieve_in_select = 0;  // SPIN_RETRIEVE_IN_SELECT: misses copied by the select/manage kernel
+  int retr_warps = 2;  // retriever warps per CTA from the start of the retrieval phase
+  int retr_late = 4;   // retriever warps that join after the CTA's resident pages are issued
+  int mgr_gs = 512;    // threads of one manager group
   int store_warm = 1;          // SPIN_STORE_WARM: read passes over the host store after it is written (0..8)
   bool store_cold = false;     // the store was written since its last read pass
   int64_t warm_stride = 32768; // bytes between the read pass's loads: the host page size, at most 32 KiB
@@ -147,6 +149,8 @@ struct spin_ctx {
   // stage timing
   std::vector<TimedCall> pending;
   std::vector<cudaEvent_t> spare_events;
+  unsigned long long* d_timeline = nullptr;  // [kTimelineCalls][kTlSlots]
+  int next_rec = 0;
   double ms[kNumStages] = {0, 0, 0, 0, 0};
   int64_t timed_calls = 0;
   int64_t bytes_meta = 0, bytes_flat = 0, bytes_pool = 0, bytes_store = 0, bytes_summ = 0;
@@ -263,19 +267,31 @@ int check_device_error(spin_ctx* c) {
 int sync_ctx(spin_ctx* c) {
   SPIN_CUDA(c, cudaDeviceSynchronize(), "synchronising the device");
   // fold finished stage timings
-  for (auto& t : c->pending) {
-    auto el = [&](int x, int y) {
+  if (!c->pending.empty()) {
+    std::vector<unsigned long long> tl((size_t)kTimelineCalls * kTlSlots);
+    SPIN_CUDA(c, cudaMemcpy(tl.data(), c->d_timeline, tl.size() * 8, cudaMemcpyDeviceToHost), "reading stage stamps");
+    for (auto& t : c->pending) {
       float ms = 0.f;
-      return cudaEventElapsedTime(&ms, t.ev[x], t.ev[y]) == cudaSuccess ? (double)ms : 0.0;
-    };
-    c->ms[0] += el(0, 1);
-    c->ms[1] += el(1, 2);
-    c->ms[2] += el(2, 3);  // retrieve, attention and combine share one kernel: retrieve and
-    c->ms[3] += el(2, 3);  // attention both report its time, combine reports none
-
-    for (auto e : t.ev) c->spare_events.push_back(e);
+      if (cudaEventElapsedTime(&ms, t.ev[0], t.ev[1]) == cudaSuccess) c->ms[4] += ms;
+      const unsigned long long* r = tl.data() + (size_t)t.rec * kTlSlots;
+      const unsigned long long t0 = ~r[kTlStart];
+      auto seg = [&](unsigned long long from, unsigned long long to) {
+        return (to > from && from != 0) ? (double)(to - from) * 1e-6 : 0.0;
+      };
+      // consecutive stamps of the critical path: scoring done, last unit published,
+      // last page attended, last combine done
+      const unsigned long long s1 = r[kTlScored], s2 = std::max(r[kTlManaged], s1), s3 = std::max(r[kTlPages], s2),
+                               s4 = std::max(r[kTlEnd], s3);
+      c->ms[0] += seg(t0, s1);
+      c->ms[1] += seg(s1, s2);
+      c->ms[2] += seg(s2, s3);
+      c->ms[3] += seg(s3, s4);
+      for (auto e : t.ev) c->spare_events.push_back(e);
+    }
+    c->pending.clear();
+    SPIN_CUDA(c, cudaMemset(c->d_timeline, 0, (size_t)kTimelineCalls * kTlSlots * 8), "clearing stage stamps");
+    c->next_rec = 0;
   }
-  c->pending.clear();
   return check_device_error(c);
 }
 
@@ -312,6 +328,7 @@ int validate(const spin_config* cfg) {
   if (!cfg) return fail(nullptr, SPIN_ERR_INVALID, "cfg is NULL");
   if (cfg->batch < 1 || cfg->layers < 1 || cfg->kv_heads < 1 || cfg->q_heads < 1)
     return fail(nullptr, SPIN_ERR_INVALID, "batch, layers, q_heads and kv_heads must be >= 1");
+  if (cfg->batch > 16384) return fail(nullptr, SPIN_ERR_INVALID, "batch must be <= 16384");
   if (cfg->q_heads % cfg->kv_heads != 0 || cfg->q_heads / cfg->kv_heads > kMaxGroup)
     return fail(nullptr, SPIN_ERR_INVALID, "q_heads must be a multiple of kv_heads with a group of at most %d",
                 kMaxGroup);
@@ -363,8 +380,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.S = (int32_t)c->S;
   a.retr_warps = c->retr_warps;
   a.retr_late = c->retr_late;
-  a.retrieve_in_select = c->retrieve_in_select;
-  a.select_group = c->select_group;
+  a.mgr_gs = c->mgr_gs;
   a.ka = c->ka;
   a.P_b = c->d_P_lb + (int64_t)l * c->B;
   a.ntok_b = c->d_ntok_lb + (int64_t)l * c->B;
@@ -397,12 +413,17 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.miss_att = lb.miss_att;
   a.miss_valid = lb.miss_valid;
   a.ready = lb.ready;
+  a.miss_tag = lb.miss_tag;
+  a.unit_rows = lb.unit_rows;
+  a.unit_ready = lb.unit_ready;
+  a.hist12 = lb.hist12;
   a.att_slot = lb.att_slot;
   a.att_valid = lb.att_valid;
   a.n_hit = lb.n_hit;
   a.counters = lb.counters;
   a.partials = lb.partials;
   a.stats = c->d_stats;
+  a.timeline = nullptr;
   a.err = c->d_err;
   return a;
 }
@@ -572,23 +593,16 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   SPIN_CUDA(nullptr, cudaMemset(c->d_stats, 0, 8 * 8), "initialising counters");
   SPIN_CUDA(nullptr, cudaMemset(c->d_err, 0, 4), "initialising counters");
 
-  if (const char* env = getenv("SPIN_RETRIEVE_WARPS")) {
-    const int v = atoi(env);
-    if (v >= 1 && v <= 8) c->retr_warps = v;
-  }
-  if (c->G > 8) c->retr_warps = std::min(c->retr_warps, 4);  // the two-tile kernel has four retriever warps
-  if (const char* env = getenv("SPIN_RETRIEVE_LATE")) {
-    const int v = atoi(env);
-    if (v >= 0 && v <= 8) c->retr_late = v;
-  }
-  if (const char* env = getenv("SPIN_RETRIEVE_IN_SELECT")) c->retrieve_in_select = atoi(env) != 0;
+  // retriever warps: two from the start, the rest (four in the one-tile kernel, two in the
+  // two-tile kernel) once the CTA's resident pages are issued
+  c->retr_warps = 2;
+  c->retr_late = c->G <= 8 ? 4 : 2;
   if (const char* env = getenv("SPIN_STORE_WARM")) c->store_warm = std::max(0, std::min(8, atoi(env)));
   {
     const long pg = sysconf(_SC_PAGESIZE);
     c->warm_stride = pg >= 4096 ? std::min<int64_t>(pg, kPageBytes) : 4096;
   }
-  if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = c->retr_late = c->retrieve_in_select = 0;
-  if (const char* env = getenv("SPIN_SELECT_GROUP")) c->select_group = atoi(env);  // 0 auto, 32, 512
+  if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = c->retr_late = 0;
 
   // attention work split: pages per task, about one task per consumer group when pages
   // are few (each task costs a merge and a partial to combine), at most 8
@@ -597,11 +611,42 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   c->ppt = (int)std::max<int64_t>(1, std::min<int64_t>(8, (pages_layer + groups - 1) / groups));
   c->n_chunks = (c->ka + c->ppt - 1) / c->ppt;
 
+  // manager groups: one warp per unit for small units, four warps for mid-size ones, all
+  // the CTA's warps for units too wide for a group of four (or whose shared memory does
+  // not fit four times in the ring's bytes)
+  {
+    LayerArgs probe{};
+    probe.G = c->G;
+    probe.P_max = c->P_max;
+    probe.cap = c->cap;
+    probe.k = c->k;
+    probe.D = c->D;
+    const int threads = step_threads(c->G), full = step_full_group(c->G);
+    auto fits = [&](int gs) { return (size_t)(threads / gs) * mgr_group_bytes(gs, probe) <= step_ring_bytes(); };
+    int gs = c->P_max > 4096 ? full : (c->P_max <= 128 && c->cap <= 1024 && c->k <= 256) ? 32 : 128;
+    if (gs == 32 && !fits(32)) gs = 128;
+    if (gs == 128 && !fits(128)) gs = full;
+    c->mgr_gs = gs;
+    probe.mgr_gs = gs;
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    if (step_smem_bytes(probe) > (size_t)optin)
+      return fail(nullptr, SPIN_ERR_INVALID,
+                  "the page manager of one unit needs %zu bytes of shared memory (max %d): reduce the longest "
+                  "context, topk or buf_mult",
+                  step_smem_bytes(probe), optin);
+  }
+  if (c->flags & SPIN_FLAG_STAGE_TIMING) {
+    ALLOC(c->d_timeline, (int64_t)kTimelineCalls * kTlSlots, "allocating stage stamps");
+    SPIN_CUDA(nullptr, cudaMemset(c->d_timeline, 0, (size_t)kTimelineCalls * kTlSlots * 8), "clearing stage stamps");
+  }
+
   const int64_t Ul = (int64_t)c->B * c->Hkv;
   c->layers.resize(c->L);
   for (int l = 0; l < c->L; ++l) {
     LayerBuf& lb = c->layers[l];
-    ALLOC(lb.scores, Ul * std::max(1, c->P_max), "allocating layer scratch");
+    // (+4: the wide top-k reads a unit's scores four at a time, up to 3 past its last partition)
+    ALLOC(lb.scores, Ul * std::max(1, c->P_max) + 4, "allocating layer scratch");
     ALLOC(lb.sel, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.sel_slot, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.sel_hit, Ul * c->k, "allocating layer scratch");
@@ -615,10 +660,20 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     ALLOC(lb.miss_att, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.miss_valid, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.ready, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.miss_tag, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.unit_rows, Ul, "allocating layer scratch");
+    ALLOC(lb.unit_ready, Ul, "allocating layer scratch");
+    if (c->P_max > 4096 && c->mgr_gs >= 256) {  // wide units: top-12-bit key counts filled while scoring
+      ALLOC(lb.hist12, Ul * 4096, "allocating layer scratch");
+      SPIN_CUDA(nullptr, cudaMemset(lb.hist12, 0, Ul * 4096 * 4), "initialising layer scratch");
+    }
     ALLOC(lb.counters, kNumCtr, "allocating layer scratch");
     ALLOC(lb.partials, Ul * (c->n_chunks + c->ka) * c->G * kPartialStride, "allocating layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.n_hit, 0, Ul * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.ready, 0, Ul * c->k * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.miss_tag, 0, Ul * c->k * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.unit_rows, 0, Ul * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.unit_ready, 0, Ul * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.counters, 0, kNumCtr * 4), "initialising layer counters");
     SPIN_CUDA(nullptr, cudaMemset(lb.keff, 0, Ul * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.sel, 0xff, Ul * c->k * 4), "initialising layer scratch");
@@ -635,44 +690,40 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     g_create_error = c->msg;
     return rc;
   }
-  SPIN_CUDA(nullptr, attention_configure(), "configuring the attention kernel");
-  SPIN_CUDA(nullptr, select_manage_configure(select_manage_smem_bytes(c->layers[0].args)),
-            "configuring the select kernel");
+  SPIN_CUDA(nullptr, step_configure(c->layers[0].args), "configuring the decode-step kernel");
   SPIN_CUDA(nullptr, cudaDeviceSynchronize(), "finishing context set-up");
   return SPIN_OK;
 }
 
-// Enqueue one layer's step on `st`: score -> select/manage -> retrieve+attention+combine.
+// Enqueue one layer's step on `st`: one cooperative kernel (score -> select + manage ->
+// retrieve + attention -> combine).
 int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStream_t st) {
   LayerBuf& lb = c->layers[layer];
   LayerArgs a = lb.args;
   a.q = q;
   a.out = out;
-  const bool timed = (c->flags & SPIN_FLAG_STAGE_TIMING) != 0;
+  // stage timing: CUDA events around the kernel and a record of in-kernel stage stamps
+  // (up to kTimelineCalls timed calls between two synchronising calls)
+  const bool timed = (c->flags & SPIN_FLAG_STAGE_TIMING) != 0 && c->next_rec < kTimelineCalls;
   TimedCall tc{};
   if (timed) {
     for (auto& e : tc.ev) {
       int rc = get_event(c, &e);
       if (rc) return rc;
     }
+    tc.rec = c->next_rec++;
+    a.timeline = c->d_timeline + (size_t)tc.rec * kTlSlots;
   }
-  auto mark = [&](int i) {
-    if (timed) cudaEventRecord(tc.ev[i], st);
-  };
   for (int i = 0; c->store_cold && i < c->store_warm; ++i) {
     // after the store is (re)written, before the first retrieval can touch it
     SPIN_CUDA(c, launch_warm_store(c->d_store, c->bytes_store, c->warm_stride, c->d_warm_sink, c->sm_count, st),
               "launching the host-store read pass");
   }
   c->store_cold = false;
-  mark(0);
-  SPIN_CUDA(c, launch_score(a, st), "launching score");
-  mark(1);
-  SPIN_CUDA(c, launch_select_manage(a, st), "launching select/manage");
-  mark(2);
-  SPIN_CUDA(c, launch_attend_retrieve(a, &c->tmap, c->sm_count, st), "launching retrieve + attention");
-  mark(3);
+  if (timed) cudaEventRecord(tc.ev[0], st);
+  SPIN_CUDA(c, launch_decode_step(a, &c->tmap, c->sm_count, st), "launching the decode step");
   if (timed) {
+    cudaEventRecord(tc.ev[1], st);
     c->pending.push_back(tc);
     c->timed_calls += 1;
   }
@@ -1010,11 +1061,11 @@ int spin_stats(spin_ctx* c, spin_stats_t* out) {
   out->host_store_bytes = c->bytes_store;
   out->summary_bytes = c->bytes_summ;
   out->timed_calls = c->timed_calls;
-  out->ms_select = c->ms[0];
+  out->ms_score = c->ms[0];
   out->ms_manage = c->ms[1];
-  out->ms_retrieve = c->ms[2];
-  out->ms_attention = c->ms[3];
-  out->ms_combine = c->ms[4];
+  out->ms_pages = c->ms[2];
+  out->ms_combine = c->ms[3];
+  out->ms_kernel = c->ms[4];
   out->device_error = c->sticky;
   out->appended_tokens = c->appended;
   out->tail_flushes = (int64_t)st[kStatFlushes];

@@ -33,10 +33,9 @@ enum : uint32_t {
 struct LayerArgs {
   int32_t layer, B, Hq, Hkv, G, k, cap, D, P_max, n_chunks, ppt, S;
   int32_t ka;                // attention entries per unit: k, plus one for the tail page in tail mode
-  int32_t retr_warps;        // retriever warps active per CTA of the attend kernel from its start
+  int32_t retr_warps;        // retriever warps active per CTA from the start of phase C
   int32_t retr_late;         // further retriever warps that join once the CTA's resident pages are issued
-  int32_t retrieve_in_select;// 1: the select/manage kernel copies each unit's misses; the attend kernel only reads HBM
-  int32_t select_group;      // 0 = choose by unit size, else 32 or 512 threads for top-k + manager
+  int32_t mgr_gs;            // threads of one manager group (32, 128, or the CTA's full group)
   const int32_t* P_b;        // [B] selectable partitions of request b in this layer (tail mode: complete ones)
   const int32_t* ntok_b;     // [B] tokens held by those partitions
   const int32_t* tail_n;     // [B] tokens in the request's tail page (tail mode), else nullptr
@@ -68,12 +67,18 @@ struct LayerArgs {
   int32_t* miss_att;         // [U_l * k] ul * ka + attention position of each miss
   int32_t* miss_valid;       // [U_l * k] valid tokens of each miss's page
   int32_t* ready;            // [U_l * k] per miss-list entry: step tag once its page is in HBM
+  int32_t* miss_tag;         // [U_l * k] per miss-list entry: step tag once the entry is written
+  int32_t* unit_rows;        // [U_l] partitions scored so far in this step (reset by the unit's manager)
+  int32_t* unit_ready;       // [U_l] step tag once the unit is managed
+  int32_t* hist12;           // [U_l][4096] wide units only (else nullptr): count of keys per top-12-bit value,
+                             // filled while scoring, cleared by the unit's manager
   int32_t* att_slot;         // [U_l][ka] slots in attention order: hits, the tail (slot == cap), then misses
   int32_t* att_valid;        // [U_l][ka] valid tokens of those pages
   int32_t* n_hit;            // [U_l] resident pages of the step, tail included (pages [0, n_hit) of att_slot)
-  int32_t* counters;         // [4]: see kCtr*
+  int32_t* counters;         // [kNumCtr]: see kCtr*
   float* partials;           // hits [U_l][n_chunks][G][132], then misses [U_l][ka][G][132]
   unsigned long long* stats; // [8] device counters
+  unsigned long long* timeline; // [5] globaltimer stamps of this call (stage timing), else nullptr
   uint32_t* err;             // device error word
   const uint16_t* q;         // [B][Hq][128] bf16 (device)
   float* out;                // [B][Hq][128] fp32 (device)
@@ -87,10 +92,21 @@ __device__ inline int64_t host_page_index(const LayerArgs& a, int b, int h, int6
 
 // Per-layer device counters.
 enum : int {
-  kCtrMiss = 0, kCtrTaskHits = 1, kCtrTaskMisses = 2, kCtrStep = 3, kCtrRetrieve = 4,
-  kCtrArrive = 5,  // CTAs of the attend kernel done with their pages (grows by grid size every step)
+  kCtrMiss = 0,      // miss-list entries allocated in this step
+  kCtrTaskHits = 1,  // resident-page tasks claimed
+  kCtrTaskMisses = 2,// retrieved pages claimed by producers
+  kCtrStep = 3,      // the layer's step t
+  kCtrRetrieve = 4,  // miss-list entries claimed by retrievers
+  kCtrArrive = 5,    // CTAs done with their pages (grows by the grid size every step)
+  kCtrManage = 6,    // units claimed by manager groups
+  kCtrManaged = 7,   // units managed and published
   kNumCtr = 8
 };
+
+// Stage stamps of one timed decode-step call (globaltimer ns): first CTA start (stored
+// inverted, so that atomicMax keeps the minimum), last CTA done scoring, last unit
+// managed, last CTA done with its pages, last combine done.
+enum : int { kTlStart = 0, kTlScored = 1, kTlManaged = 2, kTlPages = 3, kTlEnd = 4, kTlSlots = 8 };
 
 // Device stats slots.
 enum : int {
@@ -108,7 +124,6 @@ cudaError_t launch_gather_offload(const uint16_t* k, const uint16_t* v, int64_t 
                                   uint16_t* host_unit0, int64_t unit_pages, uint8_t* valid_unit0, cudaStream_t st);
 cudaError_t launch_warm_store(const void* store, int64_t bytes, int64_t stride, uint32_t* sink, int sm_count,
                               cudaStream_t st);
-cudaError_t launch_score(const LayerArgs& a, cudaStream_t st);
 // KV append of one token per request of the layer (tail mode).
 cudaError_t launch_append(const LayerArgs& a, const uint16_t* k_new, const uint16_t* v_new, int32_t* P_b,
                           int32_t* ntok_b, int32_t* tail_n, cudaStream_t st);
@@ -117,13 +132,14 @@ cudaError_t launch_set_int(int32_t* p, int32_t v, cudaStream_t st);
 // Sets the request's layer state (partitions, their tokens, tail tokens) on the device.
 cudaError_t launch_set_request(int32_t* P_b, int32_t* ntok_b, int32_t* tail_n, int32_t P, int32_t ntok,
                                int32_t tail, cudaStream_t st);
-cudaError_t launch_select_manage(const LayerArgs& a, cudaStream_t st);
-// Retrieve + attention in one cooperative persistent launch (one CTA per SM).
-cudaError_t launch_attend_retrieve(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st);
+// The whole decode step of one layer in one cooperative persistent launch (one CTA per SM).
+cudaError_t launch_decode_step(const LayerArgs& a, const CUtensorMap* tmap, int grid, cudaStream_t st);
+cudaError_t step_configure(const LayerArgs& a);
+size_t step_smem_bytes(const LayerArgs& a);   // dynamic shared memory of that launch
+size_t step_ring_bytes();                     // the ring of phase C (the manager groups share its bytes)
+size_t mgr_group_bytes(int gs, const LayerArgs& a);  // shared memory of one manager group of gs threads
+int step_threads(int G);                      // threads per CTA
+int step_full_group(int G);                   // the largest manager group (all warps of a CTA's roles)
 cudaError_t launch_resolve_all(const LayerArgs& a, int32_t* resolve, int32_t* live_segs, cudaStream_t st);
-size_t select_manage_smem_bytes(const LayerArgs& a);
-size_t attention_smem_bytes();
-cudaError_t attention_configure();
-cudaError_t select_manage_configure(size_t smem);
 
 }  // namespace spin

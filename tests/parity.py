@@ -316,3 +316,147 @@ def sample_units(w: W.Workload, n: int, seed: int = 0) -> List[Tuple[int, int, i
     allu = [(l, b, h) for l in range(w.L) for b in range(w.B) for h in range(w.Hkv)]
     idx = rng.choice(len(allu), size=min(n, len(allu)), replace=False)
     return sorted(allu[i] for i in idx)
+
+
+class AllUnits:
+    """Every unit of a fixed-partition workload, GPU against the oracle every step.
+
+    The oracle side runs all units of a step with its thread pool (step_units_full).
+    Per step and layer: selections are checked against the oracle's top-k with the
+    tie band; for every unit whose selections have always matched exactly, slots,
+    hits, the manager record, slot map, timestamps, the resolved two-level table and
+    live segments are compared bit for bit (vectorised over the layer) and outputs
+    within OUT_TOL. A unit that diverged inside the tie band is checked for validity
+    (invariants) and its output against the oracle's attention over the GPU's set.
+    """
+
+    def __init__(self, w: W.Workload, device: int = 0, flags: int = 0, gen_threads: int = 0, threads: int = 0):
+        import torch
+        from sparse_attention_tiered_gb300 import SpinContext
+        assert not getattr(w, "mean_part", 0), "fixed partitions only"
+        self.torch = torch
+        self.w = w
+        self.threads = threads
+        self.dev = torch.device(f"cuda:{device}")
+        self.ctx = SpinContext.for_workload(w, device=device, flags=flags)
+        self.units: List[O.Unit] = []
+        self.keys: List[Tuple[int, int, int]] = []
+        for l in range(w.L):
+            for b in range(w.B):
+                k, v = w.request_kv(l, b, threads=gen_threads)
+                self.ctx.index_offload_host(b, l, k, v)
+                torch.cuda.synchronize()  # the host arrays are reused/freed next
+                for h in range(w.Hkv):
+                    self.units.append(O.Unit(w.ctx_len[b], w.cap, np.ascontiguousarray(k[h]),
+                                             np.ascontiguousarray(v[h])))
+                    self.keys.append((l, b, h))
+                del k, v
+        self.Ul = w.B * w.Hkv
+        self.diverged = np.zeros(len(self.units), bool)
+        self.qs = w.queries()
+        self.t = 0
+        self.out = torch.empty((w.L, w.B, w.Hq, 128), dtype=torch.float32, device=self.dev)
+        self.report = Report()
+        self.exact_unit_steps = 0
+
+    def close(self):
+        self.ctx.close()
+        self.units = []
+
+    def step(self):
+        torch, w, t = self.torch, self.w, self.t
+        qb = self.qs.bf16()
+        qd = torch.from_numpy(qb.view(np.int16)).to(self.dev)
+        for l in range(w.L):
+            self.ctx.decode_step(l, qd[l], self.out[l])
+        qlist = [np.ascontiguousarray(qb[l, b, h * w.G:(h + 1) * w.G]) for (l, b, h) in self.keys]
+        res = O.step_units_full(self.units, qlist, w.topk, t, threads=self.threads)
+        torch.cuda.synchronize()
+        out = self.out.cpu().numpy()
+        for l in range(w.L):
+            self._check_layer(l, qb, out, res[l * self.Ul:(l + 1) * self.Ul])
+        self.report.steps += 1
+        self.qs.advance()
+        self.t += 1
+
+    def _check_layer(self, l, qb, out, res):
+        w, t, rep = self.w, self.t, self.report
+        ex = self.ctx.export(l, resolve=True)
+        U, cap, Pm = self.Ul, w.cap, self.ctx.P_max
+        base = l * U
+        sp_o = np.empty((U, cap), np.int32)
+        lu_o = np.empty((U, cap), np.int32)
+        rs_o = np.full((U, max(Pm, 1)), -1, np.int32)
+        live_o = np.empty(U, np.int32)
+        out_o = np.empty((U, w.G, 128), np.float64)
+        exact = np.zeros(U, bool)
+        for ul in range(U):
+            i = base + ul
+            u, r = self.units[i], res[ul]
+            b, h = ul // w.Hkv, ul % w.Hkv
+            where = f"step {t} unit {(l, b, h)}"
+            rep.compared_units += 1
+            keff = int(ex["keff"][ul])
+            sel_g = ex["sel"][ul][:keff]
+            if u.P == 0:
+                assert keff == 0 and np.all(out[l, b, h * w.G:(h + 1) * w.G] == 0), f"{where}: empty request"
+                exact[ul] = not self.diverged[i]
+                sp_o[ul], lu_o[ul], _ = u.export()
+                live_o[ul] = u.live_segments()
+                out_o[ul] = 0.0
+                continue
+            same = check_selection(r["scores"], r["sel"], sel_g, where)
+            if same and not self.diverged[i]:
+                exact[ul] = True
+                sp, lu, rs = u.export()
+                sp_o[ul], lu_o[ul] = sp, lu
+                rs_o[ul, :u.P] = rs
+                live_o[ul] = u.live_segments()
+                out_o[ul] = r["out"]
+                mo = r["mo"]
+                assert r["mo"].error == 0, f"{where}: oracle page pool error"
+                info = ex["unit_info"][ul]
+                if (info[0], info[1], info[2], info[3], info[4], info[5]) != (
+                        mo.hits, mo.misses, mo.resident_before, mo.demand, mo.cutoff, mo.evicted):
+                    raise AssertionError(f"{where}: manager record differs: gpu {info[:6].tolist()} oracle "
+                                         f"{[mo.hits, mo.misses, mo.resident_before, mo.demand, mo.cutoff, mo.evicted]}")
+                assert np.array_equal(ex["sel_slot"][ul][:keff], r["sel_slot"]), f"{where}: slots differ"
+                assert np.array_equal(ex["sel_hit"][ul][:keff].astype(bool), r["sel_hit"]), f"{where}: hits differ"
+                rep.evictions += mo.evicted
+                rep.misses += mo.misses
+                rep.hits += mo.hits
+            else:
+                if not self.diverged[i]:
+                    self.diverged[i] = True
+                    rep.tie_divergences += 1
+                    rep.notes.append(f"{where}: tie-band divergence")
+                check_invariants(ex, ul, u.P, t, where)
+                match = None
+                for cand in valid_sets(r["scores"], r["sel"]):
+                    if np.array_equal(cand, sel_g):
+                        match = cand
+                        break
+                assert match is not None, f"{where}: GPU set is not one of the valid tie-band sets"
+                fresh = u.clone_empty(max(w.topk, 1))
+                ss, _, _, _ = fresh.manage(match, 0)
+                q = np.ascontiguousarray(qb[l, b, h * w.G:(h + 1) * w.G])
+                o_div = fresh.attend(match, ss, q)
+                err = float(np.abs(out[l, b, h * w.G:(h + 1) * w.G] - o_div).max())
+                rep.max_out_err = max(rep.max_out_err, err)
+                assert err <= OUT_TOL, f"{where}: output max-abs error {err} > {OUT_TOL}"
+        # bit-exact page state and outputs of every exact unit, vectorised over the layer
+        idx = np.nonzero(exact)[0]
+        self.exact_unit_steps += len(idx)
+        rep.exact_units += len(idx)
+        if len(idx):
+            for name, g_arr, o_arr in (("slot map", ex["slot_part"], sp_o), ("timestamps", ex["last_use"], lu_o),
+                                       ("page table", ex["resolve"][:, :max(Pm, 1)], rs_o),
+                                       ("live segments", ex["live_segs"], live_o)):
+                bad = np.nonzero(np.any((g_arr[idx] != o_arr[idx]).reshape(len(idx), -1), axis=1))[0]
+                if len(bad):
+                    ul = int(idx[bad[0]])
+                    raise AssertionError(f"step {t} unit {(l, ul // w.Hkv, ul % w.Hkv)}: {name} differs")
+            g_out = out[l].reshape(w.B, w.Hkv, w.G, 128).reshape(U, w.G, 128)
+            err = float(np.abs(g_out[idx] - out_o[idx]).max())
+            rep.max_out_err = max(rep.max_out_err, err)
+            assert err <= OUT_TOL, f"step {t} layer {l}: output max-abs error {err} > {OUT_TOL}"
