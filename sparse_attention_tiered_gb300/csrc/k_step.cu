@@ -121,7 +121,7 @@ __host__ __device__ inline void step_smem_layout(StepSmem* s, uint8_t* base) {
   s->hits_groups = (int*)take(sizeof(int), 4);
   s->region = base + kHeaderBytes;
 }
-static_assert(sizeof(uint64_t) * (2 * kStages + 2 * kMaxGroups) + 16 * (kStages + 1) + 16 <= kHeaderBytes,
+static_assert(sizeof(uint64_t) * (2 * kStages + 2 * kMaxGroups) + sizeof(StageMeta) * kStages + 64 <= kHeaderBytes,
               "header overflow");
 
 // ---------------------------------------------------------------------------
@@ -298,11 +298,11 @@ __device__ __forceinline__ uint32_t swz(int r, int cd) {
 // ---------------------------------------------------------------------------
 // Combine of one (unit, query head): out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c
 // over the unit's partials (its hit tasks and its retrieved pages), by one warp, four
-// columns per lane. The lanes fetch the (m, l) of up to 32 partials at once; the
-// accumulator rows are loaded eight at a time before they are used, so a head costs
-// a few round trips to L2 whatever the number of partials.
+// columns per lane, in one online pass: 16 partials at a time, their (m, l) and
+// accumulator rows all loaded before use, folded into a running maximum.
 // ---------------------------------------------------------------------------
 __device__ void combine_head(const LayerArgs& a, int ul, int g, int lane) {
+  constexpr int kBatch = 16;
   const int b = ul / a.Hkv, h = ul - b * a.Hkv;
   const int has_tail = (a.tail_n != nullptr && a.tail_n[b] > 0) ? 1 : 0;
   const int keff = __ldcg(a.keff + ul) + has_tail, nh = __ldcg(a.n_hit + ul);  // attended; resident (tail incl.)
@@ -316,47 +316,48 @@ __device__ void combine_head(const LayerArgs& a, int ul, int g, int lane) {
         i < nc ? (int64_t)ul * a.n_chunks + i : (int64_t)U * a.n_chunks + (int64_t)ul * a.ka + nh + (i - nc);
     return a.partials + (slot * a.G + g) * kPartialStride;
   };
-  float M = -INFINITY;
-  for (int i0 = 0; i0 < n; i0 += 32)
-    if (i0 + lane < n) M = fmaxf(M, __ldcg(part_ptr(i0 + lane)));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int i0 = 0; i0 < n; i0 += 32) {
-      float sc_l = 0.f, l_l = 0.f;
-      if (i0 + lane < n) {
-        const float* pp = part_ptr(i0 + lane);
-        sc_l = exp2f(__ldcg(pp) - M);
-        l_l = __ldcg(pp + 1);
-      }
-      float ls = sc_l * l_l;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-      L += ls;
-      const int cnt = min(32, n - i0);
-      for (int i1 = 0; i1 < cnt; i1 += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          v[u] = (i1 + u < cnt) ? __ldcg(reinterpret_cast<const float4*>(part_ptr(i0 + i1 + u) + 4) + lane)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float sc = __shfl_sync(0xffffffffu, sc_l, (i1 + u) & 31);  // 0 past cnt: its v is 0 too
-          acc.x = fmaf(sc, v[u].x, acc.x);
-          acc.y = fmaf(sc, v[u].y, acc.y);
-          acc.z = fmaf(sc, v[u].z, acc.z);
-          acc.w = fmaf(sc, v[u].w, acc.w);
-        }
-      }
+  for (int i0 = 0; i0 < n; i0 += kBatch) {
+    float m_l = -INFINITY, l_l = 0.f;  // lane u < kBatch: partial i0 + u
+    if (lane < kBatch && i0 + lane < n) {
+      const float* pp = part_ptr(i0 + lane);
+      m_l = __ldcg(pp);
+      l_l = __ldcg(pp + 1);
     }
+    float4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      v[u] = (i0 + u < n) ? __ldcg(reinterpret_cast<const float4*>(part_ptr(i0 + u) + 4) + lane)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    float Mc = m_l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, o));
+    const float Mn = fmaxf(M, Mc);
+    if (Mn == -INFINITY) continue;  // nothing attended so far
+    const float al = exp2f(M - Mn);  // M = -inf gives 0
+    const float sc_l = exp2f(m_l - Mn);  // lanes without a partial: m = -inf gives 0
+    float ls = sc_l * l_l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    L = fmaf(L, al, ls);
+    acc.x *= al;
+    acc.y *= al;
+    acc.z *= al;
+    acc.w *= al;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const float sc = __shfl_sync(0xffffffffu, sc_l, u);
+      acc.x = fmaf(sc, v[u].x, acc.x);
+      acc.y = fmaf(sc, v[u].y, acc.y);
+      acc.z = fmaf(sc, v[u].z, acc.z);
+      acc.w = fmaf(sc, v[u].w, acc.w);
+    }
+    M = Mn;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   out[lane] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
-
 
 // Combine of one (unit, query head) by the nw consumer warps of a CTA (named barrier
 // `bar`), for units with many partials: warp w folds partials w, w + nw, ... (their loads
@@ -606,9 +607,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
             // publish the unit with nothing selected, so nobody waits for it
             a.keff[ul] = 0;
             a.n_hit[ul] = 0;
-            __threadfence();
-            st_release(a.unit_ready + ul, tag);
-            atomicAdd(&a.counters[kCtrManaged], 1);
+            sel::publish_unit(a, ul, tag);
           }
           continue;
         }
@@ -1064,7 +1063,6 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       if (lane == 0) mbar_arrive(smem_u32(&sm.empty[st]));  // the group's four warps free the stage
       i += NG;
     }
-
   }
 
   // ---------------- all pages of all CTAs done: combine the partials ----------------
@@ -1073,7 +1071,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
   // counter reset below cannot race with a late claim of this step.
   __syncthreads();
   if (tid == 0) {
-    if (tl) atomicMax(tl + 3, globaltimer_ns());
+    if (tl) atomicMax(tl + kTlPages, globaltimer_ns());
     __threadfence();
     atomicAdd(&a.counters[kCtrArrive], 1);
     const int target = (int)gridDim.x * tag;  // the counter grows by gridDim.x every step
@@ -1102,7 +1100,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     // (unit, head) pairs spread over every consumer warp of the grid
     for (int p = blockIdx.x * NC + warp; p < pairs; p += gridDim.x * NC) combine_head(a, p / a.G, p % a.G, lane);
   }
-  if (tl && lane == 0) atomicMax(tl + 4, globaltimer_ns());
+  if (tl && lane == 0) atomicMax(tl + kTlEnd, globaltimer_ns());
 }
 
 // ---------------------------------------------------------------------------

@@ -631,6 +631,14 @@ __device__ __forceinline__ void st_release_i32(int32_t* p, int32_t v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Publishes unit ul (by one thread, after the group's writes): its ready flag, then the
+// managed count.
+__device__ inline void publish_unit(const LayerArgs& a, int ul, int tag) {
+  __threadfence();
+  st_release_i32(a.unit_ready + ul, tag);
+  atomicAdd(&a.counters[kCtrManaged], 1);
+}
+
 // Select + manage unit ul of the layer at step t, once its scores are all in a.scores.
 // Writes the selection, slots, attention order, page state, two-level table, stats and
 // this step's miss-list entries (each published with its tag in miss_tag), then
@@ -717,11 +725,7 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
       a.keff[ul] = 0;
     }
     gsync<NT>(bar);
-    if (gt == 0) {
-      __threadfence();
-      st_release_i32(a.unit_ready + ul, tag);
-      atomicAdd(&a.counters[kCtrManaged], 1);
-    }
+    if (gt == 0) publish_unit(a, ul, tag);
     return;
   }
 
@@ -988,11 +992,7 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
     if (keff) atomicAdd(&a.stats[kStatSelected], (unsigned long long)keff);
   }
   gsync<NT>(bar);
-  if (gt == 0) {
-    __threadfence();
-    st_release_i32(a.unit_ready + ul, tag);
-    atomicAdd(&a.counters[kCtrManaged], 1);
-  }
+  if (gt == 0) publish_unit(a, ul, tag);
   (void)kW;
 }
 
