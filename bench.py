@@ -106,10 +106,91 @@ class Ranks:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
+    def sum(self, x: float) -> float:
+        if self.world == 1:
+            return float(x)
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.dev if self.dev is not None else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    def min(self, x: float) -> float:
+        return -self.max(-x)
+
+    def check_host_memory(self, need_bytes: int, avail_bytes=None, headroom: float = 0.9):
+        """Every rank of the node pins its own host page store: the ranks' stores together
+        must fit in the node's available memory (MemAvailable, less a margin). The decision
+        is the same on every rank; when it fails every rank exits with the figures."""
+        avail = float(avail_bytes if avail_bytes is not None else mem_available_bytes())
+        need_total = self.sum(need_bytes)
+        avail = self.min(avail)
+        if need_total > headroom * avail:
+            raise SystemExit(f"host memory: {self.world} rank(s) would pin {need_total / 2**30:.1f} GiB of page stores "
+                             f"but the node has {avail / 2**30:.1f} GiB available ({headroom:.0%} usable); "
+                             f"use fewer GPUs per node or a smaller workload")
+        return need_total, avail
+
     def close(self):
         if self.world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
+
+
+def mem_available_bytes(meminfo: str = "/proc/meminfo") -> int:
+    """MemAvailable of the host in bytes (0 when unknown)."""
+    try:
+        with open(meminfo) as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def parse_cpulist(text: str):
+    """CPUs of a sysfs cpulist ("0-15,32-47")."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        else:
+            cpus.add(int(part))
+    return cpus
+
+
+def gpu_local_cpus(pci_bus_id: str, sysfs: str = "/sys"):
+    """CPUs local to a GPU (its PCI device's local_cpulist), or None when unknown."""
+    try:
+        with open(os.path.join(sysfs, "bus", "pci", "devices", pci_bus_id.lower(), "local_cpulist")) as f:
+            cpus = parse_cpulist(f.read())
+        return cpus or None
+    except (OSError, ValueError):
+        return None
+
+
+def bind_near_gpu(dev_index: int):
+    """Keeps this rank's threads on the CPUs local to its GPU, so the pinned host page store,
+    first touched by the allocating thread, lands in that CPU's memory (one NUMA node per
+    Grace). Returns the CPUs, or None when the topology is not exposed."""
+    import torch
+    props = torch.cuda.get_device_properties(dev_index)
+    bus = getattr(props, "pci_bus_id", None)
+    dom = getattr(props, "pci_domain_id", 0)
+    dv = getattr(props, "pci_device_id", None)
+    if bus is None or dv is None:
+        return None
+    cpus = gpu_local_cpus(f"{dom:08x}:{bus:02x}:{dv:02x}.0")
+    if cpus:
+        try:
+            os.sched_setaffinity(0, cpus & os.sched_getaffinity(0) or cpus)
+        except OSError:
+            return None
+    return cpus
 
 
 def job_tokens_per_s(tokens_per_rank: int, world: int, max_ms: float) -> float:
@@ -473,7 +554,11 @@ def bench_spin(args):
 
     w = make_workload(args, rank)
     K, Wm = args.steps, max(3, args.warmup)
-    n_steps_total = Wm + K + (0 if args.no_e2e else K)
+    n_steps_total = Wm + K
+    if world > 1:
+        bind_near_gpu(local)
+    # every rank pins its own page store (plus the step queries): they must fit together
+    R.check_host_memory(w.host_kv_bytes() + n_steps_total * w.L * w.B * w.Hq * 128 * 2)
     if args.append and w.mean_part:
         raise SystemExit("--append and --mean-part cannot be combined (tail mode has fixed partitions)")
     if args.budget and not (w.topk <= args.budget <= w.cap):
@@ -499,7 +584,7 @@ def bench_spin(args):
         gen = torch.Generator().manual_seed(1000 + rank)
         kv_host = torch.randn((n_steps_total, w.L, 2, w.B, w.Hkv, 128), generator=gen).to(torch.bfloat16)
         kv_host = kv_host.view(torch.int16).pin_memory()
-        kv_dev = kv_host[:Wm + K].to(dev)
+        kv_dev = kv_host.to(dev)
         kv_stage = torch.empty((2, w.B, w.Hkv, 128), dtype=torch.int16, device=dev)
 
     # ---- queries for every step, resident in HBM (and pinned on the host for e2e) ----
@@ -508,7 +593,7 @@ def bench_spin(args):
     for t in range(n_steps_total):
         q_host[t].copy_(torch.from_numpy(qs.bf16().view(np.int16)))
         qs.advance()
-    q_dev = q_host[:Wm + K].to(dev)
+    q_dev = q_host.to(dev)
     out = torch.empty((w.L, w.B, w.Hq, 128), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
 
@@ -552,14 +637,24 @@ def bench_spin(args):
     traffic = attention_traffic(hbm_b)
     gpu_launches = K * w.L * (1 + (1 if args.append else 0))
 
-    # ---- end to end through the host-buffer entry point ----
+    st2 = ctx.stats()
+    ctx.close()
+    # ---- end to end through the host-buffer entry point: a fresh context, the same warm-up
+    # and the same timed step range, with q read from and out written to pinned host memory ----
     e2e = None
     if not args.no_e2e:
+        ctx = make_context(w, args, local, SPIN_FLAG_TIER_SPLIT if args.tier_split else 0,
+                           append_tokens=n_steps_total if args.append else 0, rank=rank)
+        if args.budget:
+            for b in range(w.B):
+                ctx.set_buffer(b, args.budget)
+        for t in range(Wm):
+            step(t)
         o_host = torch.empty((w.L, w.B, w.Hq, 128), dtype=torch.float32).pin_memory()
         barrier()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record()
-        for t in range(Wm + K, Wm + 2 * K):
+        for t in range(Wm, Wm + K):
             for l in range(w.L):
                 if args.append:  # the new token's K and V come from host memory too
                     kv_stage.copy_(kv_host[t, l], non_blocking=True)
@@ -570,9 +665,9 @@ def bench_spin(args):
         ms_e2e = R.max(a0.elapsed_time(a1))
         e2e = {"value": job_tokens_per_s(w.B * K, world, ms_e2e), "unit": "tokens/s",
                "h2d_bytes_per_step": int(q_host[0].numel() * 2 + (kv_host[0].numel() * 2 if args.append else 0)),
-               "d2h_bytes_per_step": int(o_host.numel() * 4)}
-    st2 = ctx.stats()
-    ctx.close()
+               "d2h_bytes_per_step": int(o_host.numel() * 4),
+               "timed_steps": f"{Wm}..{Wm + K - 1} on a fresh context after the same {Wm} warm-up steps"}
+        ctx.close()
     del q_dev, q_host, out
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

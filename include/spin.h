@@ -114,6 +114,12 @@ typedef struct spin_config {
                                 spin_index_offload_parts groups them; spin_index_offload is then refused.
                                 Needs append_tokens == 0, max_partitions <= 2^20 and
                                 ceil(ctx_len[b] / 64) <= max_partitions for every request. */
+  int64_t max_context;       /* the logical context capacity of a request in tokens ([XT] §3: a flat table is
+                                sized for the worst-case logical space, max batch x max context x layers x
+                                heads, where the two-level table grows with the resident pages). 0 = the
+                                longest ctx_len[b] + append_tokens. Sizes the static first level (the
+                                directory) and the flat table spin_stats reports for comparison; must be >=
+                                every ctx_len[b] + append_tokens and <= 2^21. */
 } spin_config;
 
 /* Counters since spin_create. */
@@ -129,7 +135,9 @@ typedef struct spin_stats_t {
   int64_t pool_segments;     /* segments in the shared pool */
   int64_t metadata_bytes;    /* HBM bytes of the page metadata: directory + segment pool (unless tier
                                 split) + live counts + bitmap + per-page state */
-  int64_t flat_table_bytes;  /* HBM bytes of a flat [unit][max partitions] table plus the same per-page state */
+  int64_t flat_table_bytes;  /* HBM bytes of the flat table of the worst-case logical space ([XT] §3): one
+                                int32 entry per (request, layer, KV head, partition of max_context), plus the
+                                same per-page state */
   int64_t hbm_pool_bytes;    /* HBM page pool */
   int64_t host_store_bytes;  /* pinned host page store */
   int64_t summary_bytes;     /* HBM partition summaries (fp32) */
@@ -246,10 +254,11 @@ int spin_set_buffer(spin_ctx* ctx, int32_t b, int32_t pages, spin_stream_t strea
 int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream);
 
 /* The same step with host buffers: q_host [batch][q_heads][128] bf16 and
- * out_host [batch][q_heads][128] fp32 (pinned for asynchronous copies). The
- * host->device copy of q, the step and the device->host copy of out are all
- * enqueued on `stream`; out_host is valid once the stream has reached that point,
- * and neither buffer may be reused before then. */
+ * out_host [batch][q_heads][128] fp32. Pinned, device-mapped buffers (cudaHostAlloc'd or
+ * registered) are used in place: the kernel reads q_host (8-byte aligned) and writes
+ * out_host (16-byte aligned) over the host link. Other buffers go through HBM with
+ * host<->device copies enqueued on `stream` around the step. out_host is valid once the
+ * stream has reached the end of the step, and neither buffer may be reused before then. */
 int spin_decode_step_host(spin_ctx* ctx, int32_t layer, const uint16_t* q_host, float* out_host,
                           spin_stream_t stream);
 

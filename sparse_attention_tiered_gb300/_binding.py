@@ -64,6 +64,7 @@ class spin_config(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("append_tokens", ctypes.c_int32),
         ("max_partitions", ctypes.c_int32),
+        ("max_context", ctypes.c_int64),
     ]
 
 

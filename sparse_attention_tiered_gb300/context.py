@@ -22,7 +22,7 @@ class SpinContext:
 
     def __init__(self, batch: int, layers: int, q_heads: int, kv_heads: int, ctx_len: Sequence[int], topk: int,
                  buf_mult: int, device: int = 0, seg_pool_segments: int = 0, flags: int = 0,
-                 append_tokens: int = 0, max_partitions: int = 0):
+                 append_tokens: int = 0, max_partitions: int = 0, max_context: int = 0):
         self.B, self.L, self.Hq, self.Hkv = batch, layers, q_heads, kv_heads
         self.G = q_heads // kv_heads
         self.ctx_len = [int(x) for x in ctx_len]
@@ -53,7 +53,7 @@ class SpinContext:
         self._ctx_arr = (ctypes.c_int64 * batch)(*self.ctx_len)
         cfg = B.spin_config(batch, layers, q_heads, kv_heads, B.HEAD_DIM, B.PART_TOKENS, topk, buf_mult,
                             self._ctx_arr, 0, seg_pool_segments, device, flags, self.append_tokens,
-                            self.max_partitions)
+                            self.max_partitions, int(max_context))
         self.h = B.spin_create(cfg)
 
     @classmethod
@@ -61,6 +61,8 @@ class SpinContext:
         """A context for a workload; variable partitions when the workload has mean_part > 0."""
         if getattr(w, "mean_part", 0) and "max_partitions" not in kw:
             kw["max_partitions"] = w.max_partitions
+        if getattr(w, "max_context", 0) and "max_context" not in kw:
+            kw["max_context"] = w.max_context
         return cls(w.B, w.L, w.Hq, w.Hkv, w.ctx_len, w.topk, w.buf_mult, device=device, **kw)
 
     def close(self):

@@ -525,7 +525,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       int n = (int)min((int64_t)min(sel::kRowsPerBatch, Pb - p), r_end - r);
       float4 cur[sel::kRowsPerBatch], nxt[sel::kRowsPerBatch];
       sel::load_rows(cur, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, p) * kD), n, lane);
-      float4 qv = sel::qsum_lane(a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
+      float4 qv = sel::qsum_lane(a.q_src + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
       int counted = 0;
       for (;;) {
         // the next batch: the rest of this unit, else the start of the next non-empty unit
@@ -559,7 +559,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
           counted = 0;
         }
         if (!more) break;
-        if (leave) qv = sel::qsum_lane(a.q + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
+        if (leave) qv = sel::qsum_lane(a.q_src + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
         r = r2;
         b = b2;
         h = h2;
@@ -708,6 +708,9 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       if (r <= 0) return false;
       __syncwarp();
       (void)ld_acquire(a.unit_ready + tu);
+      // the unit's query rows may have been staged with generic stores in this kernel: the
+      // TMA bulk copy that reads them follows a proxy fence
+      if (lane == 0 && a.q_src != a.q) asm volatile("fence.proxy.async.global;" ::: "memory");
       nhit = __ldcg(a.n_hit + tu);
       const bool in = lane < a.ppt && j0 + lane < a.ka;
       slot = in ? __ldcg(a.att_slot + (int64_t)tu * a.ka + j0 + lane) : 0;

@@ -657,6 +657,14 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
   const int64_t unit = a.unit_base + ul;
   const bool dead = (*((volatile uint32_t*)a.err) & (kErrCapacity | kErrInternal | kErrSelCount | kErrSegId | kErrIndex)) != 0;
   bool ok = !dead;
+  if (a.q_src != a.q) {
+    // queries read from host memory: the unit's G rows go to HBM for the attention's TMA
+    // loads (published with the unit)
+    const int64_t q0 = ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD;
+    const uint2* src = reinterpret_cast<const uint2*>(a.q_src + q0);
+    uint2* dst = reinterpret_cast<uint2*>(const_cast<uint16_t*>(a.q) + q0);
+    for (int i = gt; i < a.G * (kD / 4); i += NT) dst[i] = src[i];
+  }
   if (dead && a.hist12)
     for (int i = gt; i < kHistBins; i += NT) a.hist12[(int64_t)ul * kHistBins + i] = 0;
 

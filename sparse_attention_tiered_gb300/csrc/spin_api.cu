@@ -154,6 +154,7 @@ struct spin_ctx {
   double ms[kNumStages] = {0, 0, 0, 0, 0};
   int64_t timed_calls = 0;
   int64_t bytes_meta = 0, bytes_flat = 0, bytes_pool = 0, bytes_store = 0, bytes_summ = 0;
+  int64_t P_logical = 0;  // partitions per unit of the logical capacity (max_context)
 };
 
 namespace {
@@ -357,6 +358,12 @@ int validate(const spin_config* cfg) {
                     (long long)cfg->ctx_len[b], cfg->max_partitions);
   }
   if (cfg->seg_pool_segments < 0) return fail(nullptr, SPIN_ERR_INVALID, "seg_pool_segments must be >= 0");
+  if (cfg->max_context < 0 || cfg->max_context > (int64_t)32768 * kPart)
+    return fail(nullptr, SPIN_ERR_INVALID, "max_context must be in [0, %d]", 32768 * kPart);
+  for (int b = 0; cfg->max_context > 0 && b < cfg->batch; ++b)
+    if (cfg->ctx_len[b] + cfg->append_tokens > cfg->max_context)
+      return fail(nullptr, SPIN_ERR_INVALID, "ctx_len[%d] + append_tokens = %lld exceeds max_context = %lld", b,
+                  (long long)(cfg->ctx_len[b] + cfg->append_tokens), (long long)cfg->max_context);
   const int64_t units = (int64_t)cfg->batch * cfg->layers * cfg->kv_heads;
   if (units * ((int64_t)cfg->buf_mult * cfg->topk + 1) >= (int64_t)1 << 24)
     return fail(nullptr, SPIN_ERR_INVALID, "units * (capacity + 1) must stay below 2^24 pages");
@@ -468,7 +475,10 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   c->tail_lb.assign((size_t)c->L * c->B, 0);
   for (int l = 0; l < c->L && !c->tail_mode && !c->part_mode; ++l)
     for (int b = 0; b < c->B; ++b) c->P_lb[(size_t)l * c->B + b] = c->P_b[b];
-  c->D = std::max(1, (c->P_max + kSeg - 1) / kSeg);
+  // the logical capacity in partitions per unit: the static directory covers it, and the flat
+  // worst-case table spin_stats reports is sized for it
+  c->P_logical = std::max<int64_t>(c->P_max, (cfg->max_context + kPart - 1) / kPart);
+  c->D = (int)std::max<int64_t>(1, (c->P_logical + kSeg - 1) / kSeg);
   c->pages_per_layer = poff * c->Hkv;
   c->units = (int64_t)c->B * c->L * c->Hkv;
   c->S = cfg->seg_pool_segments > 0 ? cfg->seg_pool_segments : std::max<int64_t>(auto_S, 1);
@@ -555,7 +565,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   ALLOC(c->d_err, 1, "allocating counters");
   ALLOC(c->d_warm_sink, 1, "allocating counters");
   c->bytes_meta = (c->units * c->D + (c->h_seg ? 0 : c->S * kSeg) + c->S + nwords + 2 * slots) * 4;
-  c->bytes_flat = (c->units * (int64_t)c->P_max + 2 * slots) * 4;
+  c->bytes_flat = (c->units * c->P_logical + 2 * slots) * 4;
 
   {
     // fixed mode: every layer holds the request's partitions; tail mode and variable
@@ -697,10 +707,13 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
 
 // Enqueue one layer's step on `st`: one cooperative kernel (score -> select + manage ->
 // retrieve + attention -> combine).
-int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStream_t st) {
+// q: the queries in HBM the attention stages; q_src: the queries the scores read (q, or a
+// device-usable address of pinned host memory whose rows the unit managers copy into q).
+int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, const uint16_t* q_src, float* out, cudaStream_t st) {
   LayerBuf& lb = c->layers[layer];
   LayerArgs a = lb.args;
   a.q = q;
+  a.q_src = q_src;
   a.out = out;
   // stage timing: CUDA events around the kernel and a record of in-kernel stage stamps
   // (up to kTimelineCalls timed calls between two synchronising calls)
@@ -729,6 +742,20 @@ int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, float* out, cudaStre
   }
   c->steps_host += 1;
   return SPIN_OK;
+}
+
+// The device-usable address of pinned, device-mapped host memory at p when it is
+// `align`-byte aligned; nullptr for pageable or unaligned memory.
+const void* mapped_host(const void* p, uintptr_t align) {
+  if (reinterpret_cast<uintptr_t>(p) & (align - 1)) return nullptr;
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (pa.type != cudaMemoryTypeHost || !pa.devicePointer) return nullptr;
+  if (reinterpret_cast<uintptr_t>(pa.devicePointer) & (align - 1)) return nullptr;
+  return pa.devicePointer;
 }
 
 int check_layer(spin_ctx* c, int layer) {
@@ -999,7 +1026,7 @@ int spin_decode_step(spin_ctx* c, int32_t layer, const uint16_t* q, float* out, 
   if (rc) return rc;
   DeviceGuard g(c->device);
   if (!g.ok) return fail(c, SPIN_ERR_CUDA, "cannot select device %d", c->device);
-  return enqueue_step(c, layer, q, out, static_cast<cudaStream_t>(stream));
+  return enqueue_step(c, layer, q, q, out, static_cast<cudaStream_t>(stream));
 }
 
 int spin_decode_step_host(spin_ctx* c, int32_t layer, const uint16_t* q_host, float* out_host, spin_stream_t stream) {
@@ -1017,13 +1044,19 @@ int spin_decode_step_host(spin_ctx* c, int32_t layer, const uint16_t* q_host, fl
     if ((e = dalloc(c, &lb.out_stage, nq)) != cudaSuccess) return cuda_fail(c, e, "allocating the output buffer");
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Copy-engine transfers on both sides. Using mapped pinned buffers in place (a kernel
-  // staging q, the combine writing out over the host link) measured about 70 us slower
-  // per layer call on GB300.
-  SPIN_CUDA(c, cudaMemcpyAsync(lb.q_stage, q_host, nq * 2, cudaMemcpyHostToDevice, st), "copying q to the device");
-  rc = enqueue_step(c, layer, lb.q_stage, lb.out_stage, st);
+  // Pinned, device-mapped buffers are used in place: the kernel reads q over the host link
+  // (each unit's manager copies the unit's rows into HBM for the attention) and the combine
+  // writes out into host memory. A copy-engine transfer between two steps costs 11-17 us on
+  // GB300 whatever its size; the zero-copy reads and writes cost a few. Pageable or
+  // unaligned buffers go through HBM with cudaMemcpyAsync.
+  const uint16_t* q_dev_src = static_cast<const uint16_t*>(mapped_host(q_host, 8));
+  float* out_dev = static_cast<float*>(const_cast<void*>(mapped_host(out_host, 16)));
+  if (!q_dev_src)
+    SPIN_CUDA(c, cudaMemcpyAsync(lb.q_stage, q_host, nq * 2, cudaMemcpyHostToDevice, st), "copying q to the device");
+  rc = enqueue_step(c, layer, lb.q_stage, q_dev_src ? q_dev_src : lb.q_stage, out_dev ? out_dev : lb.out_stage, st);
   if (rc) return rc;
-  SPIN_CUDA(c, cudaMemcpyAsync(out_host, lb.out_stage, nq * 4, cudaMemcpyDeviceToHost, st), "copying out to the host");
+  if (!out_dev)
+    SPIN_CUDA(c, cudaMemcpyAsync(out_host, lb.out_stage, nq * 4, cudaMemcpyDeviceToHost, st), "copying out to the host");
   return SPIN_OK;
 }
 

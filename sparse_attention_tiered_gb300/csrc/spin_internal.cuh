@@ -80,7 +80,9 @@ struct LayerArgs {
   unsigned long long* stats; // [8] device counters
   unsigned long long* timeline; // [5] globaltimer stamps of this call (stage timing), else nullptr
   uint32_t* err;             // device error word
-  const uint16_t* q;         // [B][Hq][128] bf16 (device)
+  const uint16_t* q;         // [B][Hq][128] bf16 (HBM): the query rows the attention stages through TMA
+  const uint16_t* q_src;     // the queries the scores read: q itself, or pinned host memory (zero copy), in
+                             // which case each unit's manager first copies the unit's rows into q
   float* out;                // [B][Hq][128] fp32 (device)
 };
 

@@ -457,6 +457,28 @@ def test_tier_split_metadata_same_results_less_hbm():
     assert st_b["metadata_bytes"] == st_a["metadata_bytes"] - st_a["pool_segments"] * 64 * 4
 
 
+def test_metadata_accounting_flat_worst_case():
+    """The flat table of the pages' worst-case logical space (one int32 per partition of
+    max_context, per request, layer and KV head, plus the per-page state) against the
+    two-level table's directory (covering max_context), segment pool, live counts, bitmap
+    and the same per-page state; identical results with and without the larger directory."""
+    w = W.Workload("meta", B=3, L=2, Hq=10, Hkv=2, ctx_len=[1000, 4113, 9000], topk=8, buf_mult=2,
+                   drift_a=0.8, drift_c=0.2, steps=6, seed=41)
+    rep_a, st_a = _run(w)
+    wl = w.with_(max_context=65536)
+    rep_b, st_b = _run(wl)
+    for key in ("hits", "misses", "evictions", "live_segments"):
+        assert st_a[key] == st_b[key], key
+    units, slots = w.units, w.units * w.cap
+    S = st_b["pool_segments"]
+    Dl = -(-(65536 // 64) // 64)
+    assert st_b["flat_table_bytes"] == (units * (65536 // 64) + 2 * slots) * 4
+    assert st_b["metadata_bytes"] == (units * Dl + S * 64 + S + (S + 31) // 32 + 2 * slots) * 4
+    assert st_b["flat_table_bytes"] > st_b["metadata_bytes"]
+    P_max = max(w.partitions(b) for b in range(w.B))
+    assert st_a["flat_table_bytes"] == (units * P_max + 2 * slots) * 4
+
+
 def test_hugepage_host_store_same_results():
     """The page store as a huge-page mapping registered with CUDA: identical lockstep results."""
     from sparse_attention_tiered_gb300._binding import SPIN_FLAG_HOST_HUGEPAGES

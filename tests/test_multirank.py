@@ -65,3 +65,55 @@ def test_single_rank_defaults():
     assert (R.world, R.rank) == (1, 0)
     assert R.max(3.5) == 3.5
     assert bench.job_tokens_per_s(32, 1, 2.0) == pytest.approx(16000.0)
+
+
+def _mem_worker(rank, world, port, avail, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    import bench
+    R = bench.Ranks()
+    R.init("gloo")
+    need = (10 + rank) << 30  # 10 and 11 GiB of page store
+    try:
+        tot, av = R.check_host_memory(need, avail_bytes=avail + rank * (1 << 30))
+        q.put((rank, "ok", tot, av))
+    except SystemExit as e:
+        q.put((rank, "refused", str(e), None))
+    R.barrier()
+    R.close()
+
+
+@pytest.mark.parametrize("avail_gib,expect", [(40, "ok"), (20, "refused")])
+def test_two_gloo_ranks_host_memory_check(avail_gib, expect):
+    """Both ranks' page stores (21 GiB together) against the node's available memory (the
+    smaller rank report, 90% usable): the same decision on every rank, with the figures."""
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_mem_worker, args=(r, world, port, avail_gib << 30, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [expect, expect]
+    if expect == "ok":
+        assert res[0][2] == res[1][2] == float(21 << 30) and res[0][3] == float(avail_gib << 30)
+    else:
+        assert "21.0 GiB" in res[0][2] and "20.0 GiB available" in res[0][2]
+
+
+def test_gpu_local_cpus_from_sysfs(tmp_path):
+    sys.path.insert(0, ROOT)
+    import bench
+    d = tmp_path / "bus" / "pci" / "devices" / "0000:00:07.0"
+    d.mkdir(parents=True)
+    (d / "local_cpulist").write_text("0-3,8,10-11\n")
+    assert bench.gpu_local_cpus("0000:00:07.0", sysfs=str(tmp_path)) == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.gpu_local_cpus("0000:00:08.0", sysfs=str(tmp_path)) is None
+    assert bench.parse_cpulist("5") == {5}
+    meminfo = tmp_path / "meminfo"
+    meminfo.write_text("MemTotal: 100 kB\nMemAvailable:    2048 kB\n")
+    assert bench.mem_available_bytes(str(meminfo)) == 2048 * 1024

@@ -116,6 +116,7 @@ class Workload:
     d: int = D
     part: int = PART
     mean_part: int = 0          # > 0: variable partitions averaging about this many tokens
+    max_context: int = 0        # logical context capacity the deployment admits (0 = the longest context)
 
     # ---- derived shapes ----
     @property
@@ -288,30 +289,33 @@ def tiny(seed: int = 0) -> Workload:
 
 
 def qwen3_14b(seed: int = 0) -> Workload:
-    """Qwen3-14B-shaped decode: 40 q / 8 kv heads, 8 layers, batch 32, 32K context, top-32, 5x buffer, 64 steps."""
+    """Qwen3-14B-shaped decode: 40 q / 8 kv heads, 8 layers, batch 32, 32K context, top-32, 5x buffer, 64 steps;
+    logical capacity 131072 tokens (the model's extended context)."""
     return Workload("qwen3_14b_32k", B=32, L=8, Hq=40, Hkv=8, ctx_len=[32768] * 32, topk=32, buf_mult=5,
-                    drift_a=0.9, drift_c=0.1, steps=64, seed=seed)
+                    drift_a=0.9, drift_c=0.1, steps=64, seed=seed, max_context=131072)
 
 
 def llama31_70b(seed: int = 0) -> Workload:
-    """Llama-3.1-70B-shaped decode: 64 q / 8 kv heads, 4 layers, batch 16, 128K context, top-64, 5x, 32 steps."""
+    """Llama-3.1-70B-shaped decode: 64 q / 8 kv heads, 4 layers, batch 16, 128K context, top-64, 5x, 32 steps;
+    logical capacity 131072 tokens (the model's context)."""
     return Workload("llama31_70b_128k", B=16, L=4, Hq=64, Hkv=8, ctx_len=[131072] * 16, topk=64, buf_mult=5,
-                    drift_a=0.8, drift_c=0.2, steps=32, seed=seed)
+                    drift_a=0.8, drift_c=0.2, steps=32, seed=seed, max_context=131072)
 
 
 def stress(buf_mult: int = 1, seed: int = 0) -> Workload:
     """Qwen3-32B-shaped eviction/metadata stress: 64 q / 8 kv heads, 1 layer, batch 256,
-    context uniform over whole partitions in [8192, 32768] tokens, top-16, 1x or 5x buffer, 32 steps."""
+    context uniform over whole partitions in [8192, 32768] tokens, top-16, 1x or 5x buffer, 32 steps;
+    logical capacity 131072 tokens (the model's extended context)."""
     ctx = [64 * int(lib().wl_ctx_partitions(seed, b, 128, 512)) for b in range(256)]
     return Workload(f"stress_m{buf_mult}", B=256, L=1, Hq=64, Hkv=8, ctx_len=ctx, topk=16, buf_mult=buf_mult,
-                    drift_a=0.7, drift_c=0.3, steps=32, seed=seed)
+                    drift_a=0.7, drift_c=0.3, steps=32, seed=seed, max_context=131072)
 
 
 def long_1m(seed: int = 0) -> Workload:
     """Single 1M-token request: 40 q / 8 kv heads, 1 layer, 16384 partitions/head, top-128, 5x,
     1% of partitions offset by 3 * (normalised group query at step 0), drift 0.95/0.05, 64 steps."""
     return Workload("long_1m", B=1, L=1, Hq=40, Hkv=8, ctx_len=[1048576], topk=128, buf_mult=5,
-                    drift_a=0.95, drift_c=0.05, steps=64, seed=seed, hot_norm=3.0, hot_frac=0.01)
+                    drift_a=0.95, drift_c=0.05, steps=64, seed=seed, hot_norm=3.0, hot_frac=0.01, max_context=1048576)
 
 
 ALL = {"tiny": tiny, "qwen3_14b_32k": qwen3_14b, "llama31_70b_128k": llama31_70b,
