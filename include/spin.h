@@ -83,6 +83,11 @@ typedef enum spin_flags {
                                         and advised for transparent huge pages, registered with
                                         cudaHostRegister, instead of with cudaHostAlloc (falls back to
                                         cudaHostAlloc when mapping or registering fails) */
+  SPIN_FLAG_PHASED = 1u << 4,       /* run every decode step as phases over the whole grid (score, then
+                                       select + manage, then retrieve + attend) instead of the pipelined
+                                       kernel that units of at most 4096 partitions and groups of at most
+                                       8 query heads otherwise get (scoring, managing and retrieval at once);
+                                       the results are the same */
   SPIN_FLAG_TEST_FAIL_PINNED = 1u << 16, /* test hook: the pinned host allocation reports failure */
   SPIN_FLAG_TEST_NO_RETRIEVE = 1u << 17  /* test hook: no page is retrieved, so the bounded wait for the
                                             first missing page runs out and the step reports SPIN_ERR_TIMEOUT */

@@ -27,6 +27,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID", 2: "CUDA", 3: "OOM", 4: "CAPACITY", 5: "T
 SPIN_FLAG_STAGE_TIMING = 1 << 0
 SPIN_FLAG_TIER_SPLIT = 1 << 2
 SPIN_FLAG_HOST_HUGEPAGES = 1 << 3
+SPIN_FLAG_PHASED = 1 << 4
 SPIN_FLAG_TEST_FAIL_PINNED = 1 << 16
 SPIN_FLAG_TEST_NO_RETRIEVE = 1 << 17
 

@@ -62,8 +62,13 @@ namespace spin {
 namespace {
 
 constexpr int kStages = 6;    // ring stages (stage i belongs to consumer group i % groups)
+constexpr int kStagesPipe = 4;  // the pipelined kernel's ring: the manager group's shared memory sits beside it
 constexpr int kCWarps = 4;    // consumer warps of one group: 16 tokens of a page each
 constexpr int kMaxGroups = 2;
+// Stage i of the ring belongs to consumer group i % groups for good: the stage count is a
+// multiple of the group count, so each stage's barriers see one group's uses only, in order,
+// and a parity wait is never more than one phase away from the barrier's current phase.
+static_assert(kStages % kMaxGroups == 0 && kStagesPipe % kMaxGroups == 0, "stages must split evenly between groups");
 // Roles per CTA. One 8-head tile (NT = 1, at most 128 registers a thread): two
 // consumer groups that take alternate ring stages, so two pages are in the math at
 // once, each fed by its own producer warp, and six retriever warps (two saturate the
@@ -452,7 +457,7 @@ __device__ void combine_head_cta(const LayerArgs& a, int ul, int g, int w, int n
 // The decode-step kernel. NT = number of 8-head tiles (G <= 8 * NT); GS = threads of
 // one manager group in phase B.
 // ---------------------------------------------------------------------------
-template <int NT, int GS>
+template <int NT, int GS, bool PIPE>
 __global__ void __launch_bounds__(Roles<NT>::kThreads, 1)
 decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_hit_tasks) {
   extern __shared__ uint8_t smem_raw[];
@@ -460,6 +465,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
   StepSmem sm;
   step_smem_layout(&sm, base);
   constexpr int kThreads = Roles<NT>::kThreads;
+  constexpr int kSt = PIPE ? kStagesPipe : kStages;  // ring stages
+  static_assert(kSt % Roles<NT>::kGroups == 0, "each ring stage must belong to one consumer group");
   constexpr int NG = Roles<NT>::kGroups, NC = Roles<NT>::kConsumers;
   constexpr int kWarps = kThreads / 32;
   constexpr uint32_t kAll = 0xffffffffu;
@@ -468,11 +475,12 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
   const int tag = t + 1;  // flag value of this step (flags are never reset)
   const int U = a.B * a.Hkv;
   const int kmax = U * a.k;  // miss-list capacity
+  float* sc_cur = a.scores + (int64_t)(t & 1) * U * a.P_max;  // this step's score buffer
   unsigned long long* tl = a.timeline;
 
   if (tid == 0) {
     if (tl) atomicMax(tl + 0, ~globaltimer_ns());
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSt; ++s) {
       mbar_init(smem_u32(&sm.full[s]), 1);
       mbar_init(smem_u32(&sm.empty[s]), kCWarps);  // the four warps of the stage's group
     }
@@ -483,6 +491,137 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
+  if constexpr (PIPE) {
+    // ------------------------------ A + B, pipelined ------------------------------
+    // Warps 0 .. NC+NG-1 (consumers and producers) score batches of up to 8 partitions
+    // of one unit, batch j of the layer (unit-major order) going to scoring warp
+    // j mod (grid x (NC+NG)), so units complete in order across the grid; each then
+    // takes its phase-C role. Warps NC+NG .. NC+NG+3 form manager groups (one of four
+    // warps, or four of one) that claim units in order as soon as they are complete
+    // (no slot of the unit's score row still empty), then join the retrievers; the
+    // remaining retriever warps start on the miss list at once.
+    constexpr int kMgrWarps = 4;
+    constexpr int kMgrGroups = kMgrWarps * 32 / GS;
+    const size_t gbytes = sel::mgr_smem_layout(GS, a.P_max, a.cap, a.k, a.D, nullptr, nullptr);
+    uint8_t* mreg = sm.region + (size_t)kSt * kStageBytes;
+    int* s_pre = reinterpret_cast<int*>(mreg + kMgrGroups * gbytes);  // [B + 1] batches before request b
+    if (warp == 0) {
+      int run = 0;
+      for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int b = b0 + lane;
+        const int v = b < a.B ? a.Hkv * ((a.P_b[b] + sel::kRowsPerBatch - 1) / sel::kRowsPerBatch) : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(kAll, x, o);
+          if (lane >= o) x += y;
+        }
+        if (b < a.B) s_pre[b] = run + x - v;
+        run += __shfl_sync(kAll, x, 31);
+      }
+      if (lane == 0) s_pre[a.B] = run;
+    }
+    __syncthreads();
+    float* sc_next = a.scores + (int64_t)((t + 1) & 1) * U * a.P_max;
+    if (warp < NC + NG) {
+      const int nbatch = s_pre[a.B];
+      const int SWp = (int)gridDim.x * (NC + NG);
+      // request, head, first partition and row count of batch jj
+      auto locate = [&](int jj, int& b, int& h, int& p0, int& n) {
+        int lo = 0, hi = a.B;  // the largest b with s_pre[b] <= jj
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (s_pre[mid] <= jj) lo = mid;
+          else hi = mid;
+        }
+        b = lo;
+        const int Pb = a.P_b[b];
+        const int nb = (Pb + sel::kRowsPerBatch - 1) / sel::kRowsPerBatch;
+        const int off = jj - s_pre[b];
+        h = off / nb;
+        p0 = (off - h * nb) * sel::kRowsPerBatch;
+        n = min(sel::kRowsPerBatch, Pb - p0);
+      };
+      int j = (int)blockIdx.x * (NC + NG) + warp;
+      if (j < nbatch) {
+        int b, h, p0, n;
+        locate(j, b, h, p0, n);
+        float4 cur[sel::kRowsPerBatch], nxt[sel::kRowsPerBatch];
+        sel::load_rows(cur, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, p0) * kD), n, lane);
+        float4 qv = sel::qsum_lane(a.q_src + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
+        for (;;) {
+          const int j2 = j + SWp;
+          const bool more = j2 < nbatch;
+          int b2 = 0, h2 = 0, p2 = 0, n2 = 0;
+          if (more) {
+            locate(j2, b2, h2, p2, n2);
+            sel::load_rows(nxt, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b2, h2, p2) * kD), n2, lane);
+          }
+          const float x = sel::score_batch(cur, qv, lane);
+          if (lane < n) sc_cur[(int64_t)(b * a.Hkv + h) * a.P_max + p0 + lane] = x;
+          if (!more) break;
+          if (b2 != b || h2 != h) qv = sel::qsum_lane(a.q_src + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
+          j = j2;
+          b = b2;
+          h = h2;
+          p0 = p2;
+          n = n2;
+#pragma unroll
+          for (int i = 0; i < sel::kRowsPerBatch; ++i) cur[i] = nxt[i];
+        }
+      }
+      if (tl && lane == 0) atomicMax(tl + kTlScored, globaltimer_ns());
+    } else if (warp < NC + NG + kMgrWarps) {
+      const int grp = (tid - (NC + NG) * 32) / GS, gt = tid - (NC + NG) * 32 - grp * GS;
+      const int bar = 1 + grp;
+      sel::MgrSmem ms;
+      sel::mgr_smem_layout(GS, a.P_max, a.cap, a.k, a.D, &ms, mreg + grp * gbytes);
+      for (;;) {
+        if (gt == 0) ms.gs->unit = atomicAdd(&a.counters[kCtrManage], 1);
+        sel::gsync<GS>(bar);
+        const int ul = ms.gs->unit;
+        sel::gsync<GS>(bar);
+        if (ul >= U) break;
+        // wait until no slot of the unit's score row is empty (bounded)
+        const int P = a.P_b[ul / a.Hkv];
+        const float* sc = sc_cur + (int64_t)ul * a.P_max;
+        const unsigned long long t0 = globaltimer_ns();
+        bool ok = true;
+        for (uint32_t it = 0;; ++it) {
+          bool empty = false;
+          for (int p = gt; p < P; p += GS) empty |= __float_as_uint(__ldcg(sc + p)) == kScoreEmpty;
+          const bool any = __any_sync(kAll, empty);
+          if (gt == 0) ms.gs->ok = 0;
+          sel::gsync<GS>(bar);
+          if (any && lane == 0) atomicOr(&ms.gs->ok, 1);
+          if (gt == 0 && (it & 15u) == 15u &&
+              (globaltimer_ns() - t0 > kWaitNs || (ld_relaxed_u32(a.err) & kErrTimeout)))
+            atomicOr(&ms.gs->ok, 2);
+          sel::gsync<GS>(bar);
+          const int st = ms.gs->ok;
+          sel::gsync<GS>(bar);
+          if (st == 0) break;
+          if (st & 2) {
+            ok = false;
+            break;
+          }
+          __nanosleep(200);
+        }
+        if (!ok) {
+          if (gt == 0) {
+            atomicOr(a.err, kErrTimeout);
+            // publish the unit with nothing selected, so nobody waits for it
+            a.keff[ul] = 0;
+            a.n_hit[ul] = 0;
+            sel::publish_unit(a, ul, tag);
+          }
+          continue;
+        }
+        sel::manage_unit<GS>(a, ul, t, tag, ms, bar, gt, sc, sc_next + (int64_t)ul * a.P_max);
+        if (tl && gt == 0) atomicMax(tl + kTlManaged, globaltimer_ns());
+      }
+    }
+  } else {
   // ------------------------------ A. scoring ------------------------------
   // The layer's partitions, request-major then head then partition, are split into
   // equal contiguous row ranges, one per warp of the grid. A warp scores its range in
@@ -548,7 +687,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
         const int ul = b * a.Hkv + h;
         const float x = sel::score_batch(cur, qv, lane);
         if (lane < n) {
-          a.scores[(int64_t)ul * a.P_max + p + lane] = x;
+          sc_cur[(int64_t)ul * a.P_max + p + lane] = x;
           if (a.hist12) atomicAdd(a.hist12 + (int64_t)ul * sel::kHistBins + (sel::float_key(x) >> (32 - sel::kHistBits)), 1);
         }
         counted += n;
@@ -611,7 +750,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
           }
           continue;
         }
-        sel::manage_unit<GS>(a, ul, t, tag, ms, bar, gt);
+        sel::manage_unit<GS>(a, ul, t, tag, ms, bar, gt, sc_cur + (int64_t)ul * a.P_max, nullptr);
         if (tl && gt == 0) atomicMax(tl + 2, globaltimer_ns());
       }
     }
@@ -619,6 +758,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
   // the manager groups wrote the region with generic stores; TMA writes it next
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
+  }
   volatile int* abort_flag = sm.abort_flag;
 
   // ------------------------------ C. retrieval + attention ------------------------------
@@ -627,8 +767,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     // kEarly warps copy from the start; the others join once this CTA's resident pages
     // are issued (so they do not slow the HBM-bound hits).
     const int rw = warp - NC - NG;
-    bool active = rw < a.retr_warps;
-    if (!active && rw < a.retr_warps + a.retr_late) {
+    bool active = PIPE ? a.retr_warps > 0 : rw < a.retr_warps;
+    if (!PIPE && !active && rw < a.retr_warps + a.retr_late) {
       volatile int* hd = sm.hits_done;
       const unsigned long long t0 = globaltimer_ns();
       for (uint32_t it = 1; it < (1u << 30) && !*hd; ++it) {
@@ -676,7 +816,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
   } else if (warp >= NC) {
     // ------------------------------ producers ------------------------------
     // Producer warp g feeds consumer group g: stage indices i = g, g + NG, ... use ring
-    // stage i % kStages. Its stream: resident-page tasks (up to ppt pages of one unit,
+    // stage i % kSt. Its stream: resident-page tasks (up to ppt pages of one unit,
     // claimed from a shared counter, after the unit's ready flag), then retrieved pages
     // (one page each, in miss-list order, once the entry is written and its page
     // published), then a sentinel.
@@ -751,9 +891,9 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     auto leave_hits = [&]() {  // the last producer past its resident pages lets the late retrievers start
       if (lane == 0 && atomicAdd(sm.hits_groups, 1) == NG - 1) *((volatile int*)sm.hits_done) = 1;
     };
-    int last_issue[kStages];  // lane 0: last stage index that staged a page in each ring stage
+    int last_issue[kSt];  // lane 0: last stage index that staged a page in each ring stage
 #pragma unroll
-    for (int st = 0; st < kStages; ++st) last_issue[st] = -1;
+    for (int st = 0; st < kSt; ++st) last_issue[st] = -1;
     for (int i = g; ok && !done; i += NG) {
       if (__shfl_sync(kAll, *abort_flag, 0)) {
         ok = false;
@@ -848,8 +988,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
         }
       }
       if (!ok) break;
-      const int st = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      const int st = i % kSt;
+      const uint32_t ph = (uint32_t)(i / kSt) & 1u;
       int oke = 1;
       if (lane == 0) oke = mbar_wait(smem_u32(&sm.empty[st]), ph ^ 1u) ? 1 : 0;
       if (!__shfl_sync(kAll, oke, 0)) {
@@ -892,8 +1032,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       *((volatile int*)sm.hits_done) = 1;  // nobody waits for it in vain
       // drain the copies already issued before leaving (bounded)
 #pragma unroll
-      for (int st = 0; st < kStages; ++st)
-        if (last_issue[st] >= 0) (void)mbar_wait(smem_u32(&sm.full[st]), (uint32_t)(last_issue[st] / kStages) & 1u);
+      for (int st = 0; st < kSt; ++st)
+        if (last_issue[st] >= 0) (void)mbar_wait(smem_u32(&sm.full[st]), (uint32_t)(last_issue[st] / kSt) & 1u);
     }
   } else {
     // ------------------------------ consumers ------------------------------
@@ -913,8 +1053,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     int i = grp;
 
     for (;;) {
-      const int st = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      const int st = i % kSt;
+      const uint32_t ph = (uint32_t)(i / kSt) & 1u;
       if (!mbar_wait(smem_u32(&sm.full[st]), ph)) {
         atomicOr(a.err, kErrTimeout);
         *abort_flag = 1;
@@ -1133,13 +1273,19 @@ __global__ void resolve_all_kernel(LayerArgs a, int32_t* resolve, int32_t* live)
 
 __global__ void set_int_kernel(int32_t* p, int32_t v) { *p = v; }
 
-template <int NT, int GS>
+__global__ void fill_u32_kernel(uint32_t* p, uint32_t v, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = v;
+}
+
+template <int NT, int GS, bool PIPE = false>
 const void* kernel_ptr() {
-  return (const void*)decode_step_kernel<NT, GS>;
+  return (const void*)decode_step_kernel<NT, GS, PIPE>;
 }
 
 // The kernel instance for a layer: NT from the group size G, GS from mgr_gs.
 const void* pick_kernel(const LayerArgs& a) {
+  if (a.pipe) return a.mgr_gs == 32 ? kernel_ptr<1, 32, true>() : kernel_ptr<1, 128, true>();
   if (a.G <= 8) {
     switch (a.mgr_gs) {
       case 32: return kernel_ptr<1, 32>();
@@ -1165,6 +1311,10 @@ size_t step_ring_bytes() { return (size_t)kRingBytes; }
 // Dynamic shared memory of the decode-step kernel: header + max(ring, manager groups) +
 // 1 KiB for aligning the base.
 size_t step_smem_bytes(const LayerArgs& a) {
+  if (a.pipe)  // header, the ring, the manager groups (128 threads in all), the batch prefix
+    return kHeaderBytes + (size_t)kStagesPipe * kStageBytes +
+           (size_t)(128 / a.mgr_gs) * sel::mgr_smem_layout(a.mgr_gs, a.P_max, a.cap, a.k, a.D, nullptr, nullptr) +
+           4 * ((size_t)a.B + 1) + 16 + 1024;
   const int groups = step_threads(a.G) / a.mgr_gs;
   const size_t mgr = (size_t)groups * sel::mgr_smem_layout(a.mgr_gs, a.P_max, a.cap, a.k, a.D, nullptr, nullptr);
   return kHeaderBytes + (mgr > (size_t)kRingBytes ? mgr : (size_t)kRingBytes) + 1024;
@@ -1189,6 +1339,13 @@ cudaError_t launch_decode_step(const LayerArgs& a, const CUtensorMap* tmap, int 
 
 cudaError_t launch_set_int(int32_t* p, int32_t v, cudaStream_t st) {
   set_int_kernel<<<1, 1, 0, st>>>(p, v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_u32(uint32_t* p, uint32_t v, int64_t n, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4096);
+  fill_u32_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, v, n);
   return cudaGetLastError();
 }
 

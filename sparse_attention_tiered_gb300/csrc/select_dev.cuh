@@ -639,14 +639,17 @@ __device__ inline void publish_unit(const LayerArgs& a, int ul, int tag) {
   atomicAdd(&a.counters[kCtrManaged], 1);
 }
 
-// Select + manage unit ul of the layer at step t, once its scores are all in a.scores.
+// Select + manage unit ul of the layer at step t, once its scores are all in sc ([P], this
+// step's buffer). sc_reset (the pipelined kernel): the unit's slots in the other buffer,
+// set back to kScoreEmpty for the next step.
 // Writes the selection, slots, attention order, page state, two-level table, stats and
 // this step's miss-list entries (each published with its tag in miss_tag), then
 // publishes the unit (unit_ready = tag) and counts it in kCtrManaged. A unit whose
 // page state can no longer be trusted (device error word) or whose top-k failed is
 // published with nothing selected.
 template <int NT>
-__device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const MgrSmem& sm, int bar, int gt) {
+__device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const MgrSmem& sm, int bar, int gt,
+                            const float* sc, float* sc_reset) {
   constexpr int kW = NT / 32;
   GroupScalars* gs = sm.gs;
   const int lane = gt & 31;
@@ -655,6 +658,8 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
   const int k = a.k, cap = a.cap;
   int keff = P < k ? P : k;
   const int64_t unit = a.unit_base + ul;
+  if (sc_reset)  // the next step's buffer: every slot it will write starts empty
+    for (int p = gt; p < P; p += NT) sc_reset[p] = __uint_as_float(kScoreEmpty);
   const bool dead = (*((volatile uint32_t*)a.err) & (kErrCapacity | kErrInternal | kErrSelCount | kErrSegId | kErrIndex)) != 0;
   bool ok = !dead;
   if (a.q_src != a.q) {
@@ -693,7 +698,7 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
     if (ok && a.hist12 != nullptr) {
       // the list lives in the keys' shared memory: P_max / 2 (partition, key) pairs
       const int lmax = a.P_max / 2;
-      wide_done = wide_topk<NT>(a.scores + (int64_t)ul * a.P_max, P, keff, a.hist12 + (int64_t)ul * kHistBins,
+      wide_done = wide_topk<NT>(sc, P, keff, a.hist12 + (int64_t)ul * kHistBins,
                                 reinterpret_cast<int32_t*>(sm.keys), sm.keys + lmax, lmax, sm.flist, sm.whist, gs,
                                 bar, gt, sm.sel);
       if (wide_done < 0) {
@@ -703,7 +708,6 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
     }
   }
   if (ok && wide_done == 0) {
-    const float* sc = a.scores + (int64_t)ul * a.P_max;
     for (int p0 = gt; p0 < P; p0 += 8 * NT) {
       float v[8];
 #pragma unroll

@@ -79,6 +79,7 @@ struct LayerBuf {
 };
 
 constexpr int kNumStages = 5;  // score, manage, pages (retrieval + attention), combine, whole kernel
+constexpr int kPipeGroupFirst = 128;  // threads of a manager group the pipelined kernel tries first
 constexpr int kTimelineCalls = 4096;  // stage-stamp records of timed calls between two synchronisations
 
 // One timed call: CUDA events around the kernel and the slot of its stage stamps.
@@ -98,6 +99,7 @@ struct spin_ctx {
   int retr_warps = 2;  // retriever warps per CTA from the start of the retrieval phase
   int retr_late = 4;   // retriever warps that join after the CTA's resident pages are issued
   int mgr_gs = 512;    // threads of one manager group
+  int pipe = 0;        // 1: the pipelined decode-step kernel
   int store_warm = 1;          // SPIN_STORE_WARM: read passes over the host store after it is written (0..8)
   bool store_cold = false;     // the store was written since its last read pass
   int64_t warm_stride = 32768; // bytes between the read pass's loads: the host page size, at most 32 KiB
@@ -144,6 +146,7 @@ struct spin_ctx {
   CUtensorMap tmap{};
   std::vector<uint8_t> offloaded;  // [L][B]
   int64_t steps_host = 0;
+  std::vector<int64_t> layer_steps;  // decode steps enqueued per layer (the kernel's step counter)
   uint32_t sticky = 0;
   std::string msg;
   // stage timing
@@ -388,6 +391,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.retr_warps = c->retr_warps;
   a.retr_late = c->retr_late;
   a.mgr_gs = c->mgr_gs;
+  a.pipe = c->pipe;
   a.ka = c->ka;
   a.P_b = c->d_P_lb + (int64_t)l * c->B;
   a.ntok_b = c->d_ntok_lb + (int64_t)l * c->B;
@@ -638,8 +642,27 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     if (gs == 128 && !fits(128)) gs = full;
     c->mgr_gs = gs;
     probe.mgr_gs = gs;
+    probe.B = c->B;
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
+    // the pipelined kernel (scoring, manager groups and retrieval at once, a 4-stage ring) for
+    // units of at most 4096 partitions and groups of at most 8 query heads, when its shared
+    // memory fits; otherwise the phased kernel. Its four manager warps form one group of 128
+    // threads or four groups of one warp.
+    if (c->G <= 8 && c->P_max <= 4096 && c->B <= 8192 && !(c->flags & SPIN_FLAG_PHASED)) {
+      const int order[2] = {kPipeGroupFirst, kPipeGroupFirst == 32 ? 128 : 32};
+      for (int gs_p : order) {
+        LayerArgs pp = probe;
+        pp.pipe = 1;
+        pp.mgr_gs = gs_p;
+        if (step_smem_bytes(pp) <= (size_t)optin) {
+          c->pipe = 1;
+          c->mgr_gs = gs_p;
+          probe = pp;
+          break;
+        }
+      }
+    }
     if (step_smem_bytes(probe) > (size_t)optin)
       return fail(nullptr, SPIN_ERR_INVALID,
                   "the page manager of one unit needs %zu bytes of shared memory (max %d): reduce the longest "
@@ -655,8 +678,11 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   c->layers.resize(c->L);
   for (int l = 0; l < c->L; ++l) {
     LayerBuf& lb = c->layers[l];
-    // (+4: the wide top-k reads a unit's scores four at a time, up to 3 past its last partition)
-    ALLOC(lb.scores, Ul * std::max(1, c->P_max) + 4, "allocating layer scratch");
+    // two buffers (step parity); +4: the wide top-k reads a unit's scores four at a time, up to
+    // 3 past its last partition
+    ALLOC(lb.scores, 2 * Ul * std::max(1, c->P_max) + 4, "allocating layer scratch");
+    SPIN_CUDA(nullptr, launch_fill_u32(reinterpret_cast<uint32_t*>(lb.scores), kScoreEmpty,
+                                       2 * Ul * std::max(1, c->P_max) + 4, 0), "initialising layer scratch");
     ALLOC(lb.sel, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.sel_slot, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.sel_hit, Ul * c->k, "allocating layer scratch");
@@ -694,6 +720,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   }
 #undef ALLOC
   c->offloaded.assign((size_t)c->L * c->B, 0);
+  c->layer_steps.assign(c->L, 0);
 
   int rc = encode_tensor_map(c);
   if (rc != SPIN_OK) {
@@ -741,6 +768,7 @@ int enqueue_step(spin_ctx* c, int layer, const uint16_t* q, const uint16_t* q_sr
     c->timed_calls += 1;
   }
   c->steps_host += 1;
+  c->layer_steps[layer] += 1;
   return SPIN_OK;
 }
 
@@ -1126,7 +1154,8 @@ int spin_debug_export(spin_ctx* c, int32_t layer, spin_state_view* v) {
   D2H(v->slot_part, c->d_slot_part + u0 * c->cap, Ul * c->cap * 4);
   D2H(v->last_use, c->d_last_use + u0 * c->cap, Ul * c->cap * 4);
   D2H(v->unit_info, lb.unit_info, Ul * 8 * 4);
-  D2H(v->scores, lb.scores, Ul * c->P_max * 4);
+  // the last step's buffer: step t writes buffer t & 1
+  D2H(v->scores, lb.scores + (size_t)((c->layer_steps[layer] + 1) & 1) * Ul * c->P_max, Ul * c->P_max * 4);
   if (v->resolve || v->live_segs) {
     int32_t *dres = nullptr, *dlive = nullptr;
     if (cudaMalloc(&dres, std::max<int64_t>(1, Ul * c->P_max) * 4) != cudaSuccess ||

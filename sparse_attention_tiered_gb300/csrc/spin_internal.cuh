@@ -36,6 +36,7 @@ struct LayerArgs {
   int32_t retr_warps;        // retriever warps active per CTA from the start of phase C
   int32_t retr_late;         // further retriever warps that join once the CTA's resident pages are issued
   int32_t mgr_gs;            // threads of one manager group (32, 128, or the CTA's full group)
+  int32_t pipe;              // 1: the pipelined kernel (scoring, one manager group and retrieval run at once)
   const int32_t* P_b;        // [B] selectable partitions of request b in this layer (tail mode: complete ones)
   const int32_t* ntok_b;     // [B] tokens held by those partitions
   const int32_t* tail_n;     // [B] tokens in the request's tail page (tail mode), else nullptr
@@ -56,7 +57,7 @@ struct LayerArgs {
   uint32_t* seg_bitmap;      // [ceil(S/32)] 1 = segment in use
   int32_t* slot_part;        // [units][cap]
   int32_t* last_use;         // [units][cap]
-  float* scores;             // [U_l][P_max]
+  float* scores;             // [2][U_l][P_max]: step t writes buffer t & 1 (kScoreEmpty where not written yet)
   int32_t* sel;              // [U_l][k]
   int32_t* sel_slot;         // [U_l][k] local slot
   uint8_t* sel_hit;          // [U_l][k]
@@ -110,6 +111,10 @@ enum : int {
 // managed, last CTA done with its pages, last combine done.
 enum : int { kTlStart = 0, kTlScored = 1, kTlManaged = 2, kTlPages = 3, kTlEnd = 4, kTlSlots = 8 };
 
+// Bit pattern of a score slot not yet written in this step (a signalling NaN the score
+// arithmetic never produces): the pipelined kernel's managers wait until none is left.
+constexpr uint32_t kScoreEmpty = 0x7FBFFFFFu;
+
 // Device stats slots.
 enum : int {
   kStatHits = 0, kStatMisses = 1, kStatEvictions = 2, kStatLruRounds = 3, kStatSelected = 4, kStatFlushes = 5
@@ -143,5 +148,7 @@ size_t mgr_group_bytes(int gs, const LayerArgs& a);  // shared memory of one man
 int step_threads(int G);                      // threads per CTA
 int step_full_group(int G);                   // the largest manager group (all warps of a CTA's roles)
 cudaError_t launch_resolve_all(const LayerArgs& a, int32_t* resolve, int32_t* live_segs, cudaStream_t st);
+// Fills n 32-bit words with v, ordered on the stream.
+cudaError_t launch_fill_u32(uint32_t* p, uint32_t v, int64_t n, cudaStream_t st);
 
 }  // namespace spin

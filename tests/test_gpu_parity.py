@@ -479,6 +479,20 @@ def test_metadata_accounting_flat_worst_case():
     assert st_a["flat_table_bytes"] == (units * P_max + 2 * slots) * 4
 
 
+def test_phased_kernel_same_results():
+    """The phased decode-step kernel (scoring, then managing, then retrieval over the whole
+    grid) against the pipelined one this workload gets by default: both in lockstep with
+    the oracle, with the same paging record."""
+    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_PHASED
+    w = W.Workload("phased", B=5, L=2, Hq=10, Hkv=2, ctx_len=[1000, 4113, 9000, 64, 0], topk=8, buf_mult=2,
+                   drift_a=0.8, drift_c=0.2, steps=12, seed=59)
+    rep_a, st_a = _run(w)
+    rep_b, st_b = _run(w, flags=SPIN_FLAG_PHASED)
+    assert rep_a.max_out_err <= OUT_TOL and rep_b.max_out_err <= OUT_TOL
+    for key in ("hits", "misses", "evictions", "lru_rounds", "live_segments"):
+        assert st_a[key] == st_b[key], key
+
+
 def test_hugepage_host_store_same_results():
     """The page store as a huge-page mapping registered with CUDA: identical lockstep results."""
     from sparse_attention_tiered_gb300._binding import SPIN_FLAG_HOST_HUGEPAGES
