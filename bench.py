@@ -410,12 +410,16 @@ def bench_reference(args):
 # GPU path
 # ---------------------------------------------------------------------------
 
-def make_context(w, args, local, extra_flags=0, append_tokens=0, rank=0):
-    """Context with every request of every layer indexed and offloaded (set-up, untimed)."""
+def make_context(w, args, local, extra_flags=0, append_tokens=0, rank=0, stage_timing=False):
+    """Context with every request of every layer indexed and offloaded (set-up, untimed).
+    stage_timing: CUDA events around every launch and in-kernel stage stamps. They add a few
+    microseconds to each launch, so throughput is timed on contexts without them and the
+    per-launch durations and stages come from a separate pass over the same steps."""
     import torch
     from sparse_attention_tiered_gb300 import SpinContext
     from sparse_attention_tiered_gb300._binding import SPIN_FLAG_HOST_HUGEPAGES, SPIN_FLAG_STAGE_TIMING
-    flags = SPIN_FLAG_STAGE_TIMING | (SPIN_FLAG_HOST_HUGEPAGES if args.host_alloc == "hugepages" else 0) | extra_flags
+    flags = ((SPIN_FLAG_STAGE_TIMING if stage_timing else 0) |
+             (SPIN_FLAG_HOST_HUGEPAGES if args.host_alloc == "hugepages" else 0) | extra_flags)
     ctx = SpinContext.for_workload(w, device=local, flags=flags,
                                    **({"append_tokens": append_tokens} if append_tokens else {}))
     kbuf = vbuf = None
@@ -456,16 +460,11 @@ def run_config(w, args, local, hbm_gbs, host_gbs, extra_flags=0, budget=0, appen
                warm_steps=0):
     """Runs every decode step of a workload (its configured count) on a fresh context and
     reports throughput over all steps and over the steps after `warm_steps`, the paging
-    record, the roofline fractions and, optionally, the oracle on a bounded sample."""
+    record, the roofline fractions and, optionally, the oracle on a bounded sample. A second
+    fresh context runs the same steps with stage timing for the per-launch stage record."""
     import torch
     dev = torch.device(f"cuda:{local}")
     steps = w.steps
-    t_setup = time.perf_counter()
-    ctx = make_context(w, args, local, extra_flags, append_tokens=steps if append else 0)
-    if budget:
-        for b in range(w.B):
-            ctx.set_buffer(b, budget)
-    setup_s = time.perf_counter() - t_setup
     qs = w.queries()
     q_dev = torch.empty((steps, w.L, w.B, w.Hq, 128), dtype=torch.int16)
     for t in range(steps):
@@ -478,27 +477,42 @@ def run_config(w, args, local, hbm_gbs, host_gbs, extra_flags=0, budget=0, appen
         kv = torch.randn((steps, w.L, 2, w.B, w.Hkv, 128), generator=gen).to(torch.bfloat16).view(torch.int16).to(dev)
     out = torch.empty((w.L, w.B, w.Hq, 128), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    torch.cuda.synchronize()
-    st0 = ctx.stats()
-    ev[0].record()
-    stw = None
-    for t in range(steps):
-        for l in range(w.L):
-            if append:
-                ctx.append_kv(l, kv[t, l, 0], kv[t, l, 1], stream)
-            ctx.decode_step(l, q_dev[t, l], out[l], stream)
-        ev[t + 1].record()
-        if t + 1 == warm_steps:
-            torch.cuda.synchronize()
-            stw = ctx.stats()
-    torch.cuda.synchronize()
-    st1 = ctx.stats()
-    ms_step = [ev[t].elapsed_time(ev[t + 1]) for t in range(steps)]
+
+    def one_pass(stage_timing):
+        t_setup = time.perf_counter()
+        ctx = make_context(w, args, local, extra_flags, append_tokens=steps if append else 0,
+                           stage_timing=stage_timing)
+        if budget:
+            for b in range(w.B):
+                ctx.set_buffer(b, budget)
+        setup_s = time.perf_counter() - t_setup
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        torch.cuda.synchronize()
+        st0 = ctx.stats()
+        ev[0].record()
+        stw = None
+        for t in range(steps):
+            for l in range(w.L):
+                if append:
+                    ctx.append_kv(l, kv[t, l, 0], kv[t, l, 1], stream)
+                ctx.decode_step(l, q_dev[t, l], out[l], stream)
+            ev[t + 1].record()
+            if t + 1 == warm_steps:
+                torch.cuda.synchronize()
+                stw = ctx.stats()
+        torch.cuda.synchronize()
+        st1 = ctx.stats()
+        ctx.close()
+        ms_step = [ev[t].elapsed_time(ev[t + 1]) for t in range(steps)]
+        return setup_s, ms_step, st0, stw, st1
+
+    setup_s, ms_step, st0, stw, st1 = one_pass(False)
     d_all = stats_delta(st1, st0)
     d_w = stats_delta(st1, stw) if stw is not None else d_all
     ms_all, ms_w = sum(ms_step), sum(ms_step[warm_steps:])
-    calls_w = max(1, d_w["timed_calls"])
+    _, _, sst0, sstw, sst1 = one_pass(True)
+    ds = stats_delta(sst1, sstw if sstw is not None else sst0)
+    calls_s = max(1, ds["timed_calls"])
     r = {
         "workload": workload_desc(w), "steps": steps, "steady_from_step": warm_steps,
         "tokens_per_s_all_steps": w.B * steps / (ms_all * 1e-3),
@@ -508,16 +522,16 @@ def run_config(w, args, local, hbm_gbs, host_gbs, extra_flags=0, budget=0, appen
         "combined_roofline_steady": roofline_terms(w, d_w, ms_w, hbm_gbs, host_gbs, steps - warm_steps),
         "host_link_gbs_steady": d_w["retrieved_bytes"] / (ms_w * 1e-3) / 1e9 if ms_w else None,
         "hbm_selected_gbs_steady": d_w["selected_bytes"] / (ms_w * 1e-3) / 1e9 if ms_w else None,
-        "stages_ms_per_layer_call_steady": {k2[3:]: d_w[k2] / calls_w for k2 in
+        "stages_ms_per_layer_call_steady": {k2[3:]: ds[k2] / calls_s for k2 in
                                             ("ms_score", "ms_manage", "ms_pages", "ms_combine", "ms_kernel")},
+        "stages_from": "a second fresh context over the same steps with stage timing (events per launch)",
         "paging_all_steps": {"hits": d_all["hits"], "misses": d_all["misses"], "evictions": d_all["evictions"],
                              "lru_rounds": d_all["lru_rounds"], "retrieved_bytes": d_all["retrieved_bytes"]},
         "metadata": {"metadata_bytes": st1["metadata_bytes"], "flat_table_bytes": st1["flat_table_bytes"],
                      "flat_over_metadata": st1["flat_table_bytes"] / max(1, st1["metadata_bytes"]),
                      "live_segments": st1["live_segments"], "pool_segments": st1["pool_segments"]},
-        "setup_s": setup_s, "device_error": st1["device_error"],
+        "setup_s": setup_s, "device_error": st1["device_error"] or sst1["device_error"],
     }
-    ctx.close()
     del q_dev, out, kv
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -625,29 +639,48 @@ def bench_spin(args):
     value = job_tokens_per_s(w.B * K, world, ms)
 
     d = stats_delta(st1, st0)
-    calls = max(1, d["timed_calls"])
-    kern_ms = d["ms_kernel"] / calls                    # the decode-step kernel, per layer call
-    sel_b = d["selected_bytes"] / calls                 # algorithmic bytes per launch
+    gpu_launches = K * w.L * (1 + (1 if args.append else 0))
+
+    st2 = ctx.stats()
+    ctx.close()
+
+    def fresh_context(stage_timing):
+        c = make_context(w, args, local, SPIN_FLAG_TIER_SPLIT if args.tier_split else 0,
+                         append_tokens=n_steps_total if args.append else 0, rank=rank, stage_timing=stage_timing)
+        if args.budget:
+            for b in range(w.B):
+                c.set_buffer(b, args.budget)
+        return c
+
+    # ---- per-launch durations and stages: the same warm-up and timed steps on a fresh context
+    # with stage timing (CUDA events around every launch on its stream, in-kernel stage stamps),
+    # which would add a few microseconds to every launch of the timed region above ----
+    ctx = fresh_context(True)
+    for t in range(Wm):
+        step(t)
+    torch.cuda.synchronize()
+    ss0 = ctx.stats()
+    for t in range(Wm, Wm + K):
+        step(t)
+    torch.cuda.synchronize()
+    ss1 = ctx.stats()
+    ctx.close()
+    ds = stats_delta(ss1, ss0)
+    calls = max(1, ds["timed_calls"])
+    kern_ms = ds["ms_kernel"] / calls                   # the decode-step kernel, per layer call
+    sel_b = ds["selected_bytes"] / calls                # algorithmic bytes per launch
     summ_b = w.summary_bytes_per_step() / w.L
-    ret_b = d["retrieved_bytes"] / calls
+    ret_b = ds["retrieved_bytes"] / calls
     hbm_b = sel_b + summ_b
     hbm_achieved = hbm_b / (kern_ms * 1e-3) / 1e9 if kern_ms > 0 else 0.0
     host_achieved = ret_b / (kern_ms * 1e-3) / 1e9 if kern_ms > 0 else 0.0
     host_bound = ret_b / host_gbs >= hbm_b / hbm_gbs
     traffic = attention_traffic(hbm_b)
-    gpu_launches = K * w.L * (1 + (1 if args.append else 0))
-
-    st2 = ctx.stats()
-    ctx.close()
     # ---- end to end through the host-buffer entry point: a fresh context, the same warm-up
     # and the same timed step range, with q read from and out written to pinned host memory ----
     e2e = None
     if not args.no_e2e:
-        ctx = make_context(w, args, local, SPIN_FLAG_TIER_SPLIT if args.tier_split else 0,
-                           append_tokens=n_steps_total if args.append else 0, rank=rank)
-        if args.budget:
-            for b in range(w.B):
-                ctx.set_buffer(b, args.budget)
+        ctx = fresh_context(False)
         for t in range(Wm):
             step(t)
         o_host = torch.empty((w.L, w.B, w.Hq, 128), dtype=torch.float32).pin_memory()
@@ -723,8 +756,9 @@ def bench_spin(args):
                                   "definition": "(selected KV bytes / HBM GB/s + retrieved bytes / host-link GB/s) "
                                                 "/ measured time, over the timed steps; frac_with_summaries also "
                                                 "counts the summary bytes Select reads"},
-            "stages_ms_per_layer_call": {k2[3:]: d[k2] / calls for k2 in
+            "stages_ms_per_layer_call": {k2[3:]: ds[k2] / calls for k2 in
                                          ("ms_score", "ms_manage", "ms_pages", "ms_combine", "ms_kernel")},
+            "stages_from": "the same warm-up and timed steps on a second fresh context with stage timing",
             "paging": {"hits": d["hits"], "misses": d["misses"], "evictions": d["evictions"],
                        "lru_rounds": d["lru_rounds"], "live_segments": st2["live_segments"],
                        "pool_segments": st2["pool_segments"], "metadata_bytes": st2["metadata_bytes"],

@@ -253,9 +253,7 @@ int spin_set_buffer(spin_ctx* ctx, int32_t b, int32_t pages, spin_stream_t strea
  * any layer) first enqueues one read pass over the whole host store: a 4-byte load
  * every host page (at most every 32 KiB). The GPU translates each host page's
  * address on its first read, and those translations resolve slowly; the pass pays
- * for them once, so the steps' retrieval does not. Environment variable
- * SPIN_STORE_WARM, read by spin_create, sets the number of passes: 0 to 8, default
- * 1; 0 turns the pass off. */
+ * for them once, so the steps' retrieval does not. */
 int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out, spin_stream_t stream);
 
 /* The same step with host buffers: q_host [batch][q_heads][128] bf16 and

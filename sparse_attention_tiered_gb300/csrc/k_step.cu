@@ -104,6 +104,7 @@ struct StepSmem {
   int* abort_flag;
   int* hits_done;     // set once every producer of this CTA has issued its resident-page tasks
   int* hits_groups;   // producers past their resident pages
+  int* tl_count;      // [2] stage timing: scoring warps done, combining warps done
   uint8_t* region;    // ring (kStages x kStageBytes) / manager groups
 };
 
@@ -124,6 +125,7 @@ __host__ __device__ inline void step_smem_layout(StepSmem* s, uint8_t* base) {
   s->abort_flag = (int*)take(sizeof(int), 4);
   s->hits_done = (int*)take(sizeof(int), 4);
   s->hits_groups = (int*)take(sizeof(int), 4);
+  s->tl_count = (int*)take(sizeof(int) * 2, 4);
   s->region = base + kHeaderBytes;
 }
 static_assert(sizeof(uint64_t) * (2 * kStages + 2 * kMaxGroups) + sizeof(StageMeta) * kStages + 64 <= kHeaderBytes,
@@ -211,6 +213,12 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 }
 
 __device__ __forceinline__ void fence_acq_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -488,6 +496,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     *sm.abort_flag = 0;
     *sm.hits_done = 0;
     *sm.hits_groups = 0;
+    sm.tl_count[0] = sm.tl_count[1] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
 
@@ -570,7 +579,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
           for (int i = 0; i < sel::kRowsPerBatch; ++i) cur[i] = nxt[i];
         }
       }
-      if (tl && lane == 0) atomicMax(tl + kTlScored, globaltimer_ns());
+      // stage timing: the CTA's last scoring warp stamps (one global atomic per CTA)
+      if (tl && lane == 0 && atomicAdd(sm.tl_count, 1) == NC + NG - 1) atomicMax(tl + kTlScored, globaltimer_ns());
     } else if (warp < NC + NG + kMgrWarps) {
       const int grp = (tid - (NC + NG) * 32) / GS, gt = tid - (NC + NG) * 32 - grp * GS;
       const int bar = 1 + grp;
@@ -779,10 +789,17 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     }
     constexpr int kVec = kPageBytes / 16;  // 2048 x 16 B
     constexpr int kUnroll = 16;            // 16 x 16 B in flight per lane
+    constexpr int kPieceVec = kVec / kRetrChunks;
+    static_assert(kPieceVec % (32 * kUnroll) == 0 && (kRetrChunks & (kRetrChunks - 1)) == 0, "piece layout");
+    const int split = a.retr_split;
     for (; active;) {
-      int m = 0;
-      if (lane == 0) m = atomicAdd(&a.counters[kCtrRetrieve], 1);
-      m = __shfl_sync(kAll, m, 0);
+      // claim i: pieces of the first `split` entries, then whole pages (m is non-decreasing in i)
+      int i = 0;
+      if (lane == 0) i = atomicAdd(&a.counters[kCtrRetrieve], 1);
+      i = __shfl_sync(kAll, i, 0);
+      const bool piece = i < split * kRetrChunks;
+      const int m = piece ? i / kRetrChunks : split + (i - split * kRetrChunks);
+      const int v0 = piece ? (i % kRetrChunks) * kPieceVec : 0, v1 = piece ? v0 + kPieceVec : kVec;
       int st = 0;
       if (lane == 0) st = miss_entry(a, m, tag, U, kmax);
       st = __shfl_sync(kAll, st, 0);
@@ -802,7 +819,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       const uint4* src = reinterpret_cast<const uint4*>(a.host_store + sp * kPageElems);
       uint4* dst = reinterpret_cast<uint4*>(a.pool + dp * kPageElems);
 #pragma unroll 1
-      for (int c = 0; in_range && c < kVec; c += 32 * kUnroll) {
+      for (int c = v0; in_range && c < v1; c += 32 * kUnroll) {
         uint4 r[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) r[u] = __ldcs(src + c + u * 32 + lane);
@@ -811,7 +828,13 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       }
       fence_acq_rel();  // each lane's stores of the page before the flag (acq_rel: no full sc fence)
       __syncwarp();
-      if (lane == 0) st_release(a.ready + m, tag);
+      if (lane == 0) {
+        // a split entry's flag goes up with its last piece: the counter grows by kRetrChunks
+        // every step, so the piece that brings it to a multiple of kRetrChunks is the last
+        // (its acq_rel add sees the other pieces' stores, and the release store passes them on)
+        const bool last = !piece || ((atom_add_acq_rel(a.ready_cnt + m, 1u) + 1u) & (kRetrChunks - 1)) == 0;
+        if (last) st_release(a.ready + m, tag);
+      }
     }
   } else if (warp >= NC) {
     // ------------------------------ producers ------------------------------
@@ -1243,7 +1266,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     // (unit, head) pairs spread over every consumer warp of the grid
     for (int p = blockIdx.x * NC + warp; p < pairs; p += gridDim.x * NC) combine_head(a, p / a.G, p % a.G, lane);
   }
-  if (tl && lane == 0) atomicMax(tl + kTlEnd, globaltimer_ns());
+  if (tl && lane == 0 && atomicAdd(sm.tl_count + 1, 1) == NC - 1) atomicMax(tl + kTlEnd, globaltimer_ns());
 }
 
 // ---------------------------------------------------------------------------

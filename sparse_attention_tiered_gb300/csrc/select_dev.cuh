@@ -369,6 +369,19 @@ __device__ int wide_topk(const float* __restrict__ sc, int P, int keff, int32_t*
   constexpr int kPer = kHistBins / NT;
   constexpr int kShift = 32 - kHistBits;
   const int lane = gt & 31, w = gt >> 5;
+  // The unit's scores go out with the histogram's counts when they fit eight 16-byte loads
+  // a thread: one memory round trip before the list can be built.
+  const int n4 = (P + 3) >> 2;
+  const bool in_regs = (reinterpret_cast<uintptr_t>(sc) & 15) == 0 && n4 <= 8 * NT;
+  const float4* sc4 = reinterpret_cast<const float4*>(sc);
+  float4 v4[8];
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = w * 32 + u * NT + lane;
+      v4[u] = i < n4 ? __ldcg(sc4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   // 1. the threshold value of the top 12 bits
   int c[kPer], lsum = 0;
 #pragma unroll
@@ -410,9 +423,16 @@ __device__ int wide_topk(const float* __restrict__ sc, int P, int keff, int32_t*
       list_k[base + __popc(m & lanemask_lt())] = key;
     }
   };
-  if ((reinterpret_cast<uintptr_t>(sc) & 15) == 0) {
-    const float4* sc4 = reinterpret_cast<const float4*>(sc);
-    const int n4 = (P + 3) >> 2;
+  if (in_regs) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int p = 4 * (w * 32 + u * NT + lane);
+      append(p, v4[u].x);
+      append(p + 1, v4[u].y);
+      append(p + 2, v4[u].z);
+      append(p + 3, v4[u].w);
+    }
+  } else if ((reinterpret_cast<uintptr_t>(sc) & 15) == 0) {
     for (int i0 = w * 32; i0 < n4; i0 += 8 * NT) {
       float4 v[8];
 #pragma unroll
@@ -805,6 +825,10 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
   // free pages are counted against the request's budget (buffer elasticity): after a
   // shrink the demand includes the excess and the LRU reclaims down to the budget
   const int demand = misses - (a.budget_b[b] - resident);
+  // the unit's entries in the step's miss list (ranks 0 .. misses-1): one reservation, sent
+  // now so that its round trip overlaps the LRU and the slot assignment
+  int mres = 0;
+  if (gt == 0 && misses > 0) mres = atomicAdd(&a.counters[kCtrMiss], misses);
 
   // ---------------- 3. bucketed LRU ----------------
   if (demand > 0) {
@@ -904,11 +928,9 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
       }
     }
   }
+  if (gt == 0) gs->ncand = mres;
   gsync<NT>(bar);
   const int kmax = a.B * a.Hkv * k;  // miss-list capacity
-  // one reservation of the unit's entries in the step's miss list (ranks 0 .. misses-1)
-  if (gt == 0) gs->ncand = misses > 0 ? atomicAdd(&a.counters[kCtrMiss], misses) : 0;
-  gsync<NT>(bar);
   const int mbase = gs->ncand;
   for (int j = gt; j < keff; j += NT) {
     const int code = sm.hit[j];

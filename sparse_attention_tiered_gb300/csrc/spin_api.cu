@@ -64,6 +64,7 @@ struct LayerBuf {
   int32_t* miss_att = nullptr;
   int32_t* miss_valid = nullptr;
   int32_t* ready = nullptr;
+  uint32_t* ready_cnt = nullptr;
   int32_t* miss_tag = nullptr;
   int32_t* unit_rows = nullptr;
   int32_t* unit_ready = nullptr;
@@ -100,7 +101,8 @@ struct spin_ctx {
   int retr_late = 4;   // retriever warps that join after the CTA's resident pages are issued
   int mgr_gs = 512;    // threads of one manager group
   int pipe = 0;        // 1: the pipelined decode-step kernel
-  int store_warm = 1;          // SPIN_STORE_WARM: read passes over the host store after it is written (0..8)
+  int retr_split = 0;  // miss-list entries of a step copied in kRetrChunks pieces (the first ones)
+  int store_warm = 1;          // read passes over the host store after it is written
   bool store_cold = false;     // the store was written since its last read pass
   int64_t warm_stride = 32768; // bytes between the read pass's loads: the host page size, at most 32 KiB
   std::vector<int64_t> ctx_len;
@@ -392,6 +394,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.retr_late = c->retr_late;
   a.mgr_gs = c->mgr_gs;
   a.pipe = c->pipe;
+  a.retr_split = c->retr_split;
   a.ka = c->ka;
   a.P_b = c->d_P_lb + (int64_t)l * c->B;
   a.ntok_b = c->d_ntok_lb + (int64_t)l * c->B;
@@ -424,6 +427,7 @@ LayerArgs make_args(spin_ctx* c, int l) {
   a.miss_att = lb.miss_att;
   a.miss_valid = lb.miss_valid;
   a.ready = lb.ready;
+  a.ready_cnt = lb.ready_cnt;
   a.miss_tag = lb.miss_tag;
   a.unit_rows = lb.unit_rows;
   a.unit_ready = lb.unit_ready;
@@ -611,12 +615,16 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
   // two-tile kernel) once the CTA's resident pages are issued
   c->retr_warps = 2;
   c->retr_late = c->G <= 8 ? 4 : 2;
-  if (const char* env = getenv("SPIN_STORE_WARM")) c->store_warm = std::max(0, std::min(8, atoi(env)));
   {
     const long pg = sysconf(_SC_PAGESIZE);
     c->warm_stride = pg >= 4096 ? std::min<int64_t>(pg, kPageBytes) : 4096;
   }
   if (c->flags & SPIN_FLAG_TEST_NO_RETRIEVE) c->retr_warps = c->retr_late = 0;
+  // the first entries of a step's miss list are split in kRetrChunks pieces, about one piece
+  // per retriever warp of the grid that loads from the start: a step with few misses gets
+  // its pages in about one host-link round trip each instead of kRetrChunks
+  c->retr_split = (int)std::min<int64_t>((int64_t)c->B * c->Hkv * c->k,
+                                         (int64_t)std::max(1, c->sm_count) * c->retr_warps / kRetrChunks);
 
   // attention work split: pages per task, about one task per consumer group when pages
   // are few (each task costs a merge and a partial to combine), at most 8
@@ -696,6 +704,7 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     ALLOC(lb.miss_att, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.miss_valid, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.ready, Ul * c->k, "allocating layer scratch");
+    ALLOC(lb.ready_cnt, c->retr_split > 0 ? c->retr_split : 1, "allocating layer scratch");
     ALLOC(lb.miss_tag, Ul * c->k, "allocating layer scratch");
     ALLOC(lb.unit_rows, Ul, "allocating layer scratch");
     ALLOC(lb.unit_ready, Ul, "allocating layer scratch");
@@ -707,6 +716,8 @@ int create_impl(const spin_config* cfg, spin_ctx* c) {
     ALLOC(lb.partials, Ul * (c->n_chunks + c->ka) * c->G * kPartialStride, "allocating layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.n_hit, 0, Ul * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.ready, 0, Ul * c->k * 4), "initialising layer scratch");
+    SPIN_CUDA(nullptr, cudaMemset(lb.ready_cnt, 0, (c->retr_split > 0 ? c->retr_split : 1) * 4),
+              "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.miss_tag, 0, Ul * c->k * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.unit_rows, 0, Ul * 4), "initialising layer scratch");
     SPIN_CUDA(nullptr, cudaMemset(lb.unit_ready, 0, Ul * 4), "initialising layer scratch");

@@ -37,6 +37,7 @@ struct LayerArgs {
   int32_t retr_late;         // further retriever warps that join once the CTA's resident pages are issued
   int32_t mgr_gs;            // threads of one manager group (32, 128, or the CTA's full group)
   int32_t pipe;              // 1: the pipelined kernel (scoring, one manager group and retrieval run at once)
+  int32_t retr_split;        // the first retr_split miss-list entries are copied in kRetrChunks pieces
   const int32_t* P_b;        // [B] selectable partitions of request b in this layer (tail mode: complete ones)
   const int32_t* ntok_b;     // [B] tokens held by those partitions
   const int32_t* tail_n;     // [B] tokens in the request's tail page (tail mode), else nullptr
@@ -68,6 +69,7 @@ struct LayerArgs {
   int32_t* miss_att;         // [U_l * k] ul * ka + attention position of each miss
   int32_t* miss_valid;       // [U_l * k] valid tokens of each miss's page
   int32_t* ready;            // [U_l * k] per miss-list entry: step tag once its page is in HBM
+  uint32_t* ready_cnt;       // [retr_split] pieces of a split entry copied so far (never reset: grows by kRetrChunks a step)
   int32_t* miss_tag;         // [U_l * k] per miss-list entry: step tag once the entry is written
   int32_t* unit_rows;        // [U_l] partitions scored so far in this step (reset by the unit's manager)
   int32_t* unit_ready;       // [U_l] step tag once the unit is managed
@@ -114,6 +116,11 @@ enum : int { kTlStart = 0, kTlScored = 1, kTlManaged = 2, kTlPages = 3, kTlEnd =
 // Bit pattern of a score slot not yet written in this step (a signalling NaN the score
 // arithmetic never produces): the pipelined kernel's managers wait until none is left.
 constexpr uint32_t kScoreEmpty = 0x7FBFFFFFu;
+
+// Pieces of a split miss-list entry (its 32 KB page copied by kRetrChunks warps at once).
+// The first entries of a step are split so that a step with few misses still has every
+// retriever warp loading; the rest are copied a page per warp.
+constexpr int kRetrChunks = 4;
 
 // Device stats slots.
 enum : int {
