@@ -241,7 +241,7 @@ __device__ __noinline__ bool wait_flag(const int* p, int want, bool exact, const
         break;
     }
   }
-  if (ok) fence_acq_rel();
+  if (ok) (void)ld_acquire(p);  // an acquire load, not a fence: nothing earlier to wait for
   return ok;
 }
 
@@ -254,7 +254,7 @@ __device__ __noinline__ int miss_entry(const LayerArgs& a, int m, int tag, int U
   for (uint32_t it = 0; it < (1u << 30); ++it) {
     if (ld_relaxed(a.miss_tag + m) == tag) return 1;
     if (ld_relaxed(a.counters + kCtrManaged) >= U) {
-      fence_acq_rel();
+      (void)ld_acquire(a.counters + kCtrManaged);
       if (m >= ld_relaxed(a.counters + kCtrMiss)) return 0;
       continue;  // every entry below the final count is published before its unit: the tag is there
     }
@@ -826,7 +826,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) dst[c + u * 32 + lane] = r[u];
       }
-      fence_acq_rel();  // each lane's stores of the page before the flag (acq_rel: no full sc fence)
+      // every lane's stores are ordered before lane 0's release by the warp barrier (the
+      // release is cumulative): one GPU-scope ordering point per piece, not one per lane
       __syncwarp();
       if (lane == 0) {
         // a split entry's flag goes up with its last piece: the counter grows by kRetrChunks
@@ -1238,7 +1239,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
   __syncthreads();
   if (tid == 0) {
     if (tl) atomicMax(tl + kTlPages, globaltimer_ns());
-    __threadfence();
+    fence_acq_rel();  // the CTA's partials (ordered before by the block barrier), then the arrival
     atomicAdd(&a.counters[kCtrArrive], 1);
     const int target = (int)gridDim.x * tag;  // the counter grows by gridDim.x every step
     // no early exit on another wait's timeout here: block 0 resets the step's counters only

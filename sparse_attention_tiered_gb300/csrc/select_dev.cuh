@@ -623,6 +623,21 @@ __host__ __device__ inline size_t mgr_smem_layout(int nt, int P_max, int cap, in
   return off;
 }
 
+// Memory-order helpers. A GPU-scope fence waits for the executing thread's earlier
+// accesses, and on an SM whose other warps have host-link loads queued that takes many
+// microseconds: the manager uses as few as its ordering needs.
+__device__ __forceinline__ void fence_rel() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ void st_relaxed_i32(int32_t* p, int32_t v) {
+  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t atom_add_acq_rel_i32(int32_t* p, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Claim a free segment of the shared pool (bitmap, lock free). -1 when exhausted.
 __device__ inline int alloc_segment(const LayerArgs& a, uint32_t hint) {
   const int nwords = (a.S + 31) >> 5;
@@ -633,7 +648,7 @@ __device__ inline int alloc_segment(const LayerArgs& a, uint32_t hint) {
       const int bit = __ffs(~bits) - 1;
       const uint32_t old = atomicOr(&a.seg_bitmap[w], 1u << bit);
       if (!(old & (1u << bit))) {
-        __threadfence();
+        fence_rel();  // the previous owner's writes to the segment come before ours
         return w * 32 + bit;
       }
       bits = old | (1u << bit);
@@ -643,7 +658,7 @@ __device__ inline int alloc_segment(const LayerArgs& a, uint32_t hint) {
 }
 
 __device__ __forceinline__ void release_segment(const LayerArgs& a, int sg) {
-  __threadfence();
+  fence_rel();  // the unit's writes to the segment come before the next owner's
   atomicAnd(&a.seg_bitmap[sg >> 5], ~(1u << (sg & 31)));
 }
 
@@ -651,11 +666,15 @@ __device__ __forceinline__ void st_release_i32(int32_t* p, int32_t v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Publishes unit ul (by one thread, after the group's writes): its ready flag, then the
-// managed count.
-__device__ inline void publish_unit(const LayerArgs& a, int ul, int tag) {
-  __threadfence();
-  st_release_i32(a.unit_ready + ul, tag);
+// Publishes unit ul, by one thread after a barrier of the group that wrote it: the
+// release fence covers every write the barrier ordered before it (the group's), and is
+// followed by the tags of the unit's miss-list entries [mbase, mbase + misses) (entries
+// at or past kmax were never written), the unit's ready flag and the managed count.
+__device__ inline void publish_unit(const LayerArgs& a, int ul, int tag, int mbase = 0, int misses = 0,
+                                    int kmax = 0) {
+  fence_rel();
+  for (int r = 0; r < misses && mbase + r < kmax; ++r) st_relaxed_i32(a.miss_tag + mbase + r, tag);
+  st_relaxed_i32(a.unit_ready + ul, tag);
   atomicAdd(&a.counters[kCtrManaged], 1);
 }
 
@@ -870,8 +889,8 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
         atomicOr(a.err, kErrSegId);
       } else if (sg >= 0) {
         a.seg[(int64_t)sg * kSeg + (p & 63)] = -1;
-        __threadfence();
-        if (atomicSub(&a.seg_live[sg], 1) == 1) {
+        // acq_rel: the last page out of the segment sees every clear before it frees it
+        if (atom_add_acq_rel_i32(&a.seg_live[sg], -1) == 1) {
           sm.dirs[p >> 6] = -1;
           release_segment(a, sg);
         }
@@ -938,11 +957,10 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
     const int rank = -1 - code;
     if (rank >= gs->nfree) {  // cannot happen: the LRU step freed at least `demand` pages
       atomicOr(a.err, kErrInternal);
-      if (mbase + rank < kmax) {  // publish the reserved entry as one the retrievers skip
+      if (mbase + rank < kmax) {  // the reserved entry is published as one the retrievers skip
         a.miss_src[mbase + rank] = -1;
         a.miss_dst[mbase + rank] = -1;
         a.miss_att[mbase + rank] = -1;
-        st_release_i32(a.miss_tag + mbase + rank, tag);
       }
       continue;
     }
@@ -972,7 +990,6 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
     a.miss_att[idx] = ul * a.ka + hits + has_tail + rank;  // misses follow the hits and the tail
     a.miss_valid[idx] = (a.part_valid && in_range) ? (int)a.part_valid[src]
                                                     : ((p == P - 1) ? a.ntok_b[b] - p * kPart : kPart);
-    st_release_i32(a.miss_tag + idx, tag);
   }
   gsync<NT>(bar);
 
@@ -1026,7 +1043,9 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
     if (keff) atomicAdd(&a.stats[kStatSelected], (unsigned long long)keff);
   }
   gsync<NT>(bar);
-  if (gt == 0) publish_unit(a, ul, tag);
+  // one release for the whole unit: the miss-list entries, the attention order and the
+  // page state written above, then the entries' tags and the unit's flag
+  if (gt == 0) publish_unit(a, ul, tag, mbase, misses, kmax);
   (void)kW;
 }
 
