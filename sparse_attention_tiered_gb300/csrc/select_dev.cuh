@@ -424,13 +424,19 @@ __device__ int wide_topk(const float* __restrict__ sc, int P, int keff, int32_t*
     }
   };
   if (in_regs) {
+    // most groups of four hold no key at or above the threshold: the warp skips those
+    const uint32_t kb = b1 << kShift;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int p = 4 * (w * 32 + u * NT + lane);
-      append(p, v4[u].x);
-      append(p + 1, v4[u].y);
-      append(p + 2, v4[u].z);
-      append(p + 3, v4[u].w);
+      const bool any = (p < P && float_key(v4[u].x) >= kb) || (p + 1 < P && float_key(v4[u].y) >= kb) ||
+                       (p + 2 < P && float_key(v4[u].z) >= kb) || (p + 3 < P && float_key(v4[u].w) >= kb);
+      if (__any_sync(0xffffffffu, any)) {
+        append(p, v4[u].x);
+        append(p + 1, v4[u].y);
+        append(p + 2, v4[u].z);
+        append(p + 3, v4[u].w);
+      }
     }
   } else if ((reinterpret_cast<uintptr_t>(sc) & 15) == 0) {
     for (int i0 = w * 32; i0 < n4; i0 += 8 * NT) {
@@ -463,31 +469,29 @@ __device__ int wide_topk(const float* __restrict__ sc, int P, int keff, int32_t*
   }
   gsync<NT>(bar);
   const int n = gs->nlist;
-  // 3. radix over the pairs at b1: bits 19..0 in digits of 8, 8 and 4
+  // 3. radix over the pairs at b1: bits 19..0 in digits of 8, 8 and 4. One shared
+  // histogram (the pairs are few), two of them alternating: warp 0 scans one while the
+  // other warps clear the next, two barriers a pass.
   uint32_t prefix = b1 << kShift, mask = ~0u << kShift;
   int krem = keff - gs->above;
+  uint32_t* hcur = whist;
+  uint32_t* hnxt = whist + 256;
+  for (int i = gt; i < 256; i += NT) hcur[i] = 0;
+  gsync<NT>(bar);
   for (int rb = kShift; rb > 0;) {
     const int digit = rb >= 8 ? 8 : rb;
     const int shift = rb - digit;
     const uint32_t dmask = (1u << digit) - 1u;
-    for (int i = gt; i < kW * 256; i += NT) whist[i] = 0;
-    gsync<NT>(bar);
     for (int i = gt; i < n; i += NT) {
       const uint32_t key = list_k[i];
-      if ((key & mask) == prefix) atomicAdd(&whist[w * 256 + ((key >> shift) & dmask)], 1u);
-    }
-    gsync<NT>(bar);
-    for (int i = gt; i < 256; i += NT) {
-      uint32_t s = 0;
-      for (int ww = 0; ww < kW; ++ww) s += whist[ww * 256 + i];
-      whist[i] = s;
+      if ((key & mask) == prefix) atomicAdd(&hcur[(key >> shift) & dmask], 1u);
     }
     gsync<NT>(bar);
     if (w == 0) {
       int cc[8], ls = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        cc[i] = (int)whist[255 - 8 * lane - i];
+        cc[i] = (int)hcur[255 - 8 * lane - i];
         ls += cc[i];
       }
       int incl = ls;
@@ -509,12 +513,16 @@ __device__ int wide_topk(const float* __restrict__ sc, int P, int keff, int32_t*
           above += cc[i];
         }
       }
+    } else {
+      for (int i = gt - 32; i < 256; i += NT - 32) hnxt[i] = 0;
     }
     gsync<NT>(bar);
     prefix |= (uint32_t)gs->bin << shift;
     mask |= dmask << shift;
     krem -= gs->above;
-    gsync<NT>(bar);
+    uint32_t* h = hcur;
+    hcur = hnxt;
+    hnxt = h;
     rb -= digit;
   }
   const uint32_t T = prefix;  // the k-th largest key; krem = equal keys still to take
@@ -527,13 +535,24 @@ __device__ int wide_topk(const float* __restrict__ sc, int P, int keff, int32_t*
     gs->ncand = 0;
   }
   gsync<NT>(bar);
-  for (int i = gt; i < n; i += NT) {
-    const uint32_t key = list_k[i];
-    if (key > T) {
-      const int j = atomicAdd(&gs->ntaken, 1);
+  for (int i0 = w * 32; i0 < n; i0 += NT) {  // one shared-memory atomic per warp and kind
+    const int i = i0 + lane;
+    const uint32_t key = i < n ? list_k[i] : 0u;
+    const bool above = i < n && key > T, equal = i < n && key == T;
+    const uint32_t mg = __ballot_sync(0xffffffffu, above), me = __ballot_sync(0xffffffffu, equal);
+    int bg = 0, be = 0;
+    if (lane == 0) {
+      if (mg) bg = atomicAdd(&gs->ntaken, __popc(mg));
+      if (me) be = atomicAdd(&gs->ncand, __popc(me));
+    }
+    bg = __shfl_sync(0xffffffffu, bg, 0);
+    be = __shfl_sync(0xffffffffu, be, 0);
+    if (above) {
+      const int j = bg + __popc(mg & lanemask_lt());
       if (j < keff) tmp[j] = list_p[i];
-    } else if (key == T) {
-      const int j = atomicAdd(&gs->ncand, 1);
+    }
+    if (equal) {
+      const int j = be + __popc(me & lanemask_lt());
       if (j < kEqMax) eq_p[j] = list_p[i];
     }
   }
