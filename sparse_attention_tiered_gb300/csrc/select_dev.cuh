@@ -424,18 +424,40 @@ __device__ int wide_topk(const float* __restrict__ sc, int P, int keff, int32_t*
     }
   };
   if (in_regs) {
-    // most groups of four hold no key at or above the threshold: the warp skips those
+    // each lane counts its keys at or above the threshold; one warp scan and one
+    // shared-memory atomic a warp place them, and each lane writes its own
     const uint32_t kb = b1 << kShift;
+    int cnt = 0;
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int p = 4 * (w * 32 + u * NT + lane);
-      const bool any = (p < P && float_key(v4[u].x) >= kb) || (p + 1 < P && float_key(v4[u].y) >= kb) ||
-                       (p + 2 < P && float_key(v4[u].z) >= kb) || (p + 3 < P && float_key(v4[u].w) >= kb);
-      if (__any_sync(0xffffffffu, any)) {
-        append(p, v4[u].x);
-        append(p + 1, v4[u].y);
-        append(p + 2, v4[u].z);
-        append(p + 3, v4[u].w);
+      cnt += (p < P && float_key(v4[u].x) >= kb) + (p + 1 < P && float_key(v4[u].y) >= kb) +
+             (p + 2 < P && float_key(v4[u].z) >= kb) + (p + 3 < P && float_key(v4[u].w) >= kb);
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+    int base = 0;
+    if (lane == 0 && wtot) base = atomicAdd(&gs->nlist, wtot);
+    base = __shfl_sync(0xffffffffu, base, 0) + incl - cnt;
+    if (cnt) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int p = 4 * (w * 32 + u * NT + lane);
+        const float vv[4] = {v4[u].x, v4[u].y, v4[u].z, v4[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t key = float_key(vv[c]);
+          if (p + c < P && key >= kb) {
+            list_p[base] = p + c;
+            list_k[base] = key;
+            ++base;
+          }
+        }
       }
     }
   } else if ((reinterpret_cast<uintptr_t>(sc) & 15) == 0) {
@@ -718,8 +740,8 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
   const int64_t unit = a.unit_base + ul;
   if (sc_reset)  // the next step's buffer: every slot it will write starts empty
     for (int p = gt; p < P; p += NT) sc_reset[p] = __uint_as_float(kScoreEmpty);
-  const bool dead = (*((volatile uint32_t*)a.err) & (kErrCapacity | kErrInternal | kErrSelCount | kErrSegId | kErrIndex)) != 0;
-  bool ok = !dead;
+  // the device error word: read now, used once the unit's loads below are on their way
+  const uint32_t err0 = *((volatile uint32_t*)a.err);
   if (a.q_src != a.q) {
     // queries read from host memory: the unit's G rows go to HBM for the attention's TMA
     // loads (published with the unit)
@@ -728,8 +750,6 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
     uint2* dst = reinterpret_cast<uint2*>(const_cast<uint16_t*>(a.q) + q0);
     for (int i = gt; i < a.G * (kD / 4); i += NT) dst[i] = src[i];
   }
-  if (dead && a.hist12)
-    for (int i = gt; i < kHistBins; i += NT) a.hist12[(int64_t)ul * kHistBins + i] = 0;
 
   // The unit's page state does not depend on the selection: its loads go out now, into
   // registers, and land in shared memory after the top-k (when it fits kPf entries a thread).
@@ -739,7 +759,7 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
   const int32_t* g_dir = a.dir + unit * a.D;
   const bool pf = cap <= kPf * NT && a.D <= 2 * NT;
   int32_t pf_sp[kPf], pf_lu[kPf], pf_dir[2];
-  if (pf && ok) {
+  if (pf) {
 #pragma unroll
     for (int i = 0; i < kPf; ++i) {
       const int sl = gt + i * NT;
@@ -753,17 +773,20 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
   // ---------------- top-k ----------------
   int wide_done = 0;
   if constexpr (NT >= 256) {
-    if (ok && a.hist12 != nullptr) {
-      // the list lives in the keys' shared memory: P_max / 2 (partition, key) pairs
+    if (a.hist12 != nullptr) {
+      // the list lives in the keys' shared memory: P_max / 2 (partition, key) pairs. Run
+      // whatever the error word says: it also clears the unit's histogram for the next step.
       const int lmax = a.P_max / 2;
       wide_done = wide_topk<NT>(sc, P, keff, a.hist12 + (int64_t)ul * kHistBins,
                                 reinterpret_cast<int32_t*>(sm.keys), sm.keys + lmax, lmax, sm.flist, sm.whist, gs,
                                 bar, gt, sm.sel);
-      if (wide_done < 0) {
-        ok = false;
-        if (gt == 0) atomicOr(a.err, kErrSelCount);
-      }
     }
+  }
+  const bool dead = (err0 & (kErrCapacity | kErrInternal | kErrSelCount | kErrSegId | kErrIndex)) != 0;
+  bool ok = !dead;
+  if (ok && wide_done < 0) {
+    ok = false;
+    if (gt == 0) atomicOr(a.err, kErrSelCount);
   }
   if (ok && wide_done == 0) {
     for (int p0 = gt; p0 < P; p0 += 8 * NT) {
