@@ -679,19 +679,29 @@ __device__ __forceinline__ int32_t atom_add_acq_rel_i32(int32_t* p, int32_t v) {
   return old;
 }
 
-// Claim a free segment of the shared pool (bitmap, lock free). -1 when exhausted.
+__device__ __forceinline__ uint32_t atom_or_acquire(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acquire.gpu.global.or.b32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Claim a free segment of the shared pool (bitmap, lock free). -1 when exhausted. The
+// first try sets the hinted bit of the hinted word (one round trip when it is free); the
+// bits the atomic returns pick the next tries. Acquire: the previous owner's writes to
+// the segment come before ours (bits past S are set for good, so they are never taken).
 __device__ inline int alloc_segment(const LayerArgs& a, uint32_t hint) {
   const int nwords = (a.S + 31) >> 5;
+  const int w0 = (int)(hint % (uint32_t)nwords);
+  const uint32_t m0 = 1u << ((hint / (uint32_t)nwords) & 31u);
+  uint32_t bits = atom_or_acquire(&a.seg_bitmap[w0], m0);
+  if (!(bits & m0)) return w0 * 32 + (__ffs(m0) - 1);
   for (int i = 0; i < nwords; ++i) {
-    const int w = (int)((hint + (uint32_t)i) % (uint32_t)nwords);
-    uint32_t bits = *((volatile uint32_t*)&a.seg_bitmap[w]);
+    const int w = (w0 + i) % nwords;
+    if (i > 0) bits = *((volatile uint32_t*)&a.seg_bitmap[w]);
     for (int tries = 0; tries < 33 && bits != 0xffffffffu; ++tries) {
       const int bit = __ffs(~bits) - 1;
-      const uint32_t old = atomicOr(&a.seg_bitmap[w], 1u << bit);
-      if (!(old & (1u << bit))) {
-        fence_rel();  // the previous owner's writes to the segment come before ours
-        return w * 32 + bit;
-      }
+      const uint32_t old = atom_or_acquire(&a.seg_bitmap[w], 1u << bit);
+      if (!(old & (1u << bit))) return w * 32 + bit;
       bits = old | (1u << bit);
     }
   }
