@@ -258,8 +258,8 @@ int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out
 
 /* The same step with host buffers: q_host [batch][q_heads][128] bf16 and
  * out_host [batch][q_heads][128] fp32. Pinned, device-mapped buffers (cudaHostAlloc'd or
- * registered) are used in place: the kernel reads q_host (8-byte aligned) and writes
- * out_host (16-byte aligned) over the host link. Other buffers go through HBM with
+ * registered) are used in place: the kernel copies q_host (8-byte aligned) into device
+ * memory at its start and writes out_host (16-byte aligned), both over the host link. Other buffers go through HBM with
  * host<->device copies enqueued on `stream` around the step. out_host is valid once the
  * stream has reached the end of the step, and neither buffer may be reused before then. */
 int spin_decode_step_host(spin_ctx* ctx, int32_t layer, const uint16_t* q_host, float* out_host,

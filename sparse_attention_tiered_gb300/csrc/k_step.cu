@@ -245,6 +245,43 @@ __device__ __noinline__ bool wait_flag(const int* p, int want, bool exact, const
   return ok;
 }
 
+// Zero-copy queries: staging warp sw of nsw copies the query rows of units sw, sw + nsw, ...
+// from host memory into q (HBM), one 256-byte row per warp access, and counts them in
+// kCtrQStaged with one release (the warp barrier orders every lane's stores before it).
+__device__ __noinline__ void stage_queries(const LayerArgs& a, int sw, int nsw, int lane) {
+  const int U = a.B * a.Hkv;
+  int done = 0;
+  for (int u = sw; u < U; u += nsw) {
+    const int64_t q0 = ((int64_t)(u / a.Hkv) * a.Hq + (int64_t)(u % a.Hkv) * a.G) * kD;
+    const uint2* src = reinterpret_cast<const uint2*>(a.q_src + q0);
+    uint2* dst = reinterpret_cast<uint2*>(const_cast<uint16_t*>(a.q) + q0);
+    for (int g0 = 0; g0 < a.G; g0 += 4) {
+      uint2 v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (g0 + i < a.G) v[i] = src[(g0 + i) * (kD / 4) + lane];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (g0 + i < a.G) dst[(g0 + i) * (kD / 4) + lane] = v[i];
+    }
+    ++done;
+  }
+  __syncwarp();
+  if (lane == 0 && done) red_release_add(a.counters + kCtrQStaged, done);
+}
+
+// Zero-copy queries: returns once every unit's rows are in q (bounded; a wait that runs
+// out sets the time-out bit, and the step's results are not used).
+__device__ __forceinline__ void await_queries(const LayerArgs& a, int lane) {
+  if (a.q_src == a.q) return;
+  int ok = 1;
+  if (lane == 0) ok = wait_flag(a.counters + kCtrQStaged, a.B * a.Hkv, false, a.err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok && lane == 0) atomicOr(a.err, kErrTimeout);
+  __syncwarp();
+  (void)ld_acquire(a.counters + kCtrQStaged);
+}
+
 // State of miss-list entry m of this step: 1 = written (its fields may be read after an
 // acquire), 0 = past the end of the step's final list, -1 = the bounded wait ran out.
 // The list is final once every unit of the layer is managed.
@@ -557,7 +594,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
         locate(j, b, h, p0, n);
         float4 cur[sel::kRowsPerBatch], nxt[sel::kRowsPerBatch];
         sel::load_rows(cur, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, p0) * kD), n, lane);
-        float4 qv = sel::qsum_lane(a.q_src + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
+        await_queries(a, lane);
+        float4 qv = sel::qsum_lane(a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
         for (;;) {
           const int j2 = j + SWp;
           const bool more = j2 < nbatch;
@@ -569,7 +607,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
           const float x = sel::score_batch(cur, qv, lane);
           if (lane < n) sc_cur[(int64_t)(b * a.Hkv + h) * a.P_max + p0 + lane] = x;
           if (!more) break;
-          if (b2 != b || h2 != h) qv = sel::qsum_lane(a.q_src + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
+          if (b2 != b || h2 != h) qv = sel::qsum_lane(a.q + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
           j = j2;
           b = b2;
           h = h2;
@@ -630,6 +668,12 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
         sel::manage_unit<GS>(a, ul, t, tag, ms, bar, gt, sc, sc_next + (int64_t)ul * a.P_max);
         if (tl && gt == 0) atomicMax(tl + kTlManaged, globaltimer_ns());
       }
+    } else if (a.q_src != a.q) {
+      // the retriever warps copy the queries from host memory before their first claim
+      constexpr int kStageWarps = kWarps - (NC + NG + kMgrWarps);
+      static_assert(kStageWarps > 0, "the pipelined kernel keeps retriever warps");
+      stage_queries(a, (int)blockIdx.x * kStageWarps + warp - (NC + NG + kMgrWarps), (int)gridDim.x * kStageWarps,
+                    lane);
     }
   } else {
   // ------------------------------ A. scoring ------------------------------
@@ -659,6 +703,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     __syncthreads();
     const int64_t R = s_pre[a.B];
     const int64_t TW = (int64_t)gridDim.x * kWarps, gw = (int64_t)blockIdx.x * kWarps + warp;
+    if (a.q_src != a.q) stage_queries(a, (int)gw, (int)TW, lane);
     int64_t r = R * gw / TW;
     const int64_t r_end = R * (gw + 1) / TW;
     if (r < r_end) {
@@ -674,7 +719,8 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       int n = (int)min((int64_t)min(sel::kRowsPerBatch, Pb - p), r_end - r);
       float4 cur[sel::kRowsPerBatch], nxt[sel::kRowsPerBatch];
       sel::load_rows(cur, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, p) * kD), n, lane);
-      float4 qv = sel::qsum_lane(a.q_src + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
+      await_queries(a, lane);
+      float4 qv = sel::qsum_lane(a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
       int counted = 0;
       for (;;) {
         // the next batch: the rest of this unit, else the start of the next non-empty unit
@@ -708,7 +754,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
           counted = 0;
         }
         if (!more) break;
-        if (leave) qv = sel::qsum_lane(a.q_src + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
+        if (leave) qv = sel::qsum_lane(a.q + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
         r = r2;
         b = b2;
         h = h2;
@@ -852,6 +898,10 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     // the ring barriers and issues the copies.
     const int g = warp - NC;
     const uint32_t qbytes = (uint32_t)a.G * kD * 2;
+    // zero-copy queries: the rows the TMA stages were copied into q with generic stores in
+    // this kernel; after the acquire, one proxy fence orders them before every later bulk copy
+    await_queries(a, lane);
+    if (lane == 0 && a.q_src != a.q) asm volatile("fence.proxy.async.global;" ::: "memory");
     bool ok = true, done = false;
     if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
     // Descriptors of hit task T (lane j: its page j) once the task's unit is managed;
@@ -872,9 +922,6 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       if (r <= 0) return false;
       __syncwarp();
       (void)ld_acquire(a.unit_ready + tu);
-      // the unit's query rows may have been staged with generic stores in this kernel: the
-      // TMA bulk copy that reads them follows a proxy fence
-      if (lane == 0 && a.q_src != a.q) asm volatile("fence.proxy.async.global;" ::: "memory");
       nhit = __ldcg(a.n_hit + tu);
       const bool in = lane < a.ppt && j0 + lane < a.ka;
       slot = in ? __ldcg(a.att_slot + (int64_t)tu * a.ka + j0 + lane) : 0;
@@ -1252,6 +1299,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       a.counters[kCtrRetrieve] = 0;
       a.counters[kCtrManage] = 0;
       a.counters[kCtrManaged] = 0;
+      a.counters[kCtrQStaged] = 0;
       a.counters[kCtrStep] += 1;
     }
   }

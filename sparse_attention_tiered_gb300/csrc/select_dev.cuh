@@ -45,11 +45,12 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // ---------------------------------------------------------------------------
 constexpr int kRowsPerBatch = 8;  // partitions scored by one warp at a time (8 loads in flight per lane)
 
-// q: the group's query rows [G][128] bf16 (8-byte aligned rows).
+// q: the group's query rows [G][128] bf16 (8-byte aligned rows). Coherent loads: the rows
+// may have been copied into place earlier in the same kernel.
 __device__ __forceinline__ float4 qsum_lane(const uint16_t* __restrict__ q, int G, int lane) {
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int g = 0; g < G; ++g) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(q + (int64_t)g * kD) + lane);
+    const uint2 v = __ldcg(reinterpret_cast<const uint2*>(q + (int64_t)g * kD) + lane);
     s.x += bf16f(v.x & 0xffffu);
     s.y += bf16f(v.x >> 16);
     s.z += bf16f(v.y & 0xffffu);
@@ -752,14 +753,6 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
     for (int p = gt; p < P; p += NT) sc_reset[p] = __uint_as_float(kScoreEmpty);
   // the device error word: read now, used once the unit's loads below are on their way
   const uint32_t err0 = *((volatile uint32_t*)a.err);
-  if (a.q_src != a.q) {
-    // queries read from host memory: the unit's G rows go to HBM for the attention's TMA
-    // loads (published with the unit)
-    const int64_t q0 = ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD;
-    const uint2* src = reinterpret_cast<const uint2*>(a.q_src + q0);
-    uint2* dst = reinterpret_cast<uint2*>(const_cast<uint16_t*>(a.q) + q0);
-    for (int i = gt; i < a.G * (kD / 4); i += NT) dst[i] = src[i];
-  }
 
   // The unit's page state does not depend on the selection: its loads go out now, into
   // registers, and land in shared memory after the top-k (when it fits kPf entries a thread).

@@ -1083,9 +1083,9 @@ int spin_decode_step_host(spin_ctx* c, int32_t layer, const uint16_t* q_host, fl
     if ((e = dalloc(c, &lb.out_stage, nq)) != cudaSuccess) return cuda_fail(c, e, "allocating the output buffer");
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Pinned, device-mapped buffers are used in place: the kernel reads q over the host link
-  // (each unit's manager copies the unit's rows into HBM for the attention) and the combine
-  // writes out into host memory. A copy-engine transfer between two steps costs 11-17 us on
+  // Pinned, device-mapped buffers are used in place: the kernel first copies q over the host
+  // link into HBM (idle warps, one release count), and the combine writes out into host
+  // memory. A copy-engine transfer between two steps costs 11-17 us on
   // GB300 whatever its size; the zero-copy reads and writes cost a few. Pageable or
   // unaligned buffers go through HBM with cudaMemcpyAsync.
   const uint16_t* q_dev_src = static_cast<const uint16_t*>(mapped_host(q_host, 8));

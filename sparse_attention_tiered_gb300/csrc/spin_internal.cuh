@@ -84,8 +84,8 @@ struct LayerArgs {
   unsigned long long* timeline; // [5] globaltimer stamps of this call (stage timing), else nullptr
   uint32_t* err;             // device error word
   const uint16_t* q;         // [B][Hq][128] bf16 (HBM): the query rows the attention stages through TMA
-  const uint16_t* q_src;     // the queries the scores read: q itself, or pinned host memory (zero copy), in
-                             // which case each unit's manager first copies the unit's rows into q
+  const uint16_t* q_src;     // the step's queries: q itself, or pinned host memory (zero copy), in which
+                             // case the kernel first copies every unit's rows into q (counted in kCtrQStaged)
   float* out;                // [B][Hq][128] fp32 (device)
 };
 
@@ -105,7 +105,8 @@ enum : int {
   kCtrArrive = 5,    // CTAs done with their pages (grows by the grid size every step)
   kCtrManage = 6,    // units claimed by manager groups
   kCtrManaged = 7,   // units managed and published
-  kNumCtr = 8
+  kCtrQStaged = 8,   // units whose query rows were copied from host memory into q (zero-copy queries)
+  kNumCtr = 9
 };
 
 // Stage stamps of one timed decode-step call (globaltimer ns): first CTA start (stored
