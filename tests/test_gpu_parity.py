@@ -126,17 +126,22 @@ def test_resident_pages_byte_exact():
         ls.close()
 
 
-def test_host_buffer_entry_point_matches_device():
+@pytest.mark.parametrize("variant", ["pipelined", "phased", "phased_g16"])
+def test_host_buffer_entry_point_matches_device(variant):
     """spin_decode_step_host gives the device entry point's bytes whether its buffers are
-    mapped pinned memory (used in place by the kernels), pageable memory, or pinned memory
-    at an offset that is not 16-byte aligned (both copied through HBM)."""
-    w = W.Workload("hostep", B=2, L=2, Hq=10, Hkv=2, ctx_len=[2048, 1500], topk=6, buf_mult=2,
+    mapped pinned memory (the kernel copies q into HBM at its start and writes out in
+    place), pageable memory, or pinned memory at an offset that is not 16-byte aligned
+    (both copied through HBM); in both kernel variants and with two 8-head tiles."""
+    from sparse_attention_tiered_gb300._binding import SPIN_FLAG_PHASED
+    hq = 32 if variant == "phased_g16" else 10
+    w = W.Workload("hostep", B=2, L=2, Hq=hq, Hkv=2, ctx_len=[2048, 1500], topk=6, buf_mult=2,
                    drift_a=0.9, drift_c=0.1, steps=5, seed=23)
+    flags = SPIN_FLAG_PHASED if variant == "phased" else 0
     from sparse_attention_tiered_gb300 import SpinContext
     n = w.B * w.Hq * 128
     results = {}
     for mode in ("device", "pinned", "pageable", "pinned_unaligned"):
-        with SpinContext.for_workload(w) as ctx:
+        with SpinContext.for_workload(w, flags=flags) as ctx:
             for l in range(w.L):
                 for b in range(w.B):
                     k, v = w.request_kv(l, b)
