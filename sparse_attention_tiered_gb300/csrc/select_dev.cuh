@@ -384,13 +384,24 @@ __device__ int wide_topk(const float* __restrict__ sc, int P, int keff, int32_t*
     }
   }
   // 1. the threshold value of the top 12 bits
+  // thread gt holds the kPer bins below kHistBins - kPer * gt (c[0] the highest), read and
+  // cleared with 16-byte accesses
+  static_assert(kPer % 4 == 0, "whole int4 runs of bins per thread");
   int c[kPer], lsum = 0;
+  {
+    int4* h4 = reinterpret_cast<int4*>(hist12 + kHistBins - kPer * (gt + 1));
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int bin = kHistBins - 1 - kPer * gt - i;
-    c[i] = __ldcg(hist12 + bin);
-    hist12[bin] = 0;
-    lsum += c[i];
+    for (int q = 0; q < kPer / 4; ++q) {
+      const int4 x = __ldcg(h4 + q);
+      c[kPer - 1 - 4 * q] = x.x;
+      c[kPer - 2 - 4 * q] = x.y;
+      c[kPer - 3 - 4 * q] = x.z;
+      c[kPer - 4 - 4 * q] = x.w;
+    }
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) h4[q] = make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) lsum += c[i];
   }
   int tot;
   const int excl = group_exclusive_scan<NT>(lsum, &tot, gs, gt, bar);
@@ -761,14 +772,24 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
   int32_t* g_lu = a.last_use + unit * cap;
   const int32_t* g_dir = a.dir + unit * a.D;
   const bool pf = cap <= kPf * NT && a.D <= 2 * NT;
+  // 16-byte loads when the rows are 16-byte aligned: thread gt holds slots 4gt .. 4gt+3
+  const bool pf4 = pf && (cap & 3) == 0;
   int32_t pf_sp[kPf], pf_lu[kPf], pf_dir[2];
-  if (pf) {
+  if (pf4) {
+    const int4 z4 = make_int4(-1, -1, -1, -1), l4 = make_int4(0, 0, 0, 0);
+    const int4 v = 4 * gt < cap ? reinterpret_cast<const int4*>(g_sp)[gt] : z4;
+    const int4 w = 4 * gt < cap ? reinterpret_cast<const int4*>(g_lu)[gt] : l4;
+    pf_sp[0] = v.x, pf_sp[1] = v.y, pf_sp[2] = v.z, pf_sp[3] = v.w;
+    pf_lu[0] = w.x, pf_lu[1] = w.y, pf_lu[2] = w.z, pf_lu[3] = w.w;
+  } else if (pf) {
 #pragma unroll
     for (int i = 0; i < kPf; ++i) {
       const int sl = gt + i * NT;
       pf_sp[i] = sl < cap ? g_sp[sl] : -1;
       pf_lu[i] = sl < cap ? g_lu[sl] : 0;
     }
+  }
+  if (pf) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) pf_dir[i] = gt + i * NT < a.D ? g_dir[gt + i * NT] : -1;
   }
@@ -829,7 +850,7 @@ __device__ void manage_unit(const LayerArgs& a, int ul, int t, int tag, const Mg
   if (pf) {
 #pragma unroll
     for (int i = 0; i < kPf; ++i) {
-      const int sl = gt + i * NT;
+      const int sl = pf4 ? 4 * gt + i : gt + i * NT;
       if (sl < cap) {
         sm.sp[sl] = pf_sp[i];
         sm.lu[sl] = pf_lu[i];
