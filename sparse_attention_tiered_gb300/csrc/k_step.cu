@@ -595,7 +595,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
         float4 cur[sel::kRowsPerBatch], nxt[sel::kRowsPerBatch];
         sel::load_rows(cur, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, p0) * kD), n, lane);
         await_queries(a, lane);
-        float4 qv = sel::qsum_lane(a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
+        float4 qv = sel::qsum_lane(a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane, a.q_src != a.q);
         for (;;) {
           const int j2 = j + SWp;
           const bool more = j2 < nbatch;
@@ -607,7 +607,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
           const float x = sel::score_batch(cur, qv, lane);
           if (lane < n) sc_cur[(int64_t)(b * a.Hkv + h) * a.P_max + p0 + lane] = x;
           if (!more) break;
-          if (b2 != b || h2 != h) qv = sel::qsum_lane(a.q + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
+          if (b2 != b || h2 != h) qv = sel::qsum_lane(a.q + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane, a.q_src != a.q);
           j = j2;
           b = b2;
           h = h2;
@@ -720,7 +720,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
       float4 cur[sel::kRowsPerBatch], nxt[sel::kRowsPerBatch];
       sel::load_rows(cur, reinterpret_cast<const float4*>(a.summ + host_page_index(a, b, h, p) * kD), n, lane);
       await_queries(a, lane);
-      float4 qv = sel::qsum_lane(a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane);
+      float4 qv = sel::qsum_lane(a.q + ((int64_t)b * a.Hq + (int64_t)h * a.G) * kD, a.G, lane, a.q_src != a.q);
       int counted = 0;
       for (;;) {
         // the next batch: the rest of this unit, else the start of the next non-empty unit
@@ -754,7 +754,7 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
           counted = 0;
         }
         if (!more) break;
-        if (leave) qv = sel::qsum_lane(a.q + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane);
+        if (leave) qv = sel::qsum_lane(a.q + ((int64_t)b2 * a.Hq + (int64_t)h2 * a.G) * kD, a.G, lane, a.q_src != a.q);
         r = r2;
         b = b2;
         h = h2;

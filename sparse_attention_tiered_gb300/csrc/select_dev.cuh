@@ -45,12 +45,14 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // ---------------------------------------------------------------------------
 constexpr int kRowsPerBatch = 8;  // partitions scored by one warp at a time (8 loads in flight per lane)
 
-// q: the group's query rows [G][128] bf16 (8-byte aligned rows). Coherent loads: the rows
-// may have been copied into place earlier in the same kernel.
-__device__ __forceinline__ float4 qsum_lane(const uint16_t* __restrict__ q, int G, int lane) {
+// q: the group's query rows [G][128] bf16 (8-byte aligned rows). `staged`: the rows were
+// copied into place earlier in the same kernel, so they are read with coherent loads (else
+// through the read-only cache).
+__device__ __forceinline__ float4 qsum_lane(const uint16_t* __restrict__ q, int G, int lane, bool staged = false) {
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int g = 0; g < G; ++g) {
-    const uint2 v = __ldcg(reinterpret_cast<const uint2*>(q + (int64_t)g * kD) + lane);
+    const uint2* r = reinterpret_cast<const uint2*>(q + (int64_t)g * kD) + lane;
+    const uint2 v = staged ? __ldcg(r) : __ldg(r);
     s.x += bf16f(v.x & 0xffffu);
     s.y += bf16f(v.x >> 16);
     s.z += bf16f(v.y & 0xffffu);
