@@ -551,6 +551,9 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
     const size_t gbytes = sel::mgr_smem_layout(GS, a.P_max, a.cap, a.k, a.D, nullptr, nullptr);
     uint8_t* mreg = sm.region + (size_t)kSt * kStageBytes;
     int* s_pre = reinterpret_cast<int*>(mreg + kMgrGroups * gbytes);  // [B + 1] batches before request b
+    // zero-copy queries: every warp of the grid copies at most a few units' rows first
+    if (a.q_src != a.q)
+      stage_queries(a, (int)blockIdx.x * kWarps + warp, (int)gridDim.x * kWarps, lane);
     if (warp == 0) {
       int run = 0;
       for (int b0 = 0; b0 < a.B; b0 += 32) {
@@ -668,12 +671,6 @@ decode_step_kernel(const __grid_constant__ CUtensorMap tmap, LayerArgs a, int n_
         sel::manage_unit<GS>(a, ul, t, tag, ms, bar, gt, sc, sc_next + (int64_t)ul * a.P_max);
         if (tl && gt == 0) atomicMax(tl + kTlManaged, globaltimer_ns());
       }
-    } else if (a.q_src != a.q) {
-      // the retriever warps copy the queries from host memory before their first claim
-      constexpr int kStageWarps = kWarps - (NC + NG + kMgrWarps);
-      static_assert(kStageWarps > 0, "the pipelined kernel keeps retriever warps");
-      stage_queries(a, (int)blockIdx.x * kStageWarps + warp - (NC + NG + kMgrWarps), (int)gridDim.x * kStageWarps,
-                    lane);
     }
   } else {
   // ------------------------------ A. scoring ------------------------------
