@@ -9,30 +9,42 @@
 // gist.science/pt section 2A-2C). The pages give no kernel design; everything below
 // is this library's.
 //
-// The kernel is cooperative (every CTA is resident, one per SM) and runs three
-// phases per CTA:
-//   A. scoring: every warp of the grid takes items of 16 partitions in unit-major
-//      order, writes their fp32 scores and adds the rows to the unit's counter;
-//   B. managing: groups of GS threads claim units in order; a group waits until its
-//      unit's rows are all scored, runs top-k and the page manager on it (shared
-//      memory overlaying the ring of phase C), appends the unit's misses to the
-//      step's miss list (each entry published with the step tag) and publishes the
-//      unit (its ready flag);
-//   C. retrieval and attention, per CTA once its groups are done:
-//      * retriever warps walk the miss list as entries appear (host page -> HBM
-//        slot, 16-byte zero-copy loads over the host link) and publish each copied
-//        page with a release store of the step tag into its ready flag; two start
-//        at once, the others join when the CTA's resident pages have all been issued;
-//      * two consumer groups of four warps take alternate stages of a 6-stage
-//        shared-memory ring guarded by mbarriers, so two pages are in the math at once;
+// The kernel is cooperative (every CTA is resident, one per SM). With zero-copy
+// queries (pinned host memory) every warp first copies a few units' query rows into
+// HBM and counts them with one release; scorers and producers acquire that count. Its
+// work, per CTA:
+//   A. scoring: fp32 scores of 8-row batches of partition summaries, written to this
+//      step's score buffer (two buffers, alternating by step);
+//   B. managing: groups of GS threads claim units in order; once a unit's scores are
+//      all in, a group runs its top-k and the page manager, reserves the unit's entries
+//      in the step's miss list, writes them, the attention order and the page state
+//      with plain stores, and publishes them with one release fence followed by the
+//      entries' tags and the unit's ready flag;
+//   C. retrieval and attention:
+//      * retriever warps walk the miss list as entries appear (host page -> HBM slot,
+//        16-byte zero-copy loads over the host link); the first entries of a step are
+//        copied in four pieces by four warps; a page's (last piece's) lane 0 raises its
+//        ready flag with one release, the warp barrier ordering its lanes' stores;
+//      * two consumer groups of four warps take alternate stages of a shared-memory
+//        ring guarded by mbarriers, so two pages are in the math at once;
 //      * each consumer group has a producer warp that stages its pages through TMA:
 //        first resident pages (hits) in tasks of up to `ppt` pages of one unit (after
 //        the unit's ready flag), then retrieved pages in miss-list order, each after
 //        an acquire of its ready flag.
+// Two variants. Pipelined (PIPE): A, B and C run at once in different warps of every
+// CTA; scoring batches are dealt round-robin in unit-major order so units complete one
+// after another, and a manager group starts on a unit when no slot of its score row
+// still holds the empty-slot sentinel (and sets the unit's slots of the other buffer
+// back to it). Phased: A over contiguous row ranges (a unit's row counter, added with a
+// release as a warp leaves the unit; wide units also count their keys' top 12 bits),
+// then B in the CTA's manager groups overlaying the ring, then C.
 // So retrieval starts as soon as the first units are managed, the attention over the
 // hits (HBM bound) hides under the retrieval (host-link bound) and each retrieved page
 // is attended as soon as it lands (and from L2). When every CTA is done with its
 // pages (an arrival counter), every consumer warp combines (unit, query head) pairs.
+// Memory ordering uses as few GPU-scope ordering points as the protocol needs: a fence
+// waits for the thread's earlier accesses, which on an SM with host-link loads queued
+// takes many microseconds; polls end with one acquire load.
 //
 // Attention data layout. A page (32 KiB) holds K[64][128] then V[64][128] bf16.
 // A TMA tensor map views the whole HBM pool as a 2-D bf16 tensor of 128 columns

@@ -747,8 +747,8 @@ __device__ inline void publish_unit(const LayerArgs& a, int ul, int tag, int mba
 // step's buffer). sc_reset (the pipelined kernel): the unit's slots in the other buffer,
 // set back to kScoreEmpty for the next step.
 // Writes the selection, slots, attention order, page state, two-level table, stats and
-// this step's miss-list entries (each published with its tag in miss_tag), then
-// publishes the unit (unit_ready = tag) and counts it in kCtrManaged. A unit whose
+// this step's miss-list entries, then (one thread, one release fence) the entries' tags
+// in miss_tag, the unit's flag (unit_ready = tag) and its count in kCtrManaged. A unit whose
 // page state can no longer be trusted (device error word) or whose top-k failed is
 // published with nothing selected.
 template <int NT>
