@@ -554,6 +554,14 @@ def test_wide_unit_exact_ties_candidate_and_list_paths():
     _wide_ties_run(P=5000, npat=50, scale_spread=12, topk=64, steps=4, seed=61)
 
 
+@pytest.mark.parametrize("P,npat,topk", [(512, 20, 32), (300, 3, 20), (512, 1, 32), (130, 7, 32)])
+def test_small_unit_exact_ties(P, npat, topk):
+    """Small units (P <= 512, k <= 32, the manager groups of 128 threads): exact score
+    ties within and across warps' slices of the keys, resolved to the lowest partitions,
+    GPU against the oracle every step."""
+    _wide_ties_run(P=P, npat=npat, scale_spread=4, topk=topk, steps=3, seed=71 + P)
+
+
 def test_wide_unit_all_equal_scores_fallbacks():
     """P > 4096, every partition identical: more tied keys than either list holds, so the
     full-scan radix passes and the warp-scan compaction run; partitions 0..k-1 win."""
