@@ -178,7 +178,9 @@ typedef struct spin_state_view {
   float* scores;       /* [U][Pmax] fp32 scores of the last step (entries >= P_b undefined) */
 } spin_state_view;
 
-/* Create a context: validates cfg, allocates the pinned host page store
+/* Create a context ([XT] §1 and Figure 3: the state the five operations share; [XT] §2
+ * and [GS] §2B: per-head mandatory + buffer pages, cap = buf_mult * topk; [XT] §3 and
+ * Figure 6: the two-level table): validates cfg, allocates the pinned host page store
  * (sum_b S_b * L * Hkv pages, S_b = ceil(ctx_len[b]/64); ceil((ctx_len[b] +
  * append_tokens)/64) in tail mode; max_partitions with variable partitions), the
  * HBM page pool (B*L*Hkv*cap pages, plus one tail page per unit in tail mode), the
@@ -259,14 +261,18 @@ int spin_decode_step(spin_ctx* ctx, int32_t layer, const uint16_t* q, float* out
 /* The same step with host buffers: q_host [batch][q_heads][128] bf16 and
  * out_host [batch][q_heads][128] fp32. Pinned, device-mapped buffers (cudaHostAlloc'd or
  * registered) are used in place: the kernel copies q_host (8-byte aligned) into device
- * memory at its start and writes out_host (16-byte aligned), both over the host link. Other buffers go through HBM with
- * host<->device copies enqueued on `stream` around the step. out_host is valid once the
+ * memory at its start and writes out_host (16-byte aligned), both over the host link.
+ * Other buffers go through HBM with host<->device copies enqueued on `stream` around
+ * the step. out_host is valid once the
  * stream has reached the end of the step, and neither buffer may be reused before then. */
 int spin_decode_step_host(spin_ctx* ctx, int32_t layer, const uint16_t* q_host, float* out_host,
                           spin_stream_t stream);
 
-/* Synchronises the context's device work and fills *out. Returns the device
- * error status if a kernel reported one. */
+/* Synchronises the context's device work and fills *out: hits, misses, evictions and
+ * LRU rounds of the bucketed LRU ([XT] §2 and Figure 5; [GS] §2B), bytes selected and
+ * retrieved, and the metadata bytes of the two-level table next to a flat table of the
+ * worst-case logical space ([XT] §3 and Figure 6, and its "性能评估" metadata figure).
+ * Returns the device error status if a kernel reported one. */
 int spin_stats(spin_ctx* ctx, spin_stats_t* out);
 
 /* Synchronises, then copies the page state and last-step selection of `layer`
