@@ -758,7 +758,10 @@ def bench_spin(args):
                          "hbm": {"achieved": hbm_achieved, "peak": hbm_gbs, "frac": hbm_achieved / hbm_gbs},
                          "host_link": {"achieved": host_achieved, "peak": host_gbs,
                                        "frac": host_achieved / host_gbs},
-                         "avg_launch_ms": kern_ms},
+                         "avg_launch_ms": kern_ms,
+                         "scope": "one launch is a whole layer step (scoring, top-k and page management, "
+                                  "retrieval, attention, combine); the host link idles while the first units "
+                                  "are scored and managed and after the last retrieved page lands"},
             "host_link_peaks_gbs": links,
             "combined_roofline": {**roofline_terms(w, d, ms, hbm_gbs, host_gbs, K),
                                   "hbm_gbs": hbm_gbs, "host_link_gbs": host_gbs,
